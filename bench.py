@@ -1,0 +1,385 @@
+"""Benchmark: the BitNet-2B decode sweep through the exact Q1_0 . Q8_0 GEMV on GB300.
+
+One step = one decode token's pass over all 210 weight matrices of a 30-layer BitNet-2B stack
+(4 x 2560x2560, 2 x 6912x2560, 1 x 2560x6912 per layer; 334,540,800 bytes of Q1_0 weights,
+resident in HBM) with one grouped launch.  The headline metric is weight GB/s; the JSON line also
+carries the roofline of the kernel, the CPU oracle's throughput, an end-to-end number through the
+public API with host buffers, clocks sampled during the timed region, and secondary measurements
+of the other kernels (block-int8 projection, ternary GEMV, prefill).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extras]
+
+Multi-GPU: every rank runs its own replica of the sweep (the path has no exchange step), so
+value = total weight bytes of all ranks / the slowest rank's time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "Q1_0·Q8_0 GEMV weight GB/s (% of GB300 HBM peak); batched prefill GOP/s"
+UNIT = "GB/s"
+WORKLOAD = "bitnet2b_decode_sweep_30x7_q1_0_q8_0"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p.get("hbm_gbs", 6800.0), p.get("bf16_tflops", 1900.0), "measured"
+    except OSError:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def kernel_hash(*names):
+    h = hashlib.sha256()
+    for nm in names:
+        with open(os.path.join(ROOT, "gemm_q1_q8_gb300", "csrc", nm), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(profile: str, khash: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", profile)
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_hash") != khash:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def time_steps(fn, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+# ----------------------------------------------------------------------------- our arm
+def build_sweep(gq, torch, dev):
+    items, acts_host, ys = [], [], []
+    for rows, n, w, a in wl.bitnet_sweep(seed=1):
+        packed = gq.q1_0_pack(torch.from_numpy(w).to(dev), rows, n)
+        act = torch.from_numpy(a).to(dev)
+        y = torch.empty(rows, dtype=torch.float32, device=dev)
+        items.append((packed, act, y, rows, n))
+        acts_host.append(a)
+    torch.cuda.synchronize()
+    return items, acts_host
+
+
+def extras(gq, torch, dev, hbm_peak, bf16_peak):
+    """Secondary kernels, each timed alone with CUDA events (not part of the headline step)."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    # block_q8_matmul_nt 49152 x 960 at m = 1, 4, 16: 4 rotating weight copies (4 x 53 MB > L2)
+    n, k = 49152, 960
+    copies = []
+    for c in range(4):
+        x, q, s = wl.block_q8_inputs(wl.Rng(20 + c), 16, k, n)
+        copies.append((torch.from_numpy(x).to(dev), torch.from_numpy(q.view(np.int32)).to(dev),
+                       torch.from_numpy(s).to(dev)))
+    for m in (1, 4, 16):
+        ys = [torch.empty((m, n), dtype=torch.float32, device=dev) for _ in copies]
+        it = [0]
+        xs = [c[0][:m].contiguous() for c in copies]
+
+        def g():
+            i = it[0] % 4
+            it[0] += 1
+            gq.block_q8_matmul_nt(xs[i], copies[i][1], copies[i][2], out=ys[i])
+        t = time_steps(g, 40, 5, stream) / 40
+        wbytes = n * k + n * (k // 32) * 4
+        flops = 2.0 * m * n * k + 2.0 * m * n * (k // 32)
+        out[f"block_q8_m{m}"] = {"us": t * 1e6, "weight_GBps": wbytes / t / 1e9,
+                                 "hbm_frac": wbytes / t / 1e9 / hbm_peak, "GFLOPs": flops / t / 1e9}
+    del copies
+    # ternary 14336 x 4096, batch 1, 4, 16: 8 rotating copies (8 x 14.7 MB > L2)
+    rows, kk = 14336, 4096
+    planes = []
+    for c in range(8):
+        P, N, _ = wl.ternary_inputs(wl.Rng(40 + c), rows, kk, 1)
+        planes.append((torch.from_numpy(P.view(np.int32)).to(dev), torch.from_numpy(N.view(np.int32)).to(dev)))
+    for b in (1, 4, 16):
+        X = torch.from_numpy(wl.Rng(60 + b).u32(b * kk // 32).reshape(b, kk // 32).view(np.int32)).to(dev)
+        y = torch.empty((b, rows), dtype=torch.int32, device=dev)
+        it = [0]
+
+        def f():
+            i = it[0] % 8
+            it[0] += 1
+            gq.ternary_bitplane_gemv(planes[i][0], planes[i][1], X, out=y)
+        t = time_steps(f, 80, 8, stream) / 80
+        wbytes = 2 * rows * kk // 8
+        out[f"ternary_b{b}"] = {"us": t * 1e6, "weight_GBps": wbytes / t / 1e9, "hbm_frac": wbytes / t / 1e9 / hbm_peak,
+                                "Gpopc_per_s": rows * (kk // 32) * (b + 2) / t / 1e9}
+    del planes
+    # prefill M=512, K=4096, N=14336: quantize + GEMM (LUT4; MMA when available)
+    M, K, N = 512, 4096, 14336
+    signs, ws, x = wl.prefill_inputs(wl.Rng(4), M, K, N)
+    ts = torch.from_numpy(signs.view(np.int32)).to(dev)
+    tw = torch.from_numpy(ws).to(dev)
+    tx = torch.from_numpy(x).to(dev)
+    d, q, op = gq.quantize_q8_0(tx, mma_operand=True)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    tq = time_steps(lambda: gq.quantize_q8_0(tx, mma_operand=True), 20, 3, stream) / 20
+    ops = 2.0 * M * N * K
+    res = {"quantize_us": tq * 1e6}
+    for name, path in (("lut4", gq.PATH_LUT4), ("mma", gq.PATH_MMA)):
+        try:
+            t = time_steps(lambda: gq.q1s32_q8_gemm(ts, tw, d, q, op, path=path, out=y), 5, 2, stream) / 5
+            res[f"{name}_us"] = t * 1e6
+            res[f"{name}_GOPs"] = ops / t / 1e9
+        except gq.GQError as e:
+            res[f"{name}"] = f"unavailable: {e}"
+    out["prefill_512x4096x14336"] = res
+    return out
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import gemm_q1_q8_gb300 as gq
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    hbm_peak, bf16_peak, peak_src = peaks()
+    items, acts_host = build_sweep(gq, torch, dev)
+    group = gq.GroupedGemv(items, device=dev)
+    wbytes = sum(r * (n // 128) * 18 for _, _, _, r, n in items)
+    abytes = sum((n // 32) * 34 for _, _, _, r, n in items)
+    ybytes = sum(4 * r for _, _, _, r, n in items)
+    rows_total = sum(r for _, _, _, r, n in items)
+    stream = torch.cuda.current_stream()
+
+    # --- device-resident timing (the headline): one grouped launch per step
+    for _ in range(args.warmup):
+        group()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    t = time_steps(group, args.steps, 0, stream)
+    clk = clocks.stop()
+    if dist:
+        tt = torch.tensor([t], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    per_launch = t / args.steps
+    value = world * wbytes * args.steps / t / 1e9
+    achieved = (wbytes + abytes + ybytes) / per_launch / 1e9
+
+    # --- end to end through the public API with host buffers: activations H2D from pinned memory,
+    #     the grouped launch, outputs D2H into pinned memory, every step
+    act_pin = [torch.from_numpy(a).pin_memory() for a in acts_host]
+    y_pin = [torch.empty(r, dtype=torch.float32).pin_memory() for _, _, _, r, _ in items]
+
+    def e2e_step():
+        for (packed, act, y, r, n), h in zip(items, act_pin):
+            act.copy_(h, non_blocking=True)
+        group()
+        for (packed, act, y, r, n), h in zip(items, y_pin):
+            h.copy_(y, non_blocking=True)
+        stream.synchronize()
+    for _ in range(args.warmup):
+        e2e_step()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    te = time.perf_counter() - t0
+    if dist:
+        tt = torch.tensor([te], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        te = float(tt.item())
+    e2e_value = world * wbytes * args.steps / te / 1e9
+
+    khash = kernel_hash("q1.cu", "gq_internal.cuh")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u1xi8->f32 (int dot, f32 scale chain)",
+        "data": "synthetic (seeded splitmix64; shapes and distributions of the workload; no checkpoint)",
+        "config": {"workload": WORKLOAD, "matrices": len(items), "weight_bytes_per_token": wbytes,
+                   "rows_per_token": rows_total, "batch": 1, "parallelism": f"replicas x{world}",
+                   "l2": "no flush: 334.5 MB of weights per step > 129 MB L2"},
+        "rows_per_s": round(world * rows_total * args.steps / t, 1),
+        "tok_per_s_equiv": round(world * args.steps / t, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peak_src} (hbm_gbs, copy)",
+                     "traffic": recorded_traffic("gemv_bitnet_sweep.traffic.json", khash),
+                     "algorithmic_bytes_per_launch": wbytes + abytes + ybytes, "kernel_source_hash": khash},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": abytes, "d2h_bytes_per_step": ybytes},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    if rank == 0 and not args.no_extras:
+        line["kernels"] = extras(gq, torch, dev, hbm_peak, bf16_peak)
+    if gq.device_error() != 0:
+        line["device_error"] = True
+    return line
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_sample(budget_s: float):
+    """Runs the CPU oracle over matrices of the sweep (cycled) until ~budget_s has passed;
+    returns (weight bytes, seconds, sample description)."""
+    import oracle
+    oracle.lib()
+    mats = []
+    for idx, (rows, n, w, a) in enumerate(wl.bitnet_sweep(seed=1, layers=1)):
+        mats.append((rows, n, w, a))
+    done_bytes, t0, used = 0, time.perf_counter(), 0
+    while True:
+        rows, n, w, a = mats[used % len(mats)]
+        oracle.q1_q8_gemv(w, a, rows, n)
+        done_bytes += rows * (n // 128) * 18
+        used += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return done_bytes, el, f"{used} matrices of the first layer (shapes cycled), single thread"
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    b, s, desc = oracle_sample(budget_s)
+    return {"value": round(b / s / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
+            "seconds": round(s, 2)}
+
+
+def run_reference(args):
+    for _ in range(args.warmup):
+        oracle_sample(0.3)
+    total_b, total_s, desc = 0, 0.0, ""
+    for _ in range(args.steps):
+        b, s, desc = oracle_sample(args.ref_step_seconds)
+        total_b += b
+        total_s += s
+    value = total_b / total_s / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u1xi8->f32",
+        "data": "synthetic (seeded splitmix64)",
+        "config": {"workload": WORKLOAD, "sample_per_step": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    line = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,251 @@
+"""gemm_q1_q8_gb300 -- Python binding of libgq (low-bit block-quantized GEMV/GEMM for GB300).
+
+Argument marshalling only: every function checks the torch tensors it is given (device, dtype,
+contiguity, size), allocates outputs with torch, and calls the C ABI (include/gq.h) on the
+current CUDA stream.  Every step of the computation runs in the library's kernels; there is no
+CPU or PyTorch fallback, and a missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "lib", "GQError", "PATH_AUTO", "PATH_DP4A", "PATH_LUT4", "PATH_MMA",
+    "q1_0_packed_bytes", "q1_0_pack", "q1_q8_gemv", "GroupedGemv", "q1_q8_gemm",
+    "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm",
+    "device_error", "version",
+]
+
+PATH_AUTO, PATH_DP4A, PATH_LUT4, PATH_MMA = 0, 1, 2, 3
+_LIB = None
+
+
+class GQError(RuntimeError):
+    pass
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [("packed_w", ctypes.c_void_p), ("act", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("rows", ctypes.c_int), ("n", ctypes.c_int),
+                ("tile_begin", ctypes.c_int), ("reserved", ctypes.c_int)]
+
+
+def lib():
+    """The loaded libgq.so.  Raises if it has not been built (``__graft_entry__.build()``)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise GQError(f"libgq.so is not built ({path}); run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        sig = {
+            "gq_version": (ctypes.c_char_p, []),
+            "gq_status_string": (ctypes.c_char_p, [I]),
+            "gq_last_cuda_error": (I, []),
+            "gq_device_error": (I, []),
+            "gq_q1_0_packed_bytes": (S, [I, I]),
+            "gq_q1_0_pack": (I, [P, I, I, P, P]),
+            "gq_q1_q8_workspace_bytes": (S, [I]),
+            "q1_q8_gemv": (I, [P, P, P, I, I, P, P]),
+            "gq_gemv_group_plan": (I, [P, I, P]),
+            "q1_q8_gemv_grouped": (I, [P, I, I, P, P]),
+            "q1_q8_gemm": (I, [P, P, P, I, I, I, I, P]),
+            "block_q8_matmul_nt": (I, [P, P, P, P, I, I, I, P]),
+            "ternary_bitplane_gemv": (I, [P, P, P, P, I, I, I, P]),
+            "gq_quantize_q8_0": (I, [P, I, I, P, P, P, P]),
+            "q1s32_q8_gemm": (I, [P, P, P, P, P, P, I, I, I, I, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def version() -> str:
+    return lib().gq_version().decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        L = lib()
+        msg = L.gq_status_string(status).decode()
+        extra = f" (cudaError {L.gq_last_cuda_error()})" if status == 4 else ""
+        raise GQError(f"{what}: {msg}{extra}")
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t: torch.Tensor, dtype, numel: int, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise GQError(f"{name}: expected a CUDA tensor")
+    if t.dtype != dtype:
+        raise GQError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise GQError(f"{name}: must be contiguous")
+    if t.numel() != numel:
+        raise GQError(f"{name}: expected {numel} elements, got {t.numel()}")
+
+
+def device_error() -> int:
+    """Reads and clears the library's device-side error word (synchronizes the device)."""
+    return lib().gq_device_error()
+
+
+# ----------------------------------------------------------------------------- Q1_0 x Q8_0
+
+def q1_0_packed_bytes(rows: int, n: int) -> int:
+    return lib().gq_q1_0_packed_bytes(rows, n)
+
+
+def q1_0_pack(raw: torch.Tensor, rows: int, n: int) -> torch.Tensor:
+    """Repack Q1_0 AoS bytes (uint8, rows*(n/128)*18) into the resident layout."""
+    _need(raw, torch.uint8, rows * (n // 128) * 18 if n % 128 == 0 else -1, "raw")
+    nbytes = q1_0_packed_bytes(rows, n)
+    if nbytes == 0:
+        raise GQError("q1_0_pack: invalid shape")
+    packed = torch.empty(nbytes, dtype=torch.uint8, device=raw.device)
+    _check(lib().gq_q1_0_pack(_ptr(raw), rows, n, _ptr(packed), _stream()), "gq_q1_0_pack")
+    return packed
+
+
+def workspace_bytes(n: int) -> int:
+    return lib().gq_q1_q8_workspace_bytes(n)
+
+
+def q1_q8_gemv(packed: torch.Tensor, act: torch.Tensor, rows: int, n: int, out: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None):
+    """y[r] for a packed rows x n Q1_0 matrix and one Q8_0 vector (uint8, n/32*34 bytes)."""
+    _need(act, torch.uint8, (n // 32) * 34, "act")
+    _need(packed, torch.uint8, q1_0_packed_bytes(rows, n), "packed")
+    y = torch.empty(rows, dtype=torch.float32, device=act.device) if out is None else out
+    _need(y, torch.float32, rows, "out")
+    ws = torch.empty(workspace_bytes(n), dtype=torch.uint8, device=act.device) if workspace is None else workspace
+    _need(ws, torch.uint8, workspace_bytes(n), "workspace")
+    _check(lib().q1_q8_gemv(_ptr(packed), _ptr(act), _ptr(y), rows, n, _ptr(ws), _stream()), "q1_q8_gemv")
+    return y
+
+
+class GroupedGemv:
+    """A planned grouped GEMV: one launch over many (packed weights, activation, output) triples."""
+
+    def __init__(self, items, device="cuda"):
+        """items: sequence of (packed, act, y, rows, n) with CUDA tensors (kept alive here)."""
+        self._keep = []
+        host = (_Desc * len(items))()
+        offs, total = [], 0
+        for rows, n in ((it[3], it[4]) for it in items):
+            offs.append(total)
+            total += (workspace_bytes(n) + 255) // 256 * 256
+        self.workspace = torch.empty(total + 256, dtype=torch.uint8, device=device)
+        self.counter = self.workspace[total:total + 16].view(torch.int32)
+        base = self.workspace.data_ptr()
+        for i, (packed, act, y, rows, n) in enumerate(items):
+            _need(act, torch.uint8, (n // 32) * 34, f"act[{i}]")
+            _need(packed, torch.uint8, q1_0_packed_bytes(rows, n), f"packed[{i}]")
+            _need(y, torch.float32, rows, f"y[{i}]")
+            host[i] = _Desc(packed.data_ptr(), act.data_ptr(), y.data_ptr(), base + offs[i], rows, n, 0, 0)
+            self._keep += [packed, act, y]
+        tiles = ctypes.c_int(0)
+        _check(lib().gq_gemv_group_plan(ctypes.cast(host, ctypes.c_void_p), len(items), ctypes.byref(tiles)),
+               "gq_gemv_group_plan")
+        raw = bytes(host)
+        self.descs = torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(device)
+        self.count, self.tiles = len(items), tiles.value
+
+    def __call__(self):
+        _check(lib().q1_q8_gemv_grouped(_ptr(self.descs), self.count, self.tiles, _ptr(self.counter), _stream()),
+               "q1_q8_gemv_grouped")
+
+
+def q1_q8_gemm(packed: torch.Tensor, act: torch.Tensor, rows: int, n: int, cols: int, path: int = PATH_AUTO,
+               out: torch.Tensor | None = None):
+    """O[c, r] ([cols, rows] f32) for `cols` Q8_0 vectors (uint8, cols*(n/32)*34 bytes)."""
+    _need(act, torch.uint8, cols * (n // 32) * 34, "act")
+    _need(packed, torch.uint8, q1_0_packed_bytes(rows, n), "packed")
+    y = torch.empty((cols, rows), dtype=torch.float32, device=act.device) if out is None else out
+    _need(y, torch.float32, rows * cols, "out")
+    _check(lib().q1_q8_gemm(_ptr(packed), _ptr(act), _ptr(y), rows, n, cols, path, _stream()), "q1_q8_gemm")
+    return y
+
+
+# ----------------------------------------------------------------------------- block_q8_matmul_nt
+
+def block_q8_matmul_nt(x: torch.Tensor, quants: torch.Tensor, scales: torch.Tensor, out: torch.Tensor | None = None):
+    """y = x . w^T: x [m, k] f32, quants int32/uint32 words (n*k/4), scales [n, k/32] f32."""
+    m, k = x.shape
+    n = scales.shape[0]
+    _need(x, torch.float32, m * k, "x")
+    if quants.dtype not in (torch.int32, torch.uint32):
+        raise GQError("quants: expected int32 or uint32 words")
+    _need(quants, quants.dtype, n * k // 4, "quants")
+    _need(scales, torch.float32, n * (k // 32), "scales")
+    y = torch.empty((m, n), dtype=torch.float32, device=x.device) if out is None else out
+    _need(y, torch.float32, m * n, "out")
+    _check(lib().block_q8_matmul_nt(_ptr(x), _ptr(quants), _ptr(scales), _ptr(y), m, k, n, _stream()),
+           "block_q8_matmul_nt")
+    return y
+
+
+# ----------------------------------------------------------------------------- ternary
+
+def ternary_bitplane_gemv(P: torch.Tensor, N: torch.Tensor, X: torch.Tensor, out: torch.Tensor | None = None):
+    """y [batch, rows] int32 for P, N [rows, k/32] and X [batch, k/32] bitplanes (int32/uint32)."""
+    rows, kw = P.shape
+    batch = X.shape[0]
+    for t, nm, cnt in ((P, "P", rows * kw), (N, "N", rows * kw), (X, "X", batch * kw)):
+        if t.dtype not in (torch.int32, torch.uint32):
+            raise GQError(f"{nm}: expected int32 or uint32 words")
+        _need(t, t.dtype, cnt, nm)
+    y = torch.empty((batch, rows), dtype=torch.int32, device=P.device) if out is None else out
+    _need(y, torch.int32, batch * rows, "out")
+    _check(lib().ternary_bitplane_gemv(_ptr(P), _ptr(N), _ptr(X), _ptr(y), rows, kw * 32, batch, _stream()),
+           "ternary_bitplane_gemv")
+    return y
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def quantize_q8_0(x: torch.Tensor, mma_operand: bool = False):
+    """(d [m, k/32] f16 bits as int16, q [m, k] int8, operand [m, k] f16 bits or None)."""
+    m, k = x.shape
+    _need(x, torch.float32, m * k, "x")
+    d = torch.empty((m, k // 32), dtype=torch.int16, device=x.device)
+    q = torch.empty((m, k), dtype=torch.int8, device=x.device)
+    op = torch.empty((m, k), dtype=torch.int16, device=x.device) if mma_operand else None
+    _check(lib().gq_quantize_q8_0(_ptr(x), m, k, _ptr(d), _ptr(q), _ptr(op), _stream()), "gq_quantize_q8_0")
+    return d, q, op
+
+
+def q1s32_q8_gemm(signs: torch.Tensor, wscale: torch.Tensor, xd: torch.Tensor, xq: torch.Tensor,
+                  xq_mma: torch.Tensor | None = None, path: int = PATH_AUTO, out: torch.Tensor | None = None):
+    """y [M, N] f32 for 1-bit weights (signs [N, K/32] words, wscale [N, K/32] f32) and Q8_0
+    activations (xd [M, K/32] f16 bits, xq [M, K] int8, optional MMA operand [M, K])."""
+    M, K = xq.shape
+    N = signs.shape[0]
+    if signs.dtype not in (torch.int32, torch.uint32):
+        raise GQError("signs: expected int32 or uint32 words")
+    _need(signs, signs.dtype, N * (K // 32), "signs")
+    _need(wscale, torch.float32, N * (K // 32), "wscale")
+    _need(xd, torch.int16, M * (K // 32), "xd")
+    _need(xq, torch.int8, M * K, "xq")
+    if xq_mma is not None:
+        _need(xq_mma, torch.int16, M * K, "xq_mma")
+    y = torch.empty((M, N), dtype=torch.float32, device=xq.device) if out is None else out
+    _need(y, torch.float32, M * N, "out")
+    _check(lib().q1s32_q8_gemm(_ptr(signs), _ptr(wscale), _ptr(xd), _ptr(xq), _ptr(xq_mma), _ptr(y), M, N, K,
+                               path, _stream()), "q1s32_q8_gemm")
+    return y

@@ -1,0 +1,606 @@
+// Q1_0 weights x Q8_0 activations on sm_103a: one-time repack, decode GEMV (single matrix and
+// grouped layer sweep) and the token-tiled GEMM (DP4A and LUT4 paths).
+//
+// Arithmetic (browseml-gpu.js, header comment and Q1_DOT_WGSL / Q1_MM_WGSL / Q1_MM4_WGSL): per
+// row, per block i of 128 weights (f16 d0 + 128 sign bits), per sub-block k of 32 weights
+// (Q8_0 block 4i+k: f16 d1 + 32 int8) and lane l (weights 4l..4l+3):
+//   s = sum(bit ? q : -q) with the negate wrapping as int8;  p = d1*s (exact);
+//   ab[l] = p (k = 0) or ab[l] + p;  acc[l] = fma(d0, ab[l], acc[l]);
+//   y = ((a0+a4)+(a2+a6)) + ((a1+a5)+(a3+a7)).
+//
+// How the integer lane sums are formed here (the same values, fewer instructions):
+//  * -128 quants: a -128 term is -128 whatever the bit, so with q~ = q except -128 -> 0 and
+//    C = sum q~ + 128*count(-128),  s = 2*D - C  where D = sum over set bits of q~.
+//  * The repack stores each 32-bit sign word bit-transposed: packed bit 8c+l = weight 4l+c.
+//    Then (w & (0x01010101 << l)) holds lane l's four bits, one per byte, each worth 2^l, and
+//    a single dp4a against the activation word l (bytes q~_{4l..4l+3}) gives 2^l * D.
+//  * The dp4a accumulator starts at bits(1.5*2^23) - (sigma/2)*C, so its result read as f32 is
+//    exactly 1.5*2^23 + (sigma/2)*s (sigma = 2^max(l,1), the lane's mask weight; lane 0's bits
+//    are shifted up by one).  Subtracting 1.5*2^23 is exact, and multiplying by d1*2/sigma
+//    gives exactly d1*s, so ab = fma(d1*2/sigma, t, ab) is the pages' rounded add.
+//  * Pairs of lanes run through the packed f32x2 add/mul/fma (two IEEE operations each).
+#include "gq_internal.cuh"
+
+namespace gq {
+
+namespace {
+
+constexpr int kRPT = 4;          // rows per lane in the GEMV (a warp covers one 128-row tile)
+constexpr uint32_t kMagicBits = 0x4B400000u;   // 1.5 * 2^23: ulp 1 in [2^23, 2^24)
+constexpr float kMagic = 12582912.0f;
+constexpr int kConstWords = 24;  // per 32-activation sub-block: 8 quant words, 8 seeds, 8 scales
+
+// packed bit 8c + l <- page bit 4l + c (c = 0..3, l = 0..7)
+__device__ __forceinline__ uint32_t transpose_signs(uint32_t w) {
+    uint32_t out = 0;
+#pragma unroll
+    for (int l = 0; l < 8; ++l)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) out |= ((w >> (4 * l + c)) & 1u) << (8 * c + l);
+    return out;
+}
+
+__global__ void q1_pack_kernel(const uint8_t* __restrict__ raw, int rows, int nb,
+                               uint8_t* __restrict__ packed, long long total) {
+    long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int rr = static_cast<int>(idx % kTileRows);
+    const long long tb = idx / kTileRows;          // tile * nb + block
+    const int i = static_cast<int>(tb % nb);
+    const long long tile = tb / nb;
+    const long long row = tile * kTileRows + rr;
+    uint8_t* chunk = packed + static_cast<size_t>(tb) * kChunkBytes;
+    uint4 bits = make_uint4(0u, 0u, 0u, 0u);
+    uint16_t d0 = 0;
+    if (row < rows) {
+        const uint8_t* b = raw + (static_cast<size_t>(row) * nb + i) * 18;
+        d0 = static_cast<uint16_t>(b[0] | (b[1] << 8));
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = static_cast<uint32_t>(b[2 + 4 * k]) | (static_cast<uint32_t>(b[3 + 4 * k]) << 8) |
+                   (static_cast<uint32_t>(b[4 + 4 * k]) << 16) | (static_cast<uint32_t>(b[5 + 4 * k]) << 24);
+        bits = make_uint4(transpose_signs(w[0]), transpose_signs(w[1]), transpose_signs(w[2]),
+                          transpose_signs(w[3]));
+    }
+    reinterpret_cast<uint4*>(chunk)[rr] = bits;
+    reinterpret_cast<uint16_t*>(chunk + kTileRows * 16)[rr] = d0;
+}
+
+// Activation constants of one (sub-block, lane l) from its f16 d1 bits and its four quants
+// (little-endian word): the quant word with -128 zeroed, the dp4a seed and d1 * 2/sigma.
+__device__ __forceinline__ void lane_consts(uint32_t d1bits, uint32_t qw, int l, uint32_t& qt, uint32_t& seed,
+                                            float& d1s) {
+    const float d1 = f16_to_f32(d1bits);
+    int C = 0;
+    uint32_t t = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int q = static_cast<int>(static_cast<int8_t>((qw >> (8 * c)) & 0xFFu));
+        if (q == -128) {
+            C += 128;
+        } else {
+            C += q;
+            t |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * c);
+        }
+    }
+    const int half_sigma = (l <= 1) ? 1 : (1 << (l - 1));
+    qt = t;
+    seed = kMagicBits - static_cast<uint32_t>(half_sigma * C);
+    d1s = __fmul_rn(d1, 1.0f / static_cast<float>(half_sigma));   // power of two: exact
+}
+
+// The same from a 34-byte Q8_0 block in memory (2-byte aligned).
+__device__ __forceinline__ void act_lane_consts(const uint16_t* blk, int l, uint32_t& qt, uint32_t& seed,
+                                                float& d1s) {
+    lane_consts(blk[0], static_cast<uint32_t>(blk[1 + 2 * l]) | (static_cast<uint32_t>(blk[2 + 2 * l]) << 16), l,
+                qt, seed, d1s);
+}
+
+// The eight lane values t_l = (sigma_l/2) * s_l of one 32-weight sub-block word (transposed
+// layout), as four f32 pairs (lanes 0-1, 2-3, 4-5, 6-7).
+__device__ __forceinline__ void lane_values(uint32_t w, const uint4& q0, const uint4& q1, const uint4& s0,
+                                            const uint4& s1, float2 t[4]) {
+    const int r0 = dp4a_us((w << 1) & 0x02020202u, q0.x, static_cast<int>(s0.x));
+    const int r1 = dp4a_us(w & 0x02020202u, q0.y, static_cast<int>(s0.y));
+    const int r2 = dp4a_us(w & 0x04040404u, q0.z, static_cast<int>(s0.z));
+    const int r3 = dp4a_us(w & 0x08080808u, q0.w, static_cast<int>(s0.w));
+    const int r4 = dp4a_us(w & 0x10101010u, q1.x, static_cast<int>(s1.x));
+    const int r5 = dp4a_us(w & 0x20202020u, q1.y, static_cast<int>(s1.y));
+    const int r6 = dp4a_us(w & 0x40404040u, q1.z, static_cast<int>(s1.z));
+    const int r7 = dp4a_us(w & 0x80808080u, q1.w, static_cast<int>(s1.w));
+    const float2 nm = make_float2(-kMagic, -kMagic);
+    t[0] = fadd2(make_float2(__int_as_float(r0), __int_as_float(r1)), nm);
+    t[1] = fadd2(make_float2(__int_as_float(r2), __int_as_float(r3)), nm);
+    t[2] = fadd2(make_float2(__int_as_float(r4), __int_as_float(r5)), nm);
+    t[3] = fadd2(make_float2(__int_as_float(r6), __int_as_float(r7)), nm);
+}
+
+__device__ __forceinline__ float final_reduce(const float2 acc[4]) {
+    // acc[0] = (a0,a1), acc[1] = (a2,a3), acc[2] = (a4,a5), acc[3] = (a6,a7)
+    const float2 s0415 = fadd2(acc[0], acc[2]);     // (a0+a4, a1+a5)
+    const float2 s2637 = fadd2(acc[1], acc[3]);     // (a2+a6, a3+a7)
+    const float2 lohi = fadd2(s0415, s2637);        // ((a0+a4)+(a2+a6), (a1+a5)+(a3+a7))
+    return __fadd_rn(lohi.x, lohi.y);
+}
+
+// --------------------------------------------------------------------------------------------
+// Decode GEMV, in two launches.
+//  1. act_prep_kernel builds each activation's constants once per call into the caller's
+//     workspace (per 32-activation sub-block: 8 quant words, 8 seeds, 8 scales = 96 bytes) and
+//     zeroes the unit counter.
+//  2. q1_gemv_kernel: persistent warps.  A unit is 32*RPT rows of one matrix (a 128-row tile or a
+//     part of it); units are handed out through the counter (atomicAdd), largest matrix first, so
+//     the greedy hand-out balances the warps.  Each warp streams its units' (unit, block) chunks --
+//     the unit's sign bits and d0 of the block plus the block's 384 bytes of constants -- through
+//     a private ring of kStages stages: lane 0 refills the stage it has just consumed with the
+//     chunk kStages ahead (grabbing the next unit when the current one is fully requested), so the
+//     copies run ahead across unit boundaries.  The unit of each chunk run travels through a small
+//     per-warp queue; the end of the work is a full-barrier phase completed without data.  Every
+//     wait is bounded, and a warp that gives up first lets its copies in flight land.
+// --------------------------------------------------------------------------------------------
+#ifndef GQ_GEMV_RPT
+#define GQ_GEMV_RPT 4
+#endif
+constexpr int kGemvRPT = GQ_GEMV_RPT;                      // rows per lane: a unit is 32*RPT rows
+constexpr int kUnitsPerTile = 4 / kGemvRPT;                // a 128-row tile holds 4/RPT units
+constexpr int kGemvWarps = (kGemvRPT == 4) ? 16 : 20;      // 4 or 5 warps per SMSP
+constexpr int kStages = (kGemvRPT == 4) ? 4 : 6;
+constexpr int kCstBytes = 4 * kConstWords * 4;            // 384: constants of one block
+constexpr int kUnitBits = 32 * kGemvRPT * 16;              // sign bits of one unit and block
+constexpr int kUnitD0 = 32 * kGemvRPT * 2;                 // d0 of one unit and block
+constexpr int kStageBytes = kUnitBits + kUnitD0 + kCstBytes;
+constexpr int kCachedDescs = 2048;                          // tile_begin cached in smem up to this
+constexpr int kUnitQueue = 16;                              // > kStages: units requested ahead
+
+struct Fetch {                 // lane 0's cursor over the chunks still to request
+    const uint8_t* base;       // current unit's tile, first chunk
+    const uint8_t* cst;        // its matrix's constants
+    int nb, part, blk, qi;     // blocks, unit part, next block, queue slot of the next unit
+    int issued, live;
+};
+
+struct __align__(16) WarpSmem {
+    uint8_t ring[kStages][kStageBytes];
+    uint64_t full[kStages];
+    int units[kUnitQueue];
+    Fetch f;
+};
+
+struct TileInfo {
+    const uint8_t* base;   // first chunk of the tile
+    const uint8_t* cst;    // the matrix's activation constants (workspace)
+    float* y;
+    int rows;              // rows of the matrix
+    int nb;                // blocks per row
+    int row0;              // first row of the tile
+};
+
+// Descriptor of tile `tile`: binary search of tile_begin (shared-memory copy when the group is
+// small enough, else global), then one read of the descriptor.
+__device__ __forceinline__ TileInfo tile_info(const gq_gemv_desc& single, const gq_gemv_desc* __restrict__ descs,
+                                              int count, const int* s_tb, int tile) {
+    gq_gemv_desc d;
+    if (count == 0) {
+        d = single;
+    } else {
+        int lo = 0, hi = count - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            const int tb = (count <= kCachedDescs) ? s_tb[mid] : descs[mid].tile_begin;
+            if (tb <= tile) lo = mid;
+            else hi = mid - 1;
+        }
+        d = descs[lo];
+    }
+    TileInfo t;
+    const int lt = tile - d.tile_begin;
+    t.nb = d.n / 128;
+    t.base = static_cast<const uint8_t*>(d.packed_w) + static_cast<size_t>(lt) * t.nb * kChunkBytes;
+    t.cst = static_cast<const uint8_t*>(d.workspace);
+    t.y = d.y;
+    t.rows = d.rows;
+    t.row0 = lt * kTileRows;
+    return t;
+}
+
+__global__ void __launch_bounds__(256)
+act_prep_kernel(gq_gemv_desc single, const gq_gemv_desc* __restrict__ descs, int count, int* counter) {
+    const gq_gemv_desc d = (count == 0) ? single : descs[blockIdx.y];
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *counter = 0;
+    const int items = (d.n / 32) * 8;
+    const uint8_t* act = static_cast<const uint8_t*>(d.act);
+    uint32_t* ws = static_cast<uint32_t*>(d.workspace);
+    for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < items; it += gridDim.x * blockDim.x) {
+        const int kg = it >> 3, l = it & 7;
+        uint32_t qt, seed;
+        float d1s;
+        act_lane_consts(reinterpret_cast<const uint16_t*>(act + static_cast<size_t>(kg) * 34), l, qt, seed, d1s);
+        ws[kg * kConstWords + l] = qt;
+        ws[kg * kConstWords + 8 + l] = seed;
+        ws[kg * kConstWords + 16 + l] = __float_as_uint(d1s);
+    }
+}
+
+// Lane 0: request the next chunk of the warp's stream into stage `s` (or, once the units have
+// run out, complete that stage's next phase without data after posting -1).
+__device__ __forceinline__ void fetch_next(WarpSmem& ws, int s, const gq_gemv_desc& single,
+                                           const gq_gemv_desc* __restrict__ descs, int count, const int* s_tb,
+                                           int total_units, int* counter) {
+    Fetch& F = ws.f;
+    if (!F.live) return;
+    if (F.blk == F.nb) {                       // current unit fully requested: take the next one
+        const int unit = atomicAdd(counter, 1);
+        if (unit >= total_units) {
+            ws.units[F.qi % kUnitQueue] = -1;
+            mbar_arrive(&ws.full[s]);
+            ++F.issued;
+            F.live = 0;
+            return;
+        }
+        ws.units[F.qi % kUnitQueue] = unit;
+        ++F.qi;
+        const TileInfo t = tile_info(single, descs, count, s_tb, unit / kUnitsPerTile);
+        F.base = t.base;
+        F.cst = t.cst;
+        F.nb = t.nb;
+        F.part = unit % kUnitsPerTile;
+        F.blk = 0;
+    }
+    const uint8_t* ch = F.base + static_cast<size_t>(F.blk) * kChunkBytes;
+    mbar_arrive_expect_tx(&ws.full[s], kStageBytes);
+    if (kUnitsPerTile == 1) {
+        bulk_g2s(ws.ring[s], ch, kUnitBits + kUnitD0, &ws.full[s]);
+    } else {
+        bulk_g2s(ws.ring[s], ch + F.part * kUnitBits, kUnitBits, &ws.full[s]);
+        bulk_g2s(ws.ring[s] + kUnitBits, ch + kTileRows * 16 + F.part * kUnitD0, kUnitD0, &ws.full[s]);
+    }
+    bulk_g2s(ws.ring[s] + kUnitBits + kUnitD0, F.cst + static_cast<size_t>(F.blk) * kCstBytes, kCstBytes, &ws.full[s]);
+    ++F.blk;
+    ++F.issued;
+}
+
+__global__ void __launch_bounds__(kGemvWarps * 32, 1)
+q1_gemv_kernel(gq_gemv_desc single, const gq_gemv_desc* __restrict__ descs, int count, int total_tiles,
+               int* counter) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem)[warp];
+    int* s_tb = reinterpret_cast<int*>(smem + sizeof(WarpSmem) * kGemvWarps);
+    if (count > 0 && count <= kCachedDescs)
+        for (int i = threadIdx.x; i < count; i += blockDim.x) s_tb[i] = descs[i].tile_begin;
+    __syncthreads();
+    const int total_units = total_tiles * kUnitsPerTile;
+
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&ws.full[s], 1);
+        fence_barrier_init();
+        ws.f = Fetch{nullptr, nullptr, 0, 0, 0, 0, 0, 1};
+        for (int s = 0; s < kStages; ++s) fetch_next(ws, s, single, descs, count, s_tb, total_units, counter);
+    }
+    __syncwarp();
+
+    int chunk = 0;
+    auto wait_chunk = [&](int c) -> bool {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&ws.full[c % kStages], static_cast<uint32_t>(c / kStages) & 1u));
+        if (!ok && lane == 0) {
+            // let the copies still in flight land before this warp's shared memory is released
+            report_error(kErrWaitTimeout);
+            for (int cc = c + 1; cc < ws.f.issued; ++cc)
+                if (!mbar_wait(&ws.full[cc % kStages], static_cast<uint32_t>(cc / kStages) & 1u))
+                    report_error(kErrDrainTimeout);
+        }
+        return ok;
+    };
+
+    for (int i = 0;; ++i) {
+        if (!wait_chunk(chunk)) return;        // the unit's first chunk, or the end marker
+        const int unit = ws.units[i % kUnitQueue];
+        if (unit < 0) break;
+        const TileInfo t = tile_info(single, descs, count, s_tb, unit / kUnitsPerTile);
+        const int urow0 = t.row0 + (unit % kUnitsPerTile) * 32 * kGemvRPT;
+
+        float2 acc[kGemvRPT][4];
+#pragma unroll
+        for (int j = 0; j < kGemvRPT; ++j)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) acc[j][p] = make_float2(0.0f, 0.0f);
+
+        for (int blk = 0; blk < t.nb; ++blk, ++chunk) {
+            const int s = chunk % kStages;
+            if (blk > 0 && !wait_chunk(chunk)) return;
+            const uint8_t* stage = ws.ring[s];
+            uint4 wb[kGemvRPT];
+            float d0[kGemvRPT];
+#pragma unroll
+            for (int j = 0; j < kGemvRPT; ++j) {
+                wb[j] = reinterpret_cast<const uint4*>(stage)[lane + 32 * j];
+                d0[j] = f16_to_f32(reinterpret_cast<const uint16_t*>(stage + kUnitBits)[lane + 32 * j]);
+            }
+            const uint4* cst = reinterpret_cast<const uint4*>(stage + kUnitBits + kUnitD0);
+
+            float2 ab[kGemvRPT][4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4* cs4 = cst + 6 * k;
+                const uint4 q0 = cs4[0], q1 = cs4[1], s0 = cs4[2], s1 = cs4[3];
+                const uint4 dd0 = cs4[4], dd1 = cs4[5];
+                const float2 D01 = make_float2(__uint_as_float(dd0.x), __uint_as_float(dd0.y));
+                const float2 D23 = make_float2(__uint_as_float(dd0.z), __uint_as_float(dd0.w));
+                const float2 D45 = make_float2(__uint_as_float(dd1.x), __uint_as_float(dd1.y));
+                const float2 D67 = make_float2(__uint_as_float(dd1.z), __uint_as_float(dd1.w));
+#pragma unroll
+                for (int j = 0; j < kGemvRPT; ++j) {
+                    const uint32_t w = (k == 0) ? wb[j].x : (k == 1) ? wb[j].y : (k == 2) ? wb[j].z : wb[j].w;
+                    float2 tv[4];
+                    lane_values(w, q0, q1, s0, s1, tv);
+                    if (k == 0) {
+                        ab[j][0] = fmul2(D01, tv[0]);
+                        ab[j][1] = fmul2(D23, tv[1]);
+                        ab[j][2] = fmul2(D45, tv[2]);
+                        ab[j][3] = fmul2(D67, tv[3]);
+                    } else {
+                        ab[j][0] = ffma2(D01, tv[0], ab[j][0]);
+                        ab[j][1] = ffma2(D23, tv[1], ab[j][1]);
+                        ab[j][2] = ffma2(D45, tv[2], ab[j][2]);
+                        ab[j][3] = ffma2(D67, tv[3], ab[j][3]);
+                    }
+                }
+            }
+            __syncwarp();                         // every lane has read the stage
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                fetch_next(ws, s, single, descs, count, s_tb, total_units, counter);
+            }
+#pragma unroll
+            for (int j = 0; j < kGemvRPT; ++j) {
+                const float2 dd = make_float2(d0[j], d0[j]);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) acc[j][p] = ffma2(dd, ab[j][p], acc[j][p]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kGemvRPT; ++j) {
+            const int row = urow0 + lane + 32 * j;
+            if (row < t.rows) t.y[row] = final_reduce(acc[j]);
+        }
+    }
+    // the end marker was the last phase requested: nothing is in flight
+}
+
+constexpr size_t kGemvSmem = sizeof(WarpSmem) * kGemvWarps + kCachedDescs * sizeof(int);
+
+// --------------------------------------------------------------------------------------------
+// Token-tiled GEMM ([P1] Q1_MM4_WGSL: each weight word decoded once for T tokens, past the last
+// token the column is clamped, computed and never stored).  One thread block = one 128-row tile
+// (4 warps x 32 rows, one row per lane) x kTok tokens; all blocks of the tile stream through a
+// shared ring; the activation constants (DP4A) or tables (LUT4) of the block's sub-blocks are
+// built per block by the thread block itself.
+// --------------------------------------------------------------------------------------------
+constexpr int kTok = 4;
+constexpr int kGemmStages = 4;
+
+// LUT4: table[t][k][l][nib] = d1 * s(nib) for the 4 activations of lane l, with the nibble's bit
+// c (c = 0..3) the sign bit of weight 4l+c.  p = d1 * s is exact.
+__device__ __forceinline__ void lut_table(const uint16_t* blk, int l, float* table16) {
+    const float d1 = f16_to_f32(blk[0]);
+    const uint32_t qw = static_cast<uint32_t>(blk[1 + 2 * l]) | (static_cast<uint32_t>(blk[2 + 2 * l]) << 16);
+    int pos[4], neg[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int q = static_cast<int>(static_cast<int8_t>((qw >> (8 * c)) & 0xFFu));
+        pos[c] = q;
+        neg[c] = (q == -128) ? -128 : -q;
+    }
+#pragma unroll
+    for (int nib = 0; nib < 16; ++nib) {
+        int s = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s += ((nib >> c) & 1) ? pos[c] : neg[c];
+        table16[nib] = __fmul_rn(d1, static_cast<float>(s));
+    }
+}
+
+// nibble of lane l from a transposed sign word: bits l, 8+l, 16+l, 24+l -> bits 0..3
+__device__ __forceinline__ uint32_t lane_nibble(uint32_t w, int l) {
+    return (((w >> l) & 0x01010101u) * 0x01020408u) >> 24;
+}
+
+template <int kPath>
+__global__ void __launch_bounds__(128)
+q1_gemm_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ act, float* __restrict__ y,
+               int rows, int n, int cols) {
+    __shared__ __align__(128) uint8_t ring[kGemmStages][kChunkBytes];
+    __shared__ uint64_t bars[kGemmStages];
+    // per token and sub-block: DP4A constants (24 words) or LUT4 tables (8 x 16 floats)
+    constexpr int kPerTokK = (kPath == GQ_PATH_LUT4) ? 128 : kConstWords;
+    __shared__ __align__(16) uint32_t tabs[2][kTok][4][kPerTokK];
+
+    const int nb = n / 128;
+    const int tile = blockIdx.x;
+    const int c0 = blockIdx.y * kTok;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rr = warp * 32 + lane;      // row within the tile
+    const uint8_t* tile_base = packed + static_cast<size_t>(tile) * nb * kChunkBytes;
+    const size_t act_bytes = static_cast<size_t>(n / 32) * 34;
+
+    if (tid == 0) {
+        for (int s = 0; s < kGemmStages; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+        const int first = nb < kGemmStages ? nb : kGemmStages;
+        for (int s = 0; s < first; ++s) {
+            mbar_arrive_expect_tx(&bars[s], kChunkBytes);
+            bulk_g2s(ring[s], tile_base + static_cast<size_t>(s) * kChunkBytes, kChunkBytes, &bars[s]);
+        }
+    }
+
+    float2 acc[kTok][4];
+#pragma unroll
+    for (int t = 0; t < kTok; ++t)
+#pragma unroll
+        for (int p = 0; p < 4; ++p) acc[t][p] = make_float2(0.0f, 0.0f);
+
+    for (int i = 0; i < nb; ++i) {
+        const int buf = i & 1;
+        // build this block's per-token data: kTok tokens x 4 sub-blocks x 8 lanes = 128 items
+        {
+            const int t = tid >> 5, k = (tid >> 3) & 3, l = tid & 7;
+            const int c = min(c0 + t, cols - 1);
+            const uint16_t* blk = reinterpret_cast<const uint16_t*>(act + c * act_bytes + static_cast<size_t>(4 * i + k) * 34);
+            if (kPath == GQ_PATH_LUT4) {
+                lut_table(blk, l, reinterpret_cast<float*>(&tabs[buf][t][k][l * 16]));
+            } else {
+                uint32_t qt, seed;
+                float d1s;
+                act_lane_consts(blk, l, qt, seed, d1s);
+                tabs[buf][t][k][l] = qt;
+                tabs[buf][t][k][8 + l] = seed;
+                tabs[buf][t][k][16 + l] = __float_as_uint(d1s);
+            }
+        }
+        __syncthreads();    // tables of block i visible; ring stage of block i-1 fully read
+        const int s = i % kGemmStages;
+        if (tid == 0 && i >= 1 && i - 1 + kGemmStages < nb) {
+            const int sp = (i - 1) % kGemmStages;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[sp], kChunkBytes);
+            bulk_g2s(ring[sp], tile_base + static_cast<size_t>(i - 1 + kGemmStages) * kChunkBytes, kChunkBytes,
+                     &bars[sp]);
+        }
+        const bool ok = __syncthreads_and(mbar_wait(&bars[s], static_cast<uint32_t>(i / kGemmStages) & 1u));
+        if (!ok) {
+            if (tid == 0) {
+                report_error(kErrWaitTimeout);
+                const int last = (i + kGemmStages < nb ? i + kGemmStages : nb);
+                for (int b = i; b < last; ++b)
+                    if (!mbar_wait(&bars[b % kGemmStages], static_cast<uint32_t>(b / kGemmStages) & 1u))
+                        report_error(kErrDrainTimeout);
+            }
+            __syncthreads();
+            return;
+        }
+        const uint4 wb = reinterpret_cast<const uint4*>(ring[s])[rr];
+        const float d0 = f16_to_f32(reinterpret_cast<const uint16_t*>(ring[s] + kTileRows * 16)[rr]);
+        const float2 dd = make_float2(d0, d0);
+
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) {
+            float2 ab[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t w = (k == 0) ? wb.x : (k == 1) ? wb.y : (k == 2) ? wb.z : wb.w;
+                if (kPath == GQ_PATH_LUT4) {
+                    const float* tb = reinterpret_cast<const float*>(&tabs[buf][t][k][0]);
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        const float2 v = make_float2(tb[(2 * p) * 16 + lane_nibble(w, 2 * p)],
+                                                     tb[(2 * p + 1) * 16 + lane_nibble(w, 2 * p + 1)]);
+                        ab[p] = (k == 0) ? v : fadd2(v, ab[p]);
+                    }
+                } else {
+                    const uint4* cs = reinterpret_cast<const uint4*>(&tabs[buf][t][k][0]);
+                    const uint4 q0 = cs[0], q1 = cs[1], s0 = cs[2], s1 = cs[3], e0 = cs[4], e1 = cs[5];
+                    float2 tv[4];
+                    lane_values(w, q0, q1, s0, s1, tv);
+                    const float2 D[4] = {make_float2(__uint_as_float(e0.x), __uint_as_float(e0.y)),
+                                         make_float2(__uint_as_float(e0.z), __uint_as_float(e0.w)),
+                                         make_float2(__uint_as_float(e1.x), __uint_as_float(e1.y)),
+                                         make_float2(__uint_as_float(e1.z), __uint_as_float(e1.w))};
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) ab[p] = (k == 0) ? fmul2(D[p], tv[p]) : ffma2(D[p], tv[p], ab[p]);
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < 4; ++p) acc[t][p] = ffma2(dd, ab[p], acc[t][p]);
+        }
+    }
+
+    const int row = tile * kTileRows + rr;
+#pragma unroll
+    for (int t = 0; t < kTok; ++t) {
+        const int c = c0 + t;
+        if (c < cols && row < rows) y[static_cast<size_t>(c) * rows + row] = final_reduce(acc[t]);
+    }
+}
+
+}  // namespace
+
+// --------------------------------------------------------------------------------------------
+GQ_ERROR_ACCESSOR(q1)
+
+cudaError_t launch_q1_pack(const void* raw, int rows, int n, void* packed, cudaStream_t s) {
+    const int nb = n / 128;
+    const long long tiles = (rows + kTileRows - 1) / kTileRows;
+    const long long total = tiles * nb * kTileRows;
+    const int threads = 256;
+    const long long blocks = (total + threads - 1) / threads;
+    q1_pack_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(static_cast<const uint8_t*>(raw), rows, nb,
+                                                                     static_cast<uint8_t*>(packed), total);
+    return cudaGetLastError();
+}
+
+int gemv_tiles_for(int rows) { return (rows + kTileRows - 1) / kTileRows; }
+
+// Persistent grid: one thread block per SM (cached per device), fewer for small problems.
+static cudaError_t gemv_grid(int total_tiles, int* grid) {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (cached[dev] == 0) {
+        e = cudaFuncSetAttribute(q1_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kGemvSmem));
+        if (e != cudaSuccess) return e;
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q1_gemv_kernel, kGemvWarps * 32, kGemvSmem);
+        if (e != cudaSuccess) return e;
+        cached[dev] = sms * (per_sm > 0 ? per_sm : 1);
+    }
+    const int need = (total_tiles * kUnitsPerTile + kGemvWarps - 1) / kGemvWarps;
+    *grid = need < cached[dev] ? need : cached[dev];
+    return cudaSuccess;
+}
+
+// The activation constants, then 16 bytes for the tile counter.
+size_t gemv_workspace_bytes(int n) { return static_cast<size_t>(n / 32) * kConstWords * 4 + 16; }
+
+cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int rows, int n, void* workspace,
+                           cudaStream_t s) {
+    const int tiles = gemv_tiles_for(rows);
+    int grid = 0;
+    cudaError_t e = gemv_grid(tiles, &grid);
+    if (e != cudaSuccess) return e;
+    int* counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + gemv_workspace_bytes(n) - 16);
+    gq_gemv_desc d{packed, act, y, workspace, rows, n, 0, 0};
+    act_prep_kernel<<<dim3(8, 1), 256, 0, s>>>(d, nullptr, 0, counter);
+    q1_gemv_kernel<<<grid, kGemvWarps * 32, kGemvSmem, s>>>(d, nullptr, 0, tiles, counter);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q1_gemv_grouped(const gq_gemv_desc* descs, int count, int total_tiles, int* counter,
+                                   cudaStream_t s) {
+    int grid = 0;
+    cudaError_t e = gemv_grid(total_tiles, &grid);
+    if (e != cudaSuccess) return e;
+    gq_gemv_desc none{nullptr, nullptr, nullptr, nullptr, 0, 128, 0, 0};
+    act_prep_kernel<<<dim3(8, count), 256, 0, s>>>(none, descs, count, counter);
+    q1_gemv_kernel<<<grid, kGemvWarps * 32, kGemvSmem, s>>>(none, descs, count, total_tiles, counter);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q1_gemm(const void* packed, const void* act, float* y, int rows, int n, int cols, int path,
+                           cudaStream_t s) {
+    const dim3 grid((rows + kTileRows - 1) / kTileRows, (cols + kTok - 1) / kTok);
+    if (path == GQ_PATH_LUT4)
+        q1_gemm_kernel<GQ_PATH_LUT4><<<grid, 128, 0, s>>>(static_cast<const uint8_t*>(packed),
+                                                          static_cast<const uint8_t*>(act), y, rows, n, cols);
+    else
+        q1_gemm_kernel<GQ_PATH_DP4A><<<grid, 128, 0, s>>>(static_cast<const uint8_t*>(packed),
+                                                          static_cast<const uint8_t*>(act), y, rows, n, cols);
+    return cudaGetLastError();
+}
+
+}  // namespace gq

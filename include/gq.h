@@ -1,0 +1,226 @@
+/*
+ * gq.h -- C ABI of libgq: low-bit block-quantized weight x activation matvec / matmul on GB300
+ * (sm_103a).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *device* point to device memory owned by the caller; the library never
+ *    allocates or frees device memory on a call, never synchronizes the stream, and keeps no
+ *    per-call state.  Host pointers are named as such.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and
+ *    completes asynchronously.
+ *  - Every call validates its arguments on the host before launching anything and returns an
+ *    int status: GQ_OK or one of the GQ_E* codes below.  A rejected call launches nothing.
+ *    Nothing is truncated silently: a reduction length that is not a whole number of blocks is
+ *    an error, not a dropped tail.
+ *  - After GQ_ECUDA, gq_last_cuda_error() returns the cudaError_t of the failed launch (per
+ *    calling thread).
+ *  - Kernels wait on nothing but their own asynchronous copies, and every such wait is bounded
+ *    (about one second).  A wait that runs out sets a device-side error word and the kernel
+ *    returns; gq_device_error() reads and clears it.
+ *
+ * Sources (page title, section) for the operations:
+ *  [P1] browseml-gpu.js (browseML / bankML): header comment on the arithmetic; Q1_DOT_WGSL,
+ *       Q1_MM_WGSL, Q1_MM4_WGSL; packQ1 / packQ8; gpuMatMul.
+ *  [P2] kopitiam-gpu src/shaders/block_q8_matmul_nt.wgsl: header (bindings, PACKING,
+ *       ACCUMULATION ORDER), fn quant_at, fn main.
+ *  [P3] BonsaiのWebGPUカーネルを読み解く: the ternary P/N bitplane popcount identity; the
+ *       decode / prefill kernel figure (q1_bits + q1_scales, binary-lut4-matmul LUT4 prefill,
+ *       subgroup-matrix third path).
+ */
+#ifndef GQ_H
+#define GQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gq_stream_t;   /* the same type as cudaStream_t */
+
+enum gq_status {
+    GQ_OK = 0,
+    GQ_EINVAL_SHAPE = 1,   /* a size is <= 0, too large, or not a whole number of blocks  */
+    GQ_EINVAL_PTR = 2,     /* a required pointer is NULL or not aligned as documented     */
+    GQ_EUNSUPPORTED = 3,   /* the requested path does not exist for this operation/shape  */
+    GQ_ECUDA = 4           /* a CUDA launch failed; see gq_last_cuda_error()               */
+};
+
+enum gq_path {
+    GQ_PATH_AUTO = 0,      /* the library picks by shape                                    */
+    GQ_PATH_DP4A = 1,      /* integer dot products (dp4a) on the CUDA cores                 */
+    GQ_PATH_LUT4 = 2,      /* 16-entry subset-sum tables per 4 activations, nibble lookups  */
+    GQ_PATH_MMA = 3        /* tcgen05 tensor-core MMA (kind::f16) with a fixed-order epilogue */
+};
+
+/* Library version string (static storage). */
+const char* gq_version(void);
+/* Human-readable name of a status code (static storage). */
+const char* gq_status_string(int status);
+/* cudaError_t of the last failed launch on this host thread (0 if none). */
+int gq_last_cuda_error(void);
+/* Reads and clears the device-side error word of the current device: 0 if no kernel has
+ * reported a timed-out wait since the last call, else a nonzero code.  Synchronizes the device. */
+int gq_device_error(void);
+
+/* ============================================================================================
+ * Q1_0 weights x Q8_0 activations  [P1]
+ *
+ * Q1_0 block (18 bytes, the pages' storage): f16 d0 (little-endian) then 128 sign bits; weight
+ * j = 32k + e of the block is bit e%8 of byte 2 + 4k + e/8 (bit 1 -> +q, bit 0 -> -q).
+ * Q8_0 block (34 bytes): f16 d1 (little-endian) then 32 int8 quants.
+ * A row of n weights is n/128 Q1_0 blocks; an activation vector of n values is n/32 Q8_0 blocks;
+ * Q1_0 block i pairs with Q8_0 blocks 4i..4i+3.
+ *
+ * Result per (row, activation) -- the pages' exact operation order, reproduced bit for bit:
+ *   per block i, sub-block k = 0..3, lane l = 0..7 (weights 4l..4l+3 of the sub-block):
+ *     s = sum (bit ? q : -q), the negate wrapping as int8 (-(-128) = -128)
+ *     p = d1 * s (exact), ab[l] = p (k = 0) or ab[l] + p (k > 0)   (round to nearest even)
+ *     acc[l] = fma(d0, ab[l], acc[l])                                 (correctly rounded)
+ *   y = ((acc0+acc4)+(acc2+acc6)) + ((acc1+acc5)+(acc3+acc7)), acc from +0.
+ * ========================================================================================== */
+
+/* Bytes of the packed (resident) form of a rows x n Q1_0 matrix; 0 if the shape is invalid. */
+size_t gq_q1_0_packed_bytes(int rows, int n);
+
+/* One-time repack of Q1_0 weights into the kernels' resident layout ([P1] packQ1: "repacked
+ * once"; the engine keeps weights resident).
+ *   raw_device    rows * (n/128) * 18 bytes, the pages' AoS blocks, row-major; any alignment.
+ *   packed_device gq_q1_0_packed_bytes(rows, n) bytes, 16-byte aligned; fully written
+ *                 (rows are padded to a multiple of 128 with zero blocks).
+ * Layout (private to the library; treat as opaque): 128-row tiles; per (tile, block) a 2304-byte
+ * chunk of 128 x 16 bytes of sign bits (bit-permuted within each 32-bit word) then 128 f16 d0.
+ * Errors: GQ_EINVAL_SHAPE if rows < 1, n < 128, n % 128 != 0 or n > 2^20;
+ *         GQ_EINVAL_PTR if a pointer is NULL or packed_device is not 16-byte aligned. */
+int gq_q1_0_pack(const void* raw_device, int rows, int n, void* packed_device, gq_stream_t stream);
+
+/* Bytes of workspace one decode GEMV needs for an activation of n values: the activation's
+ * per-32-value constants (96 bytes per 32 values), built by the call itself, and a 16-byte tile
+ * counter. */
+size_t gq_q1_q8_workspace_bytes(int n);
+
+/* Decode GEMV ([P1] Q1_DOT_WGSL semantics): y[r] for r < rows.
+ *   packed_w_device from gq_q1_0_pack(rows, n); act_device: n/32 Q8_0 blocks (34 bytes each,
+ *   2-byte aligned); y_device: rows f32; workspace_device: gq_q1_q8_workspace_bytes(n) bytes,
+ *   16-byte aligned, overwritten by the call (two launches on `stream`: the activation's
+ *   constants into the workspace, then the GEMV, which hands 128-row tiles to its warps through
+ *   a counter at the end of the workspace).  Calls that share a workspace must not overlap on
+ *   the GPU.
+ * Errors: as gq_q1_0_pack, plus GQ_EINVAL_PTR if act_device is odd, y_device not 4-aligned or
+ * the workspace NULL or not 16-aligned. */
+int q1_q8_gemv(const void* packed_w_device, const void* act_device, float* y_device,
+               int rows, int n, void* workspace_device, gq_stream_t stream);
+
+/* One matrix of a grouped GEMV sweep (all fields filled by the caller except tile_begin). */
+typedef struct gq_gemv_desc {
+    const void* packed_w;    /* device, from gq_q1_0_pack(rows, n)                      */
+    const void* act;         /* device, n/32 Q8_0 blocks                                */
+    float* y;                /* device, rows f32                                        */
+    void* workspace;         /* device, gq_q1_q8_workspace_bytes(n), 16-aligned, its own */
+    int rows;
+    int n;
+    int tile_begin;          /* filled by gq_gemv_group_plan                            */
+    int reserved;
+} gq_gemv_desc;
+
+/* Host-side planning for q1_q8_gemv_grouped: validates every descriptor (host array), sorts the
+ * array by n, largest first (stable; each entry keeps its own pointers, so results are
+ * unaffected), and fills tile_begin (a prefix sum of 128-row tiles).  *total_tiles receives the
+ * number of tiles of the whole group.
+ * Errors: GQ_EINVAL_SHAPE / GQ_EINVAL_PTR as q1_q8_gemv for the first bad descriptor (the array
+ * is then left unsorted), or GQ_EINVAL_SHAPE if count < 1, count > 65535 or the group exceeds
+ * 2^31-1 tiles. */
+int gq_gemv_group_plan(gq_gemv_desc* descs_host, int count, int* total_tiles);
+
+/* Grouped decode GEMV: every matrix of a layer stack (e.g. one decode token's sweep) in two
+ * launches (all activations' constants, then one persistent GEMV over every tile of the group,
+ * which hands 128-row tiles to warps through *counter_device, largest matrix first).
+ * descs_device is a device copy of the planned array (count entries, 8-byte aligned);
+ * total_tiles is the value gq_gemv_group_plan returned; counter_device is one int of device
+ * memory (4-aligned) that the call resets and uses -- calls sharing it, or sharing a
+ * descriptor's workspace, must not overlap on the GPU.  Results are bit-identical to calling
+ * q1_q8_gemv on each entry.  The host cannot re-validate device descriptors: pass only arrays
+ * that gq_gemv_group_plan accepted, unchanged. */
+int q1_q8_gemv_grouped(const gq_gemv_desc* descs_device, int count, int total_tiles, int* counter_device,
+                       gq_stream_t stream);
+
+/* Prefill GEMM over `cols` Q8_0 activation vectors ([P1] Q1_MM_WGSL / Q1_MM4_WGSL): every
+ * (row, column) is the GEMV chain above, stored at y[c * rows + r].
+ *   act_device: cols * (n/32) Q8_0 blocks, column after column (2-byte aligned).
+ *   path: GQ_PATH_DP4A, GQ_PATH_LUT4 or GQ_PATH_AUTO (DP4A); GQ_PATH_MMA -> GQ_EUNSUPPORTED
+ *         (the per-4-weight lane sums of this format leave a tensor core nothing dense to do).
+ * Errors: as q1_q8_gemv, plus GQ_EINVAL_SHAPE if cols < 1. */
+int q1_q8_gemm(const void* packed_w_device, const void* act_device, float* y_device,
+               int rows, int n, int cols, int path, gq_stream_t stream);
+
+/* ============================================================================================
+ * block_q8_matmul_nt  [P2]:  y = x . w^T with w block-scaled int8.
+ *   x_device      [m, k] f32 row-major (4-byte aligned)
+ *   quants_device k*n int8 packed four per u32, little-endian: element t of weight row `col` is
+ *                 byte (t%4) of word (col*k + t)/4, sign-extended (16-byte aligned)
+ *   scales_device [n, k/32] f32
+ *   y_device      [m, n] f32 row-major
+ * Order (bit for bit): per (row, col), for block b ascending: block_sum = 0; for t < 32:
+ * block_sum = block_sum + x*q (a rounded multiply, then a rounded add); acc = acc +
+ * scale*block_sum (the same); acc from +0.
+ * Errors: GQ_EINVAL_SHAPE if m, k or n < 1, k % 32 != 0, k > 65536 or m > 65535;
+ *         GQ_EINVAL_PTR for NULL or misaligned pointers. */
+int block_q8_matmul_nt(const float* x_device, const uint32_t* quants_device,
+                       const float* scales_device, float* y_device, int m, int k, int n,
+                       gq_stream_t stream);
+
+/* ============================================================================================
+ * Ternary bitplane GEMV  [P3]:  weights w in {-1, 0, +1} as bitplanes P (w = +1) and N (w = -1),
+ * activations binarized to a bitplane X (bit 1 -> +1, bit 0 -> -1); bit j of word v is element
+ * 32v + j.  Per (batch b, row r), exactly:
+ *   y = 2 * (sum popc(P & X) - sum popc(N & X)) - sum popc(P) + sum popc(N).
+ * A position with both P and N set counts as weight 0.
+ *   P_device, N_device [rows, k/32] u32 (16-byte aligned); X_device [batch, k/32] u32
+ *   (16-byte aligned); y_device [batch, rows] int32.
+ * Errors: GQ_EINVAL_SHAPE if rows or batch < 1, k < 1024, k % 1024 != 0 (tiles of 32 words),
+ *         k > 65536 or batch > 64;
+ *         GQ_EINVAL_PTR for NULL or misaligned pointers. */
+int ternary_bitplane_gemv(const uint32_t* P_device, const uint32_t* N_device,
+                          const uint32_t* X_device, int32_t* y_device, int rows, int k,
+                          int batch, gq_stream_t stream);
+
+/* ============================================================================================
+ * Batched prefill with Bonsai-format 1-bit weights  [P3] and Q8_0 activations.
+ *
+ * Activation quantizer (the pages give none for Q8_0 blocks; the reading is stated here):
+ * per 32-block of a row of x, amax = max |x|; d = amax / 127 (round to nearest); the stored
+ * scale is f16(d) rounded to nearest even; q = clamp(floor(v) + (v - floor(v) >= 0.5), -127,
+ * 127) with v = x / d (round to nearest, the f32 d); amax == 0 gives d = 0 and q = 0.
+ *   x_device [m, k] f32; d_device [m, k/32] f16 bits; q_device [m, k] int8 (16-byte aligned);
+ *   mma_operand_device: NULL, or [m, k] f16 (16-byte aligned) receiving q as f16 with the
+ *   elements of each 32-block interleaved (position 2u <- element u, 2u+1 <- element u+16):
+ *   the operand layout q1s32_q8_gemm's MMA path reads.
+ * Errors: GQ_EINVAL_SHAPE if m or k < 1, k % 32 != 0 or k > 65536; GQ_EINVAL_PTR. */
+int gq_quantize_q8_0(const float* x_device, int m, int k, uint16_t* d_device, int8_t* q_device,
+                     uint16_t* mma_operand_device, gq_stream_t stream);
+
+/* Prefill GEMM: y[m, n] = sum over 32-blocks b ascending of
+ *     S = sum_t (sign bit ? q : -q) (int8-wrapping negate), p = f16(xd[m,b]) * S (exact),
+ *     acc = fma(w_scale[n, b], p, acc) (correctly rounded), acc from +0.
+ *   signs_device   [N, K/32] u32, bit t of word b = weight 32b+t, 1 -> +1 (16-byte aligned)
+ *   wscale_device  [N, K/32] f32
+ *   xd_device      [M, K/32] f16 bits, xq_device [M, K] int8 (16-byte aligned)
+ *   xq_mma_device  the interleaved f16 operand from gq_quantize_q8_0 (required for
+ *                  GQ_PATH_MMA, else may be NULL); it must hold the same q as xq_device, all in
+ *                  [-127, 127] (as the quantizer produces)
+ *   y_device       [M, N] f32 row-major
+ *   path: GQ_PATH_LUT4, GQ_PATH_MMA, or GQ_PATH_AUTO (MMA when M >= 64 and the operand is
+ *   given, else LUT4).  Both paths are bit-identical to the order above.
+ * Errors: GQ_EINVAL_SHAPE if M, N or K < 1, K % 64 != 0 or K > 65536; GQ_EUNSUPPORTED for an
+ * unknown path or GQ_PATH_DP4A; GQ_EINVAL_PTR for NULL/misaligned pointers (xq_mma_device NULL
+ * with GQ_PATH_MMA included). */
+int q1s32_q8_gemm(const uint32_t* signs_device, const float* wscale_device,
+                  const uint16_t* xd_device, const int8_t* xq_device,
+                  const uint16_t* xq_mma_device, float* y_device, int M, int N, int K, int path,
+                  gq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GQ_H */

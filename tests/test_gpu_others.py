@@ -1,0 +1,135 @@
+"""GPU parity of block_q8_matmul_nt (kopitiam-gpu block_q8_matmul_nt.wgsl), the ternary bitplane
+GEMV (the Bonsai P/N popcount identity), the Q8_0 activation quantizer and the Bonsai-format
+prefill GEMM, against the CPU oracle through the C ABI."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from tests.gpu_util import assert_same_bits, need_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gq():
+    return need_gpu()
+
+
+# ----------------------------------------------------------------------------- block_q8
+
+@pytest.mark.parametrize("m,k,n", [(1, 32, 1), (1, 960, 1001), (3, 96, 513), (4, 960, 257), (7, 64, 33),
+                                   (16, 960, 300), (17, 320, 129), (40, 128, 64)])
+def test_block_q8_bit_exact(gq, m, k, n):
+    rng = wl.Rng(m * 1000 + k + n)
+    x, quants, scales = wl.block_q8_inputs(rng, m, k, n)
+    y = gq.block_q8_matmul_nt(to_dev(x), to_dev(quants), to_dev(scales)).cpu().numpy()
+    assert_same_bits(y, oracle.block_q8_matmul_nt(x, quants, scales, m, k, n), f"block_q8 {m}x{k}x{n}")
+
+
+def test_block_q8_golden_on_gpu(gq):
+    from tests.test_oracle_others import pack_quants
+    cases = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "block_q8_cases.json")))["cases"]
+    for case in cases:
+        k = case["k"]
+        x = np.zeros((1, k), dtype=np.float32)
+        q = np.zeros(k, dtype=np.int8)
+        for e, v in case["x"]:
+            x[0, e] = v
+        for e, v in case["q"]:
+            q[e] = v
+        sc = np.array(case["scales"], dtype=np.float32).reshape(1, -1)
+        y = gq.block_q8_matmul_nt(to_dev(x), to_dev(pack_quants(q)), to_dev(sc)).cpu().numpy()
+        assert hex(int(y.view(np.uint32)[0, 0])) == case["expected_f32"], case["name"]
+
+
+@pytest.mark.parametrize("m", [1, 4, 16])
+def test_block_q8_full_size_sampled(gq, m):
+    """The 49152 x 960 output projection at m = 1, 4, 16 (as benchmarked); 512 sampled output
+    features against the oracle, bit for bit."""
+    n, k = 49152, 960
+    x, quants, scales = wl.block_q8_inputs(wl.Rng(2 + m), m, k, n)
+    y = gq.block_q8_matmul_nt(to_dev(x), to_dev(quants), to_dev(scales)).cpu().numpy()
+    cols = np.sort(np.random.default_rng(m).choice(n, 512, replace=False))
+    qs = quants.reshape(n, k // 4)[cols]
+    want = oracle.block_q8_matmul_nt(x, qs, scales[cols], m, k, cols.size)
+    assert_same_bits(y[:, cols], want, f"block_q8 full m={m}")
+
+
+# ----------------------------------------------------------------------------- ternary
+
+@pytest.mark.parametrize("rows,k,batch,pz", [(1, 1024, 1, 0.4), (130, 2048, 3, 0.4), (300, 4096, 16, 0.0),
+                                             (129, 1024, 17, 1.0), (64, 8192, 64, 0.4)])
+def test_ternary_exact(gq, rows, k, batch, pz):
+    P, N, X = wl.ternary_inputs(wl.Rng(rows + k + batch), rows, k, batch, p_zero=pz)
+    y = gq.ternary_bitplane_gemv(to_dev(P), to_dev(N), to_dev(X)).cpu().numpy()
+    assert np.array_equal(y, oracle.ternary_identity(P, N, X, rows, k, batch))
+
+
+def test_ternary_overlapping_planes(gq):
+    rows, k, batch = 128, 1024, 2
+    P, _, X = wl.ternary_inputs(wl.Rng(4), rows, k, batch)
+    N = P | wl.Rng(5).u32(P.size).reshape(P.shape)
+    y = gq.ternary_bitplane_gemv(to_dev(P), to_dev(N), to_dev(X)).cpu().numpy()
+    assert np.array_equal(y, oracle.ternary_direct(P, N, X, rows, k, batch))
+
+
+@pytest.mark.parametrize("batch", [1, 4, 16])
+def test_ternary_full_size(gq, batch):
+    rows, k = 14336, 4096
+    P, N, X = wl.ternary_inputs(wl.Rng(3), rows, k, batch)
+    y = gq.ternary_bitplane_gemv(to_dev(P), to_dev(N), to_dev(X)).cpu().numpy()
+    assert np.array_equal(y, oracle.ternary_identity(P, N, X, rows, k, batch))
+
+
+# ----------------------------------------------------------------------------- quantizer
+
+def _interleave(q: np.ndarray) -> np.ndarray:
+    """The MMA operand order within each 32-block: position 2u <- element u, 2u+1 <- u+16."""
+    m, k = q.shape
+    b = q.reshape(m, k // 32, 2, 16)
+    return np.stack([b[:, :, 0, :], b[:, :, 1, :]], axis=-1).reshape(m, k)
+
+
+@pytest.mark.parametrize("m,k", [(1, 32), (5, 96), (512, 4096)])
+def test_quantize_bit_exact(gq, m, k):
+    x = wl.f32_normal(wl.Rng(m + k), m * k).reshape(m, k)
+    x[0, :32] = 0.0                                   # an all-zero block
+    if k >= 64:
+        x[-1, 32:64] *= 1e-30                         # a block whose scale underflows in f16
+    d, q, op = gq.quantize_q8_0(to_dev(x), mma_operand=True)
+    dw, qw = oracle.quantize_q8_0(x, m, k)
+    assert np.array_equal(d.cpu().numpy().view(np.uint16), dw)
+    assert np.array_equal(q.cpu().numpy(), qw)
+    opf = op.cpu().numpy().view(np.float16).astype(np.float32)
+    assert np.array_equal(opf, _interleave(qw.astype(np.float32)))
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def run_prefill(gq, signs, ws, x, path):
+    d, q, op = gq.quantize_q8_0(to_dev(x), mma_operand=True)
+    y = gq.q1s32_q8_gemm(to_dev(signs), to_dev(ws), d, q, op, path=path)
+    return y.cpu().numpy(), d.cpu().numpy().view(np.uint16), q.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 64), (5, 130, 128), (33, 257, 1024), (64, 128, 4096)])
+def test_prefill_lut4_bit_exact(gq, M, N, K):
+    signs, ws, x = wl.prefill_inputs(wl.Rng(M + N + K), M, K, N)
+    y, d, q = run_prefill(gq, signs, ws, x, gq.PATH_LUT4)
+    assert_same_bits(y, oracle.prefill_q1s32(signs, ws, d, q, M, N, K), f"lut4 {M}x{N}x{K}")
+
+
+def test_prefill_lut4_full_size_sampled(gq):
+    """M = 512 tokens, K = 4096, N = 14336: 24 tokens x 96 weight rows sampled against the oracle."""
+    M, K, N = 512, 4096, 14336
+    signs, ws, x = wl.prefill_inputs(wl.Rng(4), M, K, N)
+    y, d, q = run_prefill(gq, signs, ws, x, gq.PATH_LUT4)
+    rng = np.random.default_rng(1)
+    ms = np.sort(rng.choice(M, 24, replace=False))
+    ns = np.sort(rng.choice(N, 96, replace=False))
+    want = oracle.prefill_q1s32(signs[ns], ws[ns], d[ms], q[ms], ms.size, ns.size, K)
+    assert_same_bits(y[np.ix_(ms, ns)], want, "lut4 full sampled")

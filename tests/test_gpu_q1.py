@@ -1,0 +1,173 @@
+"""GPU parity of the Q1_0 . Q8_0 path (browseml-gpu.js Q1_DOT_WGSL / Q1_MM_WGSL / Q1_MM4_WGSL
+semantics) against the CPU oracle, bit for bit, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from tests.gpu_util import assert_same_bits, need_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gq():
+    return need_gpu()
+
+
+def gemv(gq, w, a, rows, n):
+    packed = gq.q1_0_pack(to_dev(w), rows, n)
+    return gq.q1_q8_gemv(packed, to_dev(a), rows, n).cpu().numpy()
+
+
+@pytest.mark.parametrize("rows,n,dist,seed", [
+    (256, 1024, "uniform", 0),      # the small decode workload: 256 rows, 8 blocks
+    (1, 128, "uniform", 1),
+    (1, 128, "page", 2),
+    (129, 640, "page", 3),          # a ragged second tile
+    (300, 2560, "page", 4),
+    (1000, 6912, "uniform", 5),
+    (77, 16384, "page", 6),         # the largest n the GEMV takes
+])
+def test_gemv_bit_exact(gq, rows, n, dist, seed):
+    rng = wl.Rng(1000 + seed)
+    w = wl.q1_0_weights(rng, rows, n, scales=dist)
+    a = wl.q8_0_acts(rng, 1, n, scales=dist, quants=dist)
+    assert_same_bits(gemv(gq, w, a, rows, n), oracle.q1_q8_gemv(w, a, rows, n), f"gemv {rows}x{n} {dist}")
+
+
+def test_gemv_all_minus128_and_zero_scales(gq):
+    """Degenerate inputs: every quant -128 (the wrapping negate everywhere), zero scales."""
+    rows, n = 64, 512
+    rng = wl.Rng(77)
+    w = wl.q1_0_weights(rng, rows, n)
+    a = wl.q8_0_acts(rng, 1, n).reshape(-1, 34).copy()
+    a[:, 2:] = 0x80
+    a[::3, 0:2] = 0                                   # d1 = +0 on a third of the blocks
+    a = a.reshape(-1)
+    w2 = w.reshape(-1, 18).copy()
+    w2[::5, 0:2] = [0x00, 0x80]                       # d0 = -0 on a fifth
+    w2 = w2.reshape(-1)
+    assert_same_bits(gemv(gq, w2, a, rows, n), oracle.q1_q8_gemv(w2, a, rows, n), "degenerate")
+
+
+def test_golden_cases_on_gpu(gq):
+    import json
+    import os
+    from tests.test_oracle_q1 import build_case
+    cases = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "q1_q8_cases.json")))["cases"]
+    for case in cases:
+        w, a, n = build_case(case)
+        y = gemv(gq, w, a, 1, n)
+        assert hex(int(y.view(np.uint32)[0])) == case["expected_f32"], case["name"]
+
+
+def test_f16_weight_scale_every_pattern(gq):
+    """All 65536 f16 patterns as d0 (one row each, lane 0 = 1 * 1): the decode of every scale,
+    subnormals, signed zeros, Inf and NaN included, matches the oracle's integer decode."""
+    rows, n = 65536, 128
+    w = np.zeros((rows, 18), dtype=np.uint8)
+    w[:, 0:2] = np.arange(rows, dtype=np.uint16).view(np.uint8).reshape(rows, 2)
+    w[:, 2] = 0x01                                    # weight 0 of sub-block 0 set
+    a = np.zeros((4, 34), dtype=np.uint8)
+    a[0, 0:2] = [0x00, 0x3C]                          # d1 = 1
+    a[0, 2] = 1                                       # q0 = 1 -> lane 0: s = 1
+    y = gemv(gq, w.reshape(-1), a.reshape(-1), rows, n)
+    assert_same_bits(y, oracle.q1_q8_gemv(w.reshape(-1), a.reshape(-1), rows, n), "d0 patterns")
+
+
+def test_f16_activation_scale_every_pattern(gq):
+    """All 65536 f16 patterns as d1, spread over the columns of a GEMM (512 blocks per column;
+    the Inf/NaN patterns in columns of their own)."""
+    n, rows = 16384, 2
+    pats = np.arange(65536, dtype=np.uint16)
+    finite = pats[((pats >> 10) & 0x1F) != 0x1F]
+    nonfin = pats[((pats >> 10) & 0x1F) == 0x1F]
+    order = np.concatenate([finite, nonfin])
+    per = n // 32
+    cols = (order.size + per - 1) // per
+    d1 = np.zeros(cols * per, dtype=np.uint16)
+    d1[:order.size] = order
+    rng = wl.Rng(88)
+    a = wl.q8_0_acts(rng, cols, n).reshape(-1, 34)
+    a[:, 0:2] = d1.view(np.uint8).reshape(-1, 2)
+    a = a.reshape(-1)
+    w = wl.q1_0_weights(rng, rows, n)
+    packed = gq.q1_0_pack(to_dev(w), rows, n)
+    y = gq.q1_q8_gemm(packed, to_dev(a), rows, n, cols, gq.PATH_DP4A).cpu().numpy()
+    assert_same_bits(y, oracle.q1_q8_gemm(w, a, rows, n, cols), "d1 patterns")
+
+
+@pytest.mark.parametrize("path", ["dp4a", "lut4"])
+@pytest.mark.parametrize("rows,n,cols,dist", [
+    (256, 1024, 5, "page"),           # five activations: a partial tile of four (Q1_MM4_WGSL)
+    (130, 512, 1, "uniform"),
+    (300, 2560, 9, "page"),
+    (64, 6912, 4, "uniform"),
+])
+def test_gemm_bit_exact(gq, path, rows, n, cols, dist):
+    rng = wl.Rng(hash((rows, n, cols, dist)) & 0xFFFF)
+    w = wl.q1_0_weights(rng, rows, n, scales=dist)
+    a = wl.q8_0_acts(rng, cols, n, scales=dist, quants=dist)
+    p = gq.PATH_DP4A if path == "dp4a" else gq.PATH_LUT4
+    packed = gq.q1_0_pack(to_dev(w), rows, n)
+    y = gq.q1_q8_gemm(packed, to_dev(a), rows, n, cols, p).cpu().numpy()
+    assert_same_bits(y, oracle.q1_q8_gemm(w, a, rows, n, cols), f"gemm {path}")
+
+
+def test_gemm_column_equals_gemv(gq):
+    rows, n, cols = 200, 1024, 6
+    rng = wl.Rng(9)
+    w = wl.q1_0_weights(rng, rows, n)
+    a = wl.q8_0_acts(rng, cols, n, quants="page")
+    packed = gq.q1_0_pack(to_dev(w), rows, n)
+    Y = gq.q1_q8_gemm(packed, to_dev(a), rows, n, cols).cpu().numpy()
+    ab = (n // 32) * 34
+    for c in range(cols):
+        yc = gq.q1_q8_gemv(packed, to_dev(a[c * ab:(c + 1) * ab]), rows, n).cpu().numpy()
+        assert_same_bits(Y[c], yc, f"column {c}")
+
+
+def test_grouped_equals_single_small(gq):
+    import torch
+    rng = wl.Rng(12)
+    shapes = [(256, 1024), (1, 128), (1000, 2560), (129, 6912), (700, 640)]
+    items, ref = [], []
+    for rows, n in shapes:
+        w = wl.q1_0_weights(rng, rows, n, scales="page")
+        a = wl.q8_0_acts(rng, 1, n, quants="page")
+        packed = gq.q1_0_pack(to_dev(w), rows, n)
+        y = torch.empty(rows, dtype=torch.float32, device="cuda")
+        items.append((packed, to_dev(a), y, rows, n))
+        ref.append(oracle.q1_q8_gemv(w, a, rows, n))
+    g = gq.GroupedGemv(items)
+    g()
+    for (packed, act, y, rows, n), want in zip(items, ref):
+        assert_same_bits(y.cpu().numpy(), want, f"grouped {rows}x{n}")
+    assert gq.device_error() == 0
+
+
+def test_bitnet_sweep_full_size_sampled(gq):
+    """The BitNet-2B decode sweep (30 layers x 7 matrices, 334.5 MB of Q1_0 weights) in one grouped
+    launch, as the benchmark times it: every matrix's output equals its single-matrix GEMV bit for
+    bit, and 48 sampled rows of every matrix equal the oracle."""
+    import torch
+    items, raw = [], []
+    for rows, n, w, a in wl.bitnet_sweep(seed=1):
+        packed = gq.q1_0_pack(to_dev(w), rows, n)
+        y = torch.empty(rows, dtype=torch.float32, device="cuda")
+        items.append((packed, to_dev(a), y, rows, n))
+        raw.append((w, a))
+    g = gq.GroupedGemv(items)
+    g()
+    torch.cuda.synchronize()
+    sel = np.random.default_rng(5)
+    for (packed, act, y, rows, n), (w, a) in zip(items, raw):
+        got = y.cpu().numpy()
+        single = gq.q1_q8_gemv(packed, act, rows, n).cpu().numpy()
+        assert_same_bits(got, single, f"grouped vs single {rows}x{n}")
+        rb = (n // 128) * 18
+        for r in sel.choice(rows, 48, replace=False):
+            want, _ = oracle.q1_q8_row(w[r * rb:(r + 1) * rb], a, n)
+            assert_same_bits(got[r:r + 1], np.array([want]), f"row {r} of {rows}x{n}")
+    assert gq.device_error() == 0
