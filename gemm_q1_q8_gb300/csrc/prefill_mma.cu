@@ -1,10 +1,345 @@
-// tcgen05 MMA prefill path (placeholder until the kernel lands).
+// Prefill GEMM on the 5th-generation tensor cores (tcgen05, kind::f16), Bonsai-format 1-bit
+// weights x Q8_0 activations, bit-identical to the fixed order
+//   S = sum_t (bit ? q : -q) per 32-block, p = f16(xd[m,b]) * S (exact), acc = fma(w_scale[n,b], p, acc).
+// (BonsaiのWebGPUカーネルを読み解く: the prefill figure names a cooperative-matrix path beside
+// LUT4; this is its sm_103a counterpart.)
+//
+// Why f16 MMA is exact here: the weights are +-1 and the quants |q| <= 127, both exact in f16;
+// every product is an integer below 2^7 and a 32-term block sum is at most 4064 < 2^12, so the
+// tensor core's f32 accumulation of one block holds S exactly.  Each 32-block gets its own
+// accumulator (two K=16 MMAs into a fresh TMEM buffer), drained and applied in block order.
+//
+// Thread block (one per SM): 128 weight rows x 128 tokens, K in stages of 64 (two 32-blocks).
+//   warp 0      : TMA producer of the activation tiles (f16, interleaved, 128-byte swizzle)
+//   warp 1      : TMEM allocator and MMA issuer (one elected thread)
+//   warps 2-5   : weight producers -- expand sign bits to +-1 f16 in the same swizzled K-major
+//                 layout (pairs (u, u+16) of a 32-block in one 32-bit word, the order the
+//                 quantizer's MMA operand uses)
+//   warps 6-13  : epilogue -- per 32-block, tcgen05.ld of the 128x128 f32 block sums (each warp
+//                 its 32 TMEM lanes x 64 columns), p = dx*S, acc = fma(w_s, p, acc) in registers
+// Four smem stages (A 16 KB + B 16 KB each) and four TMEM accumulators of 128 columns.  Every
+// wait is bounded (~1 s); a role that gives up raises an abort flag the others honour, and the
+// block drains its copies and MMAs and frees TMEM before it exits.
 #include "gq_internal.cuh"
 
 namespace gq {
 GQ_ERROR_ACCESSOR(prefill_mma)
-cudaError_t launch_prefill_mma(const uint32_t*, const float*, const uint16_t*, const uint16_t*, float*, int, int, int,
-                               cudaStream_t) {
-    return cudaErrorNotSupported;
+
+namespace {
+
+constexpr int BM = 128;          // weight rows per tile (MMA M, TMEM lanes)
+constexpr int BN = 128;          // tokens per tile (MMA N)
+constexpr int BK = 64;           // K per stage (two 32-blocks)
+constexpr int kStagesM = 4;
+constexpr int kAccBufs = 4;      // TMEM accumulators (128 columns each)
+constexpr int kTmemCols = 512;
+constexpr int kTileA = BM * BK * 2;    // 16 KB
+constexpr int kTileB = BN * BK * 2;    // 16 KB
+
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpA0 = 2, kNumAWarps = 4, kWarpE0 = 6, kNumEWarps = 8;
+constexpr int kThreads = (kWarpE0 + kNumEWarps) * 32;   // 448
+
+// instruction descriptor: D f32, A/B f16, both K-major, N = 128, M = 128
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0u << 16) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+
+struct Bars {
+    uint64_t fullA[kStagesM], fullB[kStagesM], empty[kStagesM];
+    uint64_t tfull[kAccBufs], tempty[kAccBufs];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// 64-bit shared-memory matrix descriptor: 128-byte swizzle, K-major, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc(const void* p) {
+    const uint64_t addr = smem_u32(p);
+    uint64_t d = 0;
+    d |= (addr >> 4) & 0x3FFFull;               // start address
+    d |= static_cast<uint64_t>(1) << 16;        // leading byte offset (unused for swizzled K-major)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;  // stride byte offset: next 8-row group
+    d |= static_cast<uint64_t>(1) << 46;        // descriptor version (sm_100 family)
+    d |= static_cast<uint64_t>(2) << 61;        // layout: 128-byte swizzle
+    return d;
 }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 lanes x 32 columns of f32 from TMEM into registers (this warp's lane quadrant).
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Bounded wait that also gives up when another role has raised the abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > 1000000000ull) {
+            report_error(kErrMmaTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restrict__ signs,
+                   const float* __restrict__ ws, const uint16_t* __restrict__ xd, float* __restrict__ y, int M, int N,
+                   int K) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = base;                                   // [kStagesM][kTileA]
+    uint8_t* sB = base + kStagesM * kTileA;               // [kStagesM][kTileB]
+    Bars* bars = reinterpret_cast<Bars*>(sB + kStagesM * kTileB);
+    float* sdx = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + ((sizeof(Bars) + 15) & ~size_t(15)));
+    volatile int* abort = &bars->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
+    const int nbk = K / 32;
+    const int stages = K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStagesM; ++s) {
+            mbar_init(&bars->fullA[s], kNumAWarps);
+            mbar_init(&bars->fullB[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < kAccBufs; ++b) {
+            mbar_init(&bars->tfull[b], 1);
+            mbar_init(&bars->tempty[b], kNumEWarps);
+        }
+        mbar_init(&bars->done, 1);
+        bars->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars->tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // the epilogue's scale table: sdx[b * BN + j] = f16(xd[m0 + j, b]) for the tile's tokens
+    if (warp >= kWarpE0) {
+        const int t = threadIdx.x - kWarpE0 * 32;
+        for (int idx = t; idx < nbk * BN; idx += kNumEWarps * 32) {
+            const int j = idx / nbk, b = idx % nbk;
+            const int m = min(m0 + j, M - 1);
+            sdx[b * BN + j] = f16_to_f32(xd[static_cast<size_t>(m) * nbk + b]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    int tma_issued = 0;
+    if (warp == kWarpTma) {
+        // ---------------- activation tiles by TMA
+        if (lane == 0) {
+            prefetch_tmap(&tmB);
+            for (int k = 0; k < stages; ++k) {
+                const int s = k % kStagesM;
+                if (k >= kStagesM &&
+                    !wait_or_abort(&bars->empty[s], static_cast<uint32_t>(k / kStagesM - 1) & 1u, abort))
+                    break;
+                mbar_arrive_expect_tx(&bars->fullB[s], kTileB);
+                tma_load_2d(sB + s * kTileB, &tmB, k * BK, m0, &bars->fullB[s]);
+                ++tma_issued;
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // ---------------- MMA issue (one thread)
+        if (lane == 0) {
+            for (int k = 0; k < stages && !*abort; ++k) {
+                const int s = k % kStagesM;
+                const uint32_t ph = static_cast<uint32_t>(k / kStagesM) & 1u;
+                if (!wait_or_abort(&bars->fullA[s], ph, abort) || !wait_or_abort(&bars->fullB[s], ph, abort)) break;
+                tc_fence_after();
+                bool ok = true;
+                for (int bi = 0; bi < 2 && ok; ++bi) {
+                    const int b = 2 * k + bi;
+                    const int buf = b % kAccBufs;
+                    if (b >= kAccBufs &&
+                        !wait_or_abort(&bars->tempty[buf], static_cast<uint32_t>(b / kAccBufs - 1) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+                    for (int j = 0; j < 2; ++j) {
+                        const int koff = (bi * 32 + j * 16) * 2;     // bytes along the 128-byte row
+                        tc_mma(d, smem_desc(sA + s * kTileA + koff), smem_desc(sB + s * kTileB + koff), j);
+                    }
+                    tc_commit(&bars->tfull[buf]);
+                }
+                if (!ok) break;
+                tc_commit(&bars->empty[s]);
+            }
+            // all MMAs issued so far complete before TMEM may be freed
+            tc_commit(&bars->done);
+        }
+    } else if (warp < kWarpE0) {
+        // ---------------- weight producers: +-1 f16, swizzled K-major, one row per thread
+        const int r = threadIdx.x - kWarpA0 * 32;                 // 0..127
+        const int n = min(n0 + r, N - 1);
+        const uint32_t* srow = signs + static_cast<size_t>(n) * nbk;
+        for (int k = 0; k < stages; ++k) {
+            const int s = k % kStagesM;
+            if (k >= kStagesM &&
+                !wait_or_abort(&bars->empty[s], static_cast<uint32_t>(k / kStagesM - 1) & 1u, abort))
+                break;
+            uint8_t* tileA = sA + s * kTileA + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+            for (int bi = 0; bi < 2; ++bi) {
+                const uint32_t w = __ldg(srow + 2 * k + bi);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t h[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int u = c4 * 4 + e;        // pair (u, u+16): bits u and u+16 -> signs of two f16
+                        h[e] = ((w << (15 - u)) & 0x80008000u) ^ 0xBC00BC00u;
+                    }
+                    const int chunk = bi * 4 + c4;
+                    *reinterpret_cast<uint4*>(tileA + ((chunk ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->fullA[s]);
+        }
+    } else {
+        // ---------------- epilogue
+        const int q = warp & 3;                        // TMEM lane quadrant of this warp
+        const int h = (warp - kWarpE0) >> 2;           // column half
+        const int r = q * 32 + lane;                   // row of the tile = TMEM lane
+        const int n = n0 + r;
+        const float* wrow = ws + static_cast<size_t>(min(n, N - 1)) * nbk;
+        float acc[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+        bool ok = true;
+        float wnext = __ldg(wrow);
+        for (int b = 0; b < nbk; ++b) {
+            const int buf = b % kAccBufs;
+            const float wsc = wnext;
+            if (b + 1 < nbk) wnext = __ldg(wrow + b + 1);
+            if (!wait_or_abort(&bars->tfull[buf], static_cast<uint32_t>(b / kAccBufs) & 1u, abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + h * 64);
+            const float4* dxr = reinterpret_cast<const float4*>(sdx + b * BN + h * 64);
+            const float2 w2 = make_float2(wsc, wsc);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float S[32];
+                tc_ld32(taddr + 32 * half, S);
+                tc_wait_ld();
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const int j = half * 32 + 4 * j4;
+                    const float4 dd = dxr[half * 8 + j4];
+                    // p = dx * S (exact), then acc = fma(w_s, p, acc): two separate IEEE steps per column
+                    const float2 p01 = fmul2(make_float2(dd.x, dd.y), make_float2(S[4 * j4], S[4 * j4 + 1]));
+                    const float2 p23 = fmul2(make_float2(dd.z, dd.w), make_float2(S[4 * j4 + 2], S[4 * j4 + 3]));
+                    const float2 a01 = ffma2(w2, p01, make_float2(acc[j], acc[j + 1]));
+                    const float2 a23 = ffma2(w2, p23, make_float2(acc[j + 2], acc[j + 3]));
+                    acc[j] = a01.x;
+                    acc[j + 1] = a01.y;
+                    acc[j + 2] = a23.x;
+                    acc[j + 3] = a23.y;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[buf]);
+        }
+        if (ok && n < N) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const int m = m0 + h * 64 + j;
+                if (m < M) y[static_cast<size_t>(m) * N + n] = acc[j];
+            }
+        }
+    }
+
+    // ---------------- teardown: outstanding MMAs finish, copies land, TMEM is freed
+    __syncwarp();
+    if (warp == kWarpMma) {
+        if (lane == 0 && !mbar_wait(&bars->done, 0)) report_error(kErrMmaTimeout);
+        __syncwarp();
+    }
+    if (warp == kWarpTma && lane == 0) {
+        // every activation tile requested must have landed before shared memory is released
+        // (on a normal run they were all consumed; after an abort some may still be in flight)
+        const int first = tma_issued > kStagesM ? tma_issued - kStagesM : 0;
+        for (int k = first; k < tma_issued; ++k)
+            if (!mbar_wait(&bars->fullB[k % kStagesM], static_cast<uint32_t>(k / kStagesM) & 1u))
+                report_error(kErrDrainTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_mma(const uint32_t* signs, const float* ws, const uint16_t* xd, const uint16_t* xq_op,
+                               float* y, int M, int N, int K, cudaStream_t s) {
+    CUtensorMap tmB;
+    if (!make_tmap_2d(&tmB, xq_op, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                      static_cast<uint64_t>(K) * 2, BK, BN, true))
+        return cudaErrorInvalidValue;
+    const int nbk = K / 32;
+    const size_t smem = 1024 + static_cast<size_t>(kStagesM) * (kTileA + kTileB) + ((sizeof(Bars) + 15) & ~size_t(15)) +
+                        static_cast<size_t>(nbk) * BN * sizeof(float);
+    if (smem > 227 * 1024) return cudaErrorNotSupported;
+    static size_t configured = 0;
+    if (smem > configured) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    const dim3 grid((N + BM - 1) / BM, (M + BN - 1) / BN);
+    prefill_mma_kernel<<<grid, kThreads, smem, s>>>(tmB, signs, ws, xd, y, M, N, K);
+    return cudaGetLastError();
+}
+
 }  // namespace gq

@@ -133,3 +133,28 @@ def test_prefill_lut4_full_size_sampled(gq):
     ns = np.sort(rng.choice(N, 96, replace=False))
     want = oracle.prefill_q1s32(signs[ns], ws[ns], d[ms], q[ms], ms.size, ns.size, K)
     assert_same_bits(y[np.ix_(ms, ns)], want, "lut4 full sampled")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (1, 1, 64), (130, 257, 128), (64, 128, 1024), (300, 200, 4096)])
+def test_prefill_mma_bit_exact(gq, M, N, K):
+    """tcgen05 path: the same bits as the oracle's fixed order (exact block sums on the tensor core)."""
+    signs, ws, x = wl.prefill_inputs(wl.Rng(7 * M + N + K), M, K, N)
+    y, d, q = run_prefill(gq, signs, ws, x, gq.PATH_MMA)
+    assert_same_bits(y, oracle.prefill_q1s32(signs, ws, d, q, M, N, K), f"mma {M}x{N}x{K}")
+    assert gq.device_error() == 0
+
+
+def test_prefill_mma_full_size_sampled(gq):
+    """M = 512 tokens, K = 4096, N = 14336 (as benchmarked): MMA equals LUT4 everywhere, and 24 tokens
+    x 96 weight rows equal the oracle."""
+    M, K, N = 512, 4096, 14336
+    signs, ws, x = wl.prefill_inputs(wl.Rng(4), M, K, N)
+    y, d, q = run_prefill(gq, signs, ws, x, gq.PATH_MMA)
+    y2, _, _ = run_prefill(gq, signs, ws, x, gq.PATH_LUT4)
+    assert_same_bits(y, y2, "mma vs lut4 full")
+    rng = np.random.default_rng(2)
+    ms = np.sort(rng.choice(M, 24, replace=False))
+    ns = np.sort(rng.choice(N, 96, replace=False))
+    want = oracle.prefill_q1s32(signs[ns], ws[ns], d[ms], q[ms], ms.size, ns.size, K)
+    assert_same_bits(y[np.ix_(ms, ns)], want, "mma full sampled")
+    assert gq.device_error() == 0
