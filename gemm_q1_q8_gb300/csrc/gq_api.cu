@@ -146,7 +146,7 @@ int q1s32_q8_gemm(const uint32_t* signs, const float* wscale, const uint16_t* xd
     if (path == GQ_PATH_AUTO) path = (xq_mma && M >= 64) ? GQ_PATH_MMA : GQ_PATH_LUT4;
     if (path != GQ_PATH_LUT4 && path != GQ_PATH_MMA) return GQ_EUNSUPPORTED;
     if (!signs || !wscale || !xd || !xq || !y) return GQ_EINVAL_PTR;
-    if (!aligned(signs, 16) || !aligned(wscale, 4) || !aligned(xd, 2) || !aligned(xq, 16) || !aligned(y, 4))
+    if (!aligned(signs, 16) || !aligned(wscale, 4) || !aligned(xd, 4) || !aligned(xq, 16) || !aligned(y, 4))
         return GQ_EINVAL_PTR;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (path == GQ_PATH_MMA) {

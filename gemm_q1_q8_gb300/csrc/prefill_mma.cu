@@ -31,7 +31,7 @@ constexpr int BM = 128;          // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;          // tokens per tile (MMA N)
 constexpr int BK = 64;           // K per stage (two 32-blocks)
 constexpr int kStagesM = 4;
-constexpr int kAccBufs = 4;      // TMEM accumulators (128 columns each)
+constexpr int kPairs = 2;        // TMEM: two pairs of 128-column accumulators (one pair per stage)
 constexpr int kTmemCols = 512;
 constexpr int kTileA = BM * BK * 2;    // 16 KB
 constexpr int kTileB = BN * BK * 2;    // 16 KB
@@ -44,9 +44,10 @@ constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0
                             (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
 
 struct Bars {
-    uint64_t fullA[kStagesM], fullB[kStagesM], empty[kStagesM];
-    uint64_t tfull[kAccBufs], tempty[kAccBufs];
-    uint64_t done;
+    uint64_t fullA[kStagesM], fullB[kStagesM];
+    uint64_t done[kStagesM];          // a stage's MMAs complete: smem stage free, block sums ready
+    uint64_t tempty[2];               // a TMEM pair drained by the epilogue
+    uint64_t final_;
     uint32_t tmem_base;
     int abort;
 };
@@ -79,21 +80,18 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// 32 lanes x 32 columns of f32 from TMEM into registers (this warp's lane quadrant).
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
-    uint32_t r[32];
+// 32 lanes x 16 columns of f32 from TMEM into registers (this warp's lane quadrant).
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -134,13 +132,10 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
         for (int s = 0; s < kStagesM; ++s) {
             mbar_init(&bars->fullA[s], kNumAWarps);
             mbar_init(&bars->fullB[s], 1);
-            mbar_init(&bars->empty[s], 1);
+            mbar_init(&bars->done[s], 1);
         }
-        for (int b = 0; b < kAccBufs; ++b) {
-            mbar_init(&bars->tfull[b], 1);
-            mbar_init(&bars->tempty[b], kNumEWarps);
-        }
-        mbar_init(&bars->done, 1);
+        for (int p = 0; p < kPairs; ++p) mbar_init(&bars->tempty[p], kNumEWarps);
+        mbar_init(&bars->final_, 1);
         bars->abort = 0;
         fence_barrier_init();
     }
@@ -151,14 +146,6 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     // the epilogue's scale table: sdx[b * BN + j] = f16(xd[m0 + j, b]) for the tile's tokens
-    if (warp >= kWarpE0) {
-        const int t = threadIdx.x - kWarpE0 * 32;
-        for (int idx = t; idx < nbk * BN; idx += kNumEWarps * 32) {
-            const int j = idx / nbk, b = idx % nbk;
-            const int m = min(m0 + j, M - 1);
-            sdx[b * BN + j] = f16_to_f32(xd[static_cast<size_t>(m) * nbk + b]);
-        }
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -172,7 +159,7 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
             for (int k = 0; k < stages; ++k) {
                 const int s = k % kStagesM;
                 if (k >= kStagesM &&
-                    !wait_or_abort(&bars->empty[s], static_cast<uint32_t>(k / kStagesM - 1) & 1u, abort))
+                    !wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStagesM - 1) & 1u, abort))
                     break;
                 mbar_arrive_expect_tx(&bars->fullB[s], kTileB);
                 tma_load_2d(sB + s * kTileB, &tmB, k * BK, m0, &bars->fullB[s]);
@@ -180,68 +167,108 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
             }
         }
     } else if (warp == kWarpMma) {
-        // ---------------- MMA issue (one thread)
+        // ---------------- MMA issue (one thread): one commit per stage
         if (lane == 0) {
             for (int k = 0; k < stages && !*abort; ++k) {
                 const int s = k % kStagesM;
+                const int pair = k % kPairs;
                 const uint32_t ph = static_cast<uint32_t>(k / kStagesM) & 1u;
                 if (!wait_or_abort(&bars->fullA[s], ph, abort) || !wait_or_abort(&bars->fullB[s], ph, abort)) break;
+                if (k >= kPairs &&
+                    !wait_or_abort(&bars->tempty[pair], static_cast<uint32_t>(k / kPairs - 1) & 1u, abort))
+                    break;
                 tc_fence_after();
-                bool ok = true;
-                for (int bi = 0; bi < 2 && ok; ++bi) {
-                    const int b = 2 * k + bi;
-                    const int buf = b % kAccBufs;
-                    if (b >= kAccBufs &&
-                        !wait_or_abort(&bars->tempty[buf], static_cast<uint32_t>(b / kAccBufs - 1) & 1u, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+#pragma unroll
+                for (int bi = 0; bi < 2; ++bi) {
+                    const uint32_t d = tmem + static_cast<uint32_t>((pair * 2 + bi) * BN);
+#pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int koff = (bi * 32 + j * 16) * 2;     // bytes along the 128-byte row
                         tc_mma(d, smem_desc(sA + s * kTileA + koff), smem_desc(sB + s * kTileB + koff), j);
                     }
-                    tc_commit(&bars->tfull[buf]);
                 }
-                if (!ok) break;
-                tc_commit(&bars->empty[s]);
+                tc_commit(&bars->done[s]);
             }
             // all MMAs issued so far complete before TMEM may be freed
-            tc_commit(&bars->done);
+            tc_commit(&bars->final_);
         }
     } else if (warp < kWarpE0) {
-        // ---------------- weight producers: +-1 f16, swizzled K-major, one row per thread
+        // ---------------- weight producers: +-1 f16, swizzled K-major, one row per thread.  The
+        // row's two sign words per stage are loaded 8 bytes at a time, eight stages ahead (rows
+        // are 8-byte aligned: K is a multiple of 64 and the array 16-byte aligned).
         const int r = threadIdx.x - kWarpA0 * 32;                 // 0..127
         const int n = min(n0 + r, N - 1);
-        const uint32_t* srow = signs + static_cast<size_t>(n) * nbk;
-        for (int k = 0; k < stages; ++k) {
-            const int s = k % kStagesM;
-            if (k >= kStagesM &&
-                !wait_or_abort(&bars->empty[s], static_cast<uint32_t>(k / kStagesM - 1) & 1u, abort))
-                break;
-            uint8_t* tileA = sA + s * kTileA + (r >> 3) * 1024 + (r & 7) * 128;
+        const uint2* srow2 = reinterpret_cast<const uint2*>(signs + static_cast<size_t>(n) * nbk);
+        uint2 pf[8];
 #pragma unroll
-            for (int bi = 0; bi < 2; ++bi) {
-                const uint32_t w = __ldg(srow + 2 * k + bi);
+        for (int i = 0; i < 8; ++i) pf[i] = (i < stages) ? __ldg(srow2 + i) : make_uint2(0u, 0u);
+        bool live = true;
+        for (int k0 = 0; k0 < stages && live; k0 += 8) {
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t h[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int u = c4 * 4 + e;        // pair (u, u+16): bits u and u+16 -> signs of two f16
-                        h[e] = ((w << (15 - u)) & 0x80008000u) ^ 0xBC00BC00u;
-                    }
-                    const int chunk = bi * 4 + c4;
-                    *reinterpret_cast<uint4*>(tileA + ((chunk ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            for (int kk = 0; kk < 8; ++kk) {
+                const int k = k0 + kk;
+                if (k >= stages) break;
+                const int s = k % kStagesM;
+                if (k >= kStagesM &&
+                    !wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStagesM - 1) & 1u, abort)) {
+                    live = false;
+                    break;
                 }
+                const uint32_t w2[2] = {pf[kk].x, pf[kk].y};
+                pf[kk] = (k + 8 < stages) ? __ldg(srow2 + k + 8) : make_uint2(0u, 0u);
+                uint8_t* tileA = sA + s * kTileA + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                for (int bi = 0; bi < 2; ++bi) {
+                    const uint32_t w = w2[bi];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t hw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int u = c4 * 4 + e;    // pair (u, u+16): bits u and u+16 -> signs of two f16
+                            hw[e] = ((w << (15 - u)) & 0x80008000u) ^ 0xBC00BC00u;
+                        }
+                        const int chunk = bi * 4 + c4;
+                        *reinterpret_cast<uint4*>(tileA + ((chunk ^ (r & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->fullA[s]);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->fullA[s]);
         }
     } else {
-        // ---------------- epilogue
+        // ---------------- epilogue: the scale table (overlapping the pipeline's start), then per
+        // stage the two block sums of its TMEM pair
+        {
+        // Two scales (one 32-bit word) per load, consecutive threads on consecutive tokens so the
+        // transposed stores are conflict-free; eight independent loads in flight per thread.
+        const int t = threadIdx.x - kWarpE0 * 32;
+        const int pairs = nbk / 2;                            // nbk is even (K % 64 == 0)
+        const int total = pairs * BN;
+        for (int base_i = t; base_i < total; base_i += 8 * kNumEWarps * 32) {
+            uint32_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = base_i + u * kNumEWarps * 32;
+                if (idx < total) {
+                    const int j = idx % BN, bp = idx / BN;
+                    const int m = min(m0 + j, M - 1);
+                    v[u] = __ldg(reinterpret_cast<const uint32_t*>(xd + static_cast<size_t>(m) * nbk) + bp);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = base_i + u * kNumEWarps * 32;
+                if (idx < total) {
+                    const int j = idx % BN, bp = idx / BN;
+                    sdx[(2 * bp) * BN + j] = f16_to_f32(v[u] & 0xFFFFu);
+                    sdx[(2 * bp + 1) * BN + j] = f16_to_f32(v[u] >> 16);
+                }
+            }
+        }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kNumEWarps * 32) : "memory");
         const int q = warp & 3;                        // TMEM lane quadrant of this warp
         const int h = (warp - kWarpE0) >> 2;           // column half
         const int r = q * 32 + lane;                   // row of the tile = TMEM lane
@@ -251,42 +278,57 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
 #pragma unroll
         for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
         bool ok = true;
-        float wnext = __ldg(wrow);
-        for (int b = 0; b < nbk; ++b) {
-            const int buf = b % kAccBufs;
-            const float wsc = wnext;
-            if (b + 1 < nbk) wnext = __ldg(wrow + b + 1);
-            if (!wait_or_abort(&bars->tfull[buf], static_cast<uint32_t>(b / kAccBufs) & 1u, abort)) {
+        float wnx0 = __ldg(wrow), wnx1 = __ldg(wrow + 1);
+        for (int k = 0; k < stages; ++k) {
+            const int s = k % kStagesM;
+            const int pair = k % kPairs;
+            const float wb0 = wnx0, wb1 = wnx1;
+            if (k + 1 < stages) {
+                wnx0 = __ldg(wrow + 2 * k + 2);
+                wnx1 = __ldg(wrow + 2 * k + 3);
+            }
+            if (!wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStagesM) & 1u, abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + h * 64);
-            const float4* dxr = reinterpret_cast<const float4*>(sdx + b * BN + h * 64);
-            const float2 w2 = make_float2(wsc, wsc);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float S[32];
-                tc_ld32(taddr + 32 * half, S);
+            for (int bi = 0; bi < 2; ++bi) {
+                const int b = 2 * k + bi;
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>((pair * 2 + bi) * BN + h * 64);
+                const float4* dxr = reinterpret_cast<const float4*>(sdx + b * BN + h * 64);
+                const float wsc = bi ? wb1 : wb0;
+                const float2 w2 = make_float2(wsc, wsc);
+                // four 16-column parts, the load of part p+1 in flight while part p is applied
+                float Sa[16], Sb[16];
+                tc_ld16(taddr, Sa);
                 tc_wait_ld();
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const int j = half * 32 + 4 * j4;
-                    const float4 dd = dxr[half * 8 + j4];
-                    // p = dx * S (exact), then acc = fma(w_s, p, acc): two separate IEEE steps per column
-                    const float2 p01 = fmul2(make_float2(dd.x, dd.y), make_float2(S[4 * j4], S[4 * j4 + 1]));
-                    const float2 p23 = fmul2(make_float2(dd.z, dd.w), make_float2(S[4 * j4 + 2], S[4 * j4 + 3]));
-                    const float2 a01 = ffma2(w2, p01, make_float2(acc[j], acc[j + 1]));
-                    const float2 a23 = ffma2(w2, p23, make_float2(acc[j + 2], acc[j + 3]));
-                    acc[j] = a01.x;
-                    acc[j + 1] = a01.y;
-                    acc[j + 2] = a23.x;
-                    acc[j + 3] = a23.y;
+                for (int part = 0; part < 4; ++part) {
+                    float* S = (part & 1) ? Sb : Sa;
+                    float* Snext = (part & 1) ? Sa : Sb;
+                    if (part < 3) tc_ld16(taddr + 16 * (part + 1), Snext);
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const int j = part * 16 + 4 * j4;
+                        const float4 dd = dxr[part * 4 + j4];
+                        // p = dx * S (exact), then acc = fma(w_s, p, acc): two separate IEEE steps per column
+                        const float2 p01 = fmul2(make_float2(dd.x, dd.y), make_float2(S[4 * j4], S[4 * j4 + 1]));
+                        const float2 p23 = fmul2(make_float2(dd.z, dd.w), make_float2(S[4 * j4 + 2], S[4 * j4 + 3]));
+                        const float2 a01 = ffma2(w2, p01, make_float2(acc[j], acc[j + 1]));
+                        const float2 a23 = ffma2(w2, p23, make_float2(acc[j + 2], acc[j + 3]));
+                        acc[j] = a01.x;
+                        acc[j + 1] = a01.y;
+                        acc[j + 2] = a23.x;
+                        acc[j + 3] = a23.y;
+                    }
+                    if (part < 3) tc_wait_ld();
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->tempty[buf]);
+            if (lane == 0) mbar_arrive(&bars->tempty[pair]);
         }
         if (ok && n < N) {
 #pragma unroll
@@ -300,7 +342,7 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
     // ---------------- teardown: outstanding MMAs finish, copies land, TMEM is freed
     __syncwarp();
     if (warp == kWarpMma) {
-        if (lane == 0 && !mbar_wait(&bars->done, 0)) report_error(kErrMmaTimeout);
+        if (lane == 0 && !mbar_wait(&bars->final_, 0)) report_error(kErrMmaTimeout);
         __syncwarp();
     }
     if (warp == kWarpTma && lane == 0) {

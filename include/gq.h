@@ -205,7 +205,7 @@ int gq_quantize_q8_0(const float* x_device, int m, int k, uint16_t* d_device, in
  *     acc = fma(w_scale[n, b], p, acc) (correctly rounded), acc from +0.
  *   signs_device   [N, K/32] u32, bit t of word b = weight 32b+t, 1 -> +1 (16-byte aligned)
  *   wscale_device  [N, K/32] f32
- *   xd_device      [M, K/32] f16 bits, xq_device [M, K] int8 (16-byte aligned)
+ *   xd_device      [M, K/32] f16 bits (4-byte aligned), xq_device [M, K] int8 (16-byte aligned)
  *   xq_mma_device  the interleaved f16 operand from gq_quantize_q8_0 (required for
  *                  GQ_PATH_MMA, else may be NULL); it must hold the same q as xq_device, all in
  *                  [-127, 127] (as the quantizer produces)
