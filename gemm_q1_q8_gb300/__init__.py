@@ -16,7 +16,7 @@ from . import build as _build
 
 __all__ = [
     "lib", "GQError", "PATH_AUTO", "PATH_DP4A", "PATH_LUT4", "PATH_MMA",
-    "q1_0_packed_bytes", "q1_0_pack", "q1_q8_gemv", "GroupedGemv", "q1_q8_gemm",
+    "q1_0_packed_bytes", "q1_0_pack", "q1_q8_gemv", "q1_q8_gemv_noalloc", "GroupedGemv", "q1_q8_gemm",
     "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm",
     "device_error", "version",
 ]
@@ -53,6 +53,7 @@ def lib():
             "gq_q1_0_pack": (I, [P, I, I, P, P]),
             "gq_q1_q8_workspace_bytes": (S, [I]),
             "q1_q8_gemv": (I, [P, P, P, I, I, P, P]),
+            "q1_q8_gemv_noalloc": (I, [P, P, P, I, I, P]),
             "gq_gemv_group_plan": (I, [P, I, P]),
             "q1_q8_gemv_grouped": (I, [P, I, I, P, P]),
             "q1_q8_gemm": (I, [P, P, P, I, I, I, I, P]),
@@ -136,6 +137,19 @@ def q1_q8_gemv(packed: torch.Tensor, act: torch.Tensor, rows: int, n: int, out: 
     ws = torch.empty(workspace_bytes(n), dtype=torch.uint8, device=act.device) if workspace is None else workspace
     _need(ws, torch.uint8, workspace_bytes(n), "workspace")
     _check(lib().q1_q8_gemv(_ptr(packed), _ptr(act), _ptr(y), rows, n, _ptr(ws), _stream()), "q1_q8_gemv")
+    return y
+
+
+def q1_q8_gemv_noalloc(packed: torch.Tensor, act: torch.Tensor, rows: int, n: int,
+                       out: torch.Tensor | None = None):
+    """q1_q8_gemv without a caller workspace: the library's built-in scratch block is used (for
+    callers that cannot allocate device memory; n <= 16384; calls must not overlap on the GPU).
+    Only the output tensor, when not given, is allocated here by torch."""
+    _need(act, torch.uint8, (n // 32) * 34, "act")
+    _need(packed, torch.uint8, q1_0_packed_bytes(rows, n), "packed")
+    y = torch.empty(rows, dtype=torch.float32, device=act.device) if out is None else out
+    _need(y, torch.float32, rows, "out")
+    _check(lib().q1_q8_gemv_noalloc(_ptr(packed), _ptr(act), _ptr(y), rows, n, _stream()), "q1_q8_gemv_noalloc")
     return y
 
 

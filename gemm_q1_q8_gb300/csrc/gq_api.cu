@@ -28,6 +28,10 @@ int check_q1(const void* packed, const void* act, const float* y, int rows, int 
 
 }  // namespace
 
+namespace gq {
+void record_cuda_error(int err) { t_last_cuda_error = err; }
+}  // namespace gq
+
 extern "C" {
 
 const char* gq_version(void) { return "gq 0.1.0 (sm_103a)"; }

@@ -156,6 +156,7 @@ size_t gemv_workspace_bytes(int n);
 cudaError_t launch_q1_gemv_grouped(const gq_gemv_desc* descs, int count, int total_tiles, int* counter,
                                    cudaStream_t s);
 int gemv_tiles_for(int rows);
+void record_cuda_error(int err);   // makes err what gq_last_cuda_error() reports on this thread
 cudaError_t launch_q1_gemm(const void* packed, const void* act, float* y, int rows, int n, int cols,
                            int path, cudaStream_t s);
 cudaError_t launch_block_q8(const float* x, const uint32_t* quants, const float* scales, float* y,

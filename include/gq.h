@@ -112,6 +112,25 @@ size_t gq_q1_q8_workspace_bytes(int n);
 int q1_q8_gemv(const void* packed_w_device, const void* act_device, float* y_device,
                int rows, int n, void* workspace_device, gq_stream_t stream);
 
+/* Largest n that q1_q8_gemv_noalloc accepts. */
+#define GQ_NOALLOC_MAX_N 16384
+
+/* The decode GEMV for callers that cannot allocate device memory (code running inside another
+ * allocator's arena, plugins handed raw pointers, paths where an allocation could block or fail):
+ * the same result as q1_q8_gemv, bit for bit, with the workspace taken from a fixed block of
+ * device memory built into the library (about 48 KB, held by every GPU that loads the library
+ * until the process exits).  The pages describe no such variant.
+ *   Arguments as q1_q8_gemv without the workspace; n <= GQ_NOALLOC_MAX_N.
+ *   The first call on each device looks up that block's address (cudaGetSymbolAddress, with the
+ *   device current): make that first call before any stream capture on the device.
+ *   Every call shares the block, so calls whose work overlaps on the GPU (other streams, other
+ *   host threads) race: issue them one after another.  The call itself clears what must start
+ *   at zero.  It calls no allocator (no cudaMalloc / cudaFree, no library that allocates).
+ * Errors: GQ_EINVAL_SHAPE for rows < 1, n < 128, n % 128 != 0 or n > GQ_NOALLOC_MAX_N;
+ *         GQ_EINVAL_PTR as q1_q8_gemv; GQ_ECUDA if the address lookup or a launch fails. */
+int q1_q8_gemv_noalloc(const void* packed_w_device, const void* act_device, float* y_device, int rows,
+                       int n, gq_stream_t stream);
+
 /* One matrix of a grouped GEMV sweep (all fields filled by the caller except tile_begin). */
 typedef struct gq_gemv_desc {
     const void* packed_w;    /* device, from gq_q1_0_pack(rows, n)                      */
