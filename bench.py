@@ -146,11 +146,10 @@ def build_sweep(gq, torch, dev):
     return items, acts_host
 
 
-def extras(gq, torch, dev, hbm_peak, bf16_peak):
-    """Secondary kernels, each timed alone with CUDA events (not part of the headline step)."""
+def bench_block_q8(gq, torch, dev, hbm_peak, steps=40, warmup=5):
+    """block_q8_matmul_nt 49152 x 960 at m = 1, 4, 16; 4 rotating weight copies (4 x 53 MB > L2)."""
     out = {}
     stream = torch.cuda.current_stream()
-    # block_q8_matmul_nt 49152 x 960 at m = 1, 4, 16: 4 rotating weight copies (4 x 53 MB > L2)
     n, k = 49152, 960
     copies = []
     for c in range(4):
@@ -166,13 +165,18 @@ def extras(gq, torch, dev, hbm_peak, bf16_peak):
             i = it[0] % 4
             it[0] += 1
             gq.block_q8_matmul_nt(xs[i], copies[i][1], copies[i][2], out=ys[i])
-        t = time_steps(g, 40, 5, stream) / 40
+        t = time_steps(g, steps, warmup, stream) / steps
         wbytes = n * k + n * (k // 32) * 4
         flops = 2.0 * m * n * k + 2.0 * m * n * (k // 32)
-        out[f"block_q8_m{m}"] = {"us": t * 1e6, "weight_GBps": wbytes / t / 1e9,
-                                 "hbm_frac": wbytes / t / 1e9 / hbm_peak, "GFLOPs": flops / t / 1e9}
-    del copies
-    # ternary 14336 x 4096, batch 1, 4, 16: 8 rotating copies (8 x 14.7 MB > L2)
+        out[f"block_q8_m{m}"] = {"us": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
+                                 "hbm_frac": round(wbytes / t / 1e9 / hbm_peak, 4), "GFLOPs": round(flops / t / 1e9, 1)}
+    return out
+
+
+def bench_ternary(gq, torch, dev, hbm_peak, steps=80, warmup=8):
+    """Ternary 14336 x 4096 at batch 1, 4, 16; 8 rotating copies (8 x 14.7 MB > L2)."""
+    out = {}
+    stream = torch.cuda.current_stream()
     rows, kk = 14336, 4096
     planes = []
     for c in range(8):
@@ -187,12 +191,17 @@ def extras(gq, torch, dev, hbm_peak, bf16_peak):
             i = it[0] % 8
             it[0] += 1
             gq.ternary_bitplane_gemv(planes[i][0], planes[i][1], X, out=y)
-        t = time_steps(f, 80, 8, stream) / 80
+        t = time_steps(f, steps, warmup, stream) / steps
         wbytes = 2 * rows * kk // 8
-        out[f"ternary_b{b}"] = {"us": t * 1e6, "weight_GBps": wbytes / t / 1e9, "hbm_frac": wbytes / t / 1e9 / hbm_peak,
-                                "Gpopc_per_s": rows * (kk // 32) * (b + 2) / t / 1e9}
-    del planes
-    # prefill M=512, K=4096, N=14336: quantize + GEMM (LUT4; MMA when available)
+        out[f"ternary_b{b}"] = {"us": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
+                                "hbm_frac": round(wbytes / t / 1e9 / hbm_peak, 4),
+                                "Gpopc_per_s": round(rows * (kk // 32) * (b + 2) / t / 1e9, 1)}
+    return out
+
+
+def bench_prefill(gq, torch, dev, bf16_peak, steps=5, warmup=2, paths=("lut4", "mma")):
+    """Prefill M=512, K=4096, N=14336: quantize, then the GEMM on each path."""
+    stream = torch.cuda.current_stream()
     M, K, N = 512, 4096, 14336
     signs, ws, x = wl.prefill_inputs(wl.Rng(4), M, K, N)
     ts = torch.from_numpy(signs.view(np.int32)).to(dev)
@@ -202,16 +211,39 @@ def extras(gq, torch, dev, hbm_peak, bf16_peak):
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
     tq = time_steps(lambda: gq.quantize_q8_0(tx, mma_operand=True), 20, 3, stream) / 20
     ops = 2.0 * M * N * K
-    res = {"quantize_us": tq * 1e6}
-    for name, path in (("lut4", gq.PATH_LUT4), ("mma", gq.PATH_MMA)):
-        try:
-            t = time_steps(lambda: gq.q1s32_q8_gemm(ts, tw, d, q, op, path=path, out=y), 5, 2, stream) / 5
-            res[f"{name}_us"] = t * 1e6
-            res[f"{name}_GOPs"] = ops / t / 1e9
-        except gq.GQError as e:
-            res[f"{name}"] = f"unavailable: {e}"
-    out["prefill_512x4096x14336"] = res
+    res = {"quantize_us": round(tq * 1e6, 2)}
+    ids = {"lut4": gq.PATH_LUT4, "mma": gq.PATH_MMA}
+    for name in paths:
+        t = time_steps(lambda: gq.q1s32_q8_gemm(ts, tw, d, q, op, path=ids[name], out=y), steps, warmup, stream) / steps
+        res[f"{name}_us"] = round(t * 1e6, 2)
+        res[f"{name}_GOPs"] = round(ops / t / 1e9, 1)
+    return {"prefill_512x4096x14336": res}
+
+
+def extras(gq, torch, dev, hbm_peak, bf16_peak):
+    """Secondary kernels, each timed alone with CUDA events (not part of the headline step)."""
+    out = {}
+    out.update(bench_block_q8(gq, torch, dev, hbm_peak))
+    out.update(bench_ternary(gq, torch, dev, hbm_peak))
+    out.update(bench_prefill(gq, torch, dev, bf16_peak))
     return out
+
+
+def run_only(args):
+    """One secondary kernel alone (for profiling a single kernel on its workload)."""
+    import torch
+    import gemm_q1_q8_gb300 as gq
+    dev = torch.device("cuda", 0)
+    hbm_peak, bf16_peak, _ = peaks()
+    if args.only == "block_q8":
+        res = bench_block_q8(gq, torch, dev, hbm_peak, steps=args.steps, warmup=args.warmup)
+    elif args.only == "ternary":
+        res = bench_ternary(gq, torch, dev, hbm_peak, steps=args.steps, warmup=args.warmup)
+    elif args.only == "prefill_mma":
+        res = bench_prefill(gq, torch, dev, bf16_peak, steps=args.steps, warmup=args.warmup, paths=("mma",))
+    else:
+        res = bench_prefill(gq, torch, dev, bf16_peak, steps=args.steps, warmup=args.warmup, paths=("lut4",))
+    print(json.dumps({"only": args.only, "kernels": res}), flush=True)
 
 
 def run_ours(args, rank, world, dist):
@@ -358,8 +390,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--only", choices=["block_q8", "ternary", "prefill_lut4", "prefill_mma"], default=None,
+                    help="time one secondary kernel on its workload and print only that")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.only:
+        run_only(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
