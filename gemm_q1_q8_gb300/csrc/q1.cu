@@ -128,43 +128,50 @@ __device__ __forceinline__ float final_reduce(const float2 acc[4]) {
 // Decode GEMV, in two launches.
 //  1. act_prep_kernel builds each activation's constants once per call into the caller's
 //     workspace (per 32-activation sub-block: 8 quant words, 8 seeds, 8 scales = 96 bytes) and
-//     zeroes the unit counter.
-//  2. q1_gemv_kernel: persistent warps.  A unit is 32*RPT rows of one matrix (a 128-row tile or a
-//     part of it); units are handed out through the counter (atomicAdd), largest matrix first, so
-//     the greedy hand-out balances the warps.  Each warp streams its units' (unit, block) chunks --
-//     the unit's sign bits and d0 of the block plus the block's 384 bytes of constants -- through
-//     a private ring of kStages stages: lane 0 refills the stage it has just consumed with the
-//     chunk kStages ahead (grabbing the next unit when the current one is fully requested), so the
-//     copies run ahead across unit boundaries.  The unit of each chunk run travels through a small
-//     per-warp queue; the end of the work is a full-barrier phase completed without data.  Every
-//     wait is bounded, and a warp that gives up first lets its copies in flight land.
+//     zeroes the unit counter.  The GEMV is launched as its programmatic dependent, so the GEMV's
+//     thread blocks are set up while it runs.
+//  2. q1_gemv_kernel: persistent warps.  A unit is a 128-row tile of one matrix (four rows per
+//     lane: each activation word is loaded once for four rows); units are handed out through the
+//     counter, largest matrix first, so the greedy hand-out balances the warps.  Each warp streams
+//     its units' (unit, block) chunks -- the tile's sign bits and d0 of the block plus the
+//     block's 384 bytes of constants -- through a private ring of kStages stages: lane 0 refills
+//     the stage it has just consumed with the chunk kStages ahead, so the copies run ahead across
+//     unit boundaries.  Lane 0 claims the next unit when it requests the last block of the
+//     current one, so the counter's round trip overlaps a block of work.  The unit of each chunk
+//     run travels through a small per-warp queue; the end of the work is a full-barrier phase
+//     completed without data.  Every wait is bounded, and a warp that gives up first lets its
+//     copies in flight land.  A problem with fewer tiles than the grid has warps is spread over
+//     as many SMs as it has tiles.
 // --------------------------------------------------------------------------------------------
-#ifndef GQ_GEMV_RPT
-#define GQ_GEMV_RPT 4
-#endif
-constexpr int kGemvRPT = GQ_GEMV_RPT;                      // rows per lane: a unit is 32*RPT rows
-constexpr int kUnitsPerTile = 4 / kGemvRPT;                // a 128-row tile holds 4/RPT units
-constexpr int kGemvWarps = (kGemvRPT == 4) ? 16 : 20;      // 4 or 5 warps per SMSP
-constexpr int kStages = (kGemvRPT == 4) ? 4 : 6;
-constexpr int kCstBytes = 4 * kConstWords * 4;            // 384: constants of one block
-constexpr int kUnitBits = 32 * kGemvRPT * 16;              // sign bits of one unit and block
-constexpr int kUnitD0 = 32 * kGemvRPT * 2;                 // d0 of one unit and block
-constexpr int kStageBytes = kUnitBits + kUnitD0 + kCstBytes;
+// Measured on GB300 over the BitNet-2B layer sweep: four rows per lane beats one or two rows per
+// lane shared by four or two warps (more warps fit, but the per-row cost of the block constants
+// grows faster than the latency hiding), and cutting the last tiles into block runs that hand
+// their accumulators on (for an even finish) costs as much as the uneven finish it removes.
+constexpr int kGemvR = 4;                                   // rows per lane: a warp covers a tile
+constexpr int kGemvWarps = 16;                              // 4 per SMSP (124 registers each)
+constexpr int kStages = 4;
+constexpr int kCstBytes = 4 * kConstWords * 4;              // 384: constants of one block
+constexpr int kTileBits = kTileRows * 16;                   // sign bits of one (tile, block)
+constexpr int kTileD0 = kTileRows * 2;                      // d0 of one (tile, block)
+constexpr int kStageBytes = kTileBits + kTileD0 + kCstBytes;
 constexpr int kCachedDescs = 2048;                          // tile_begin cached in smem up to this
-constexpr int kUnitQueue = 16;                              // > kStages: units requested ahead
+constexpr int kUnitQueue = 16;                              // > kStages + 1: units requested ahead
+static_assert(kUnitQueue > kStages + 1, "unit queue too short");
 
-struct Fetch {                 // lane 0's cursor over the chunks still to request
-    const uint8_t* base;       // current unit's tile, first chunk
-    const uint8_t* cst;        // its matrix's constants
-    int nb, part, blk, qi;     // blocks, unit part, next block, queue slot of the next unit
-    int issued, live;
+// Lane 0's cursor over the chunks still to request.
+struct Fetcher {
+    const uint8_t* base;   // current unit's tile, first chunk
+    const uint8_t* cst;    // its matrix's constants
+    int blk, blk_end;      // next block to request, blocks of the unit
+    int qi, issued;        // queue slot of the next unit, chunks requested so far
+    int live;
 };
 
 struct __align__(16) WarpSmem {
     uint8_t ring[kStages][kStageBytes];
     uint64_t full[kStages];
     int units[kUnitQueue];
-    Fetch f;
+    Fetcher f;
 };
 
 struct TileInfo {
@@ -206,6 +213,8 @@ __device__ __forceinline__ TileInfo tile_info(const gq_gemv_desc& single, const 
 
 __global__ void __launch_bounds__(256)
 act_prep_kernel(gq_gemv_desc single, const gq_gemv_desc* __restrict__ descs, int count, int* counter) {
+    // the GEMV grid may launch now; its griddepcontrol.wait still waits for this grid's writes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const gq_gemv_desc d = (count == 0) ? single : descs[blockIdx.y];
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *counter = 0;
     const int items = (d.n / 32) * 8;
@@ -222,16 +231,26 @@ act_prep_kernel(gq_gemv_desc single, const gq_gemv_desc* __restrict__ descs, int
     }
 }
 
+struct GemvArgs {
+    gq_gemv_desc single;
+    const gq_gemv_desc* descs;
+    int count;
+    int total_tiles;
+    int active_warps;      // warps per thread block that take part
+    int* counter;
+};
+
 // Lane 0: request the next chunk of the warp's stream into stage `s` (or, once the units have
 // run out, complete that stage's next phase without data after posting -1).
-__device__ __forceinline__ void fetch_next(WarpSmem& ws, int s, const gq_gemv_desc& single,
-                                           const gq_gemv_desc* __restrict__ descs, int count, const int* s_tb,
-                                           int total_units, int* counter) {
-    Fetch& F = ws.f;
+// next_unit is lane 0's register holding the unit claimed when the current unit's last block was
+// requested (its round trip overlaps a block of work).
+__device__ __forceinline__ void fetch_next(WarpSmem& ws, int& next_unit, int s, const GemvArgs& a,
+                                           const int* s_tb) {
+    Fetcher& F = ws.f;
     if (!F.live) return;
-    if (F.blk == F.nb) {                       // current unit fully requested: take the next one
-        const int unit = atomicAdd(counter, 1);
-        if (unit >= total_units) {
+    if (F.blk == F.blk_end) {                  // current unit fully requested: start the next one
+        const int unit = next_unit;
+        if (unit >= a.total_tiles) {
             ws.units[F.qi % kUnitQueue] = -1;
             mbar_arrive(&ws.full[s]);
             ++F.issued;
@@ -240,86 +259,87 @@ __device__ __forceinline__ void fetch_next(WarpSmem& ws, int s, const gq_gemv_de
         }
         ws.units[F.qi % kUnitQueue] = unit;
         ++F.qi;
-        const TileInfo t = tile_info(single, descs, count, s_tb, unit / kUnitsPerTile);
+        const TileInfo t = tile_info(a.single, a.descs, a.count, s_tb, unit);
         F.base = t.base;
         F.cst = t.cst;
-        F.nb = t.nb;
-        F.part = unit % kUnitsPerTile;
         F.blk = 0;
+        F.blk_end = t.nb;
     }
     const uint8_t* ch = F.base + static_cast<size_t>(F.blk) * kChunkBytes;
     mbar_arrive_expect_tx(&ws.full[s], kStageBytes);
-    if (kUnitsPerTile == 1) {
-        bulk_g2s(ws.ring[s], ch, kUnitBits + kUnitD0, &ws.full[s]);
-    } else {
-        bulk_g2s(ws.ring[s], ch + F.part * kUnitBits, kUnitBits, &ws.full[s]);
-        bulk_g2s(ws.ring[s] + kUnitBits, ch + kTileRows * 16 + F.part * kUnitD0, kUnitD0, &ws.full[s]);
-    }
-    bulk_g2s(ws.ring[s] + kUnitBits + kUnitD0, F.cst + static_cast<size_t>(F.blk) * kCstBytes, kCstBytes, &ws.full[s]);
+    bulk_g2s(ws.ring[s], ch, kTileBits + kTileD0, &ws.full[s]);
+    bulk_g2s(ws.ring[s] + kTileBits + kTileD0, F.cst + static_cast<size_t>(F.blk) * kCstBytes, kCstBytes, &ws.full[s]);
     ++F.blk;
     ++F.issued;
+    if (F.blk == F.blk_end) next_unit = atomicAdd(a.counter, 1);     // consumed one block later
+}
+
+// Waits (bounded) for chunk c of the warp's stream.  After a timeout lane 0 lets the copies still
+// in flight land before the warp's shared memory can be released.
+__device__ __forceinline__ bool wait_chunk(WarpSmem& ws, int c, int lane) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&ws.full[c % kStages], static_cast<uint32_t>(c / kStages) & 1u));
+    if (!ok && lane == 0) {
+        report_error(kErrWaitTimeout);
+        for (int cc = c + 1; cc < ws.f.issued; ++cc)
+            if (!mbar_wait(&ws.full[cc % kStages], static_cast<uint32_t>(cc / kStages) & 1u))
+                report_error(kErrDrainTimeout);
+    }
+    return ok;
 }
 
 __global__ void __launch_bounds__(kGemvWarps * 32, 1)
-q1_gemv_kernel(gq_gemv_desc single, const gq_gemv_desc* __restrict__ descs, int count, int total_tiles,
-               int* counter) {
+q1_gemv_kernel(GemvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem)[warp];
     int* s_tb = reinterpret_cast<int*>(smem + sizeof(WarpSmem) * kGemvWarps);
-    if (count > 0 && count <= kCachedDescs)
-        for (int i = threadIdx.x; i < count; i += blockDim.x) s_tb[i] = descs[i].tile_begin;
-    __syncthreads();
-    const int total_units = total_tiles * kUnitsPerTile;
-
-    if (lane == 0) {
+    if (a.count > 0 && a.count <= kCachedDescs)
+        for (int i = threadIdx.x; i < a.count; i += blockDim.x) s_tb[i] = a.descs[i].tile_begin;
+    const bool active = warp < a.active_warps;
+    if (active && lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&ws.full[s], 1);
         fence_barrier_init();
-        ws.f = Fetch{nullptr, nullptr, 0, 0, 0, 0, 0, 1};
-        for (int s = 0; s < kStages; ++s) fetch_next(ws, s, single, descs, count, s_tb, total_units, counter);
+    }
+    __syncthreads();
+    // launched as a programmatic dependent of act_prep_kernel: its constants and the zeroed unit
+    // counter are visible after this wait (a no-op when launched the ordinary way)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!active) return;
+    int next_unit = 0;
+    if (lane == 0) {
+        ws.f = Fetcher{nullptr, nullptr, 0, 0, 0, 0, 1};
+        next_unit = atomicAdd(a.counter, 1);
+        for (int s = 0; s < kStages; ++s) fetch_next(ws, next_unit, s, a, s_tb);
     }
     __syncwarp();
 
     int chunk = 0;
-    auto wait_chunk = [&](int c) -> bool {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&ws.full[c % kStages], static_cast<uint32_t>(c / kStages) & 1u));
-        if (!ok && lane == 0) {
-            // let the copies still in flight land before this warp's shared memory is released
-            report_error(kErrWaitTimeout);
-            for (int cc = c + 1; cc < ws.f.issued; ++cc)
-                if (!mbar_wait(&ws.full[cc % kStages], static_cast<uint32_t>(cc / kStages) & 1u))
-                    report_error(kErrDrainTimeout);
-        }
-        return ok;
-    };
-
     for (int i = 0;; ++i) {
-        if (!wait_chunk(chunk)) return;        // the unit's first chunk, or the end marker
+        if (!wait_chunk(ws, chunk, lane)) return;        // the unit's first chunk, or the end marker
         const int unit = ws.units[i % kUnitQueue];
         if (unit < 0) break;
-        const TileInfo t = tile_info(single, descs, count, s_tb, unit / kUnitsPerTile);
-        const int urow0 = t.row0 + (unit % kUnitsPerTile) * 32 * kGemvRPT;
+        const TileInfo t = tile_info(a.single, a.descs, a.count, s_tb, unit);
 
-        float2 acc[kGemvRPT][4];
+        float2 acc[kGemvR][4];
 #pragma unroll
-        for (int j = 0; j < kGemvRPT; ++j)
+        for (int j = 0; j < kGemvR; ++j)
 #pragma unroll
             for (int p = 0; p < 4; ++p) acc[j][p] = make_float2(0.0f, 0.0f);
 
         for (int blk = 0; blk < t.nb; ++blk, ++chunk) {
             const int s = chunk % kStages;
-            if (blk > 0 && !wait_chunk(chunk)) return;
+            if (blk > 0 && !wait_chunk(ws, chunk, lane)) return;
             const uint8_t* stage = ws.ring[s];
-            uint4 wb[kGemvRPT];
-            float d0[kGemvRPT];
+            uint4 wb[kGemvR];
+            float d0[kGemvR];
 #pragma unroll
-            for (int j = 0; j < kGemvRPT; ++j) {
+            for (int j = 0; j < kGemvR; ++j) {
                 wb[j] = reinterpret_cast<const uint4*>(stage)[lane + 32 * j];
-                d0[j] = f16_to_f32(reinterpret_cast<const uint16_t*>(stage + kUnitBits)[lane + 32 * j]);
+                d0[j] = f16_to_f32(reinterpret_cast<const uint16_t*>(stage + kTileBits)[lane + 32 * j]);
             }
-            const uint4* cst = reinterpret_cast<const uint4*>(stage + kUnitBits + kUnitD0);
+            const uint4* cst = reinterpret_cast<const uint4*>(stage + kTileBits + kTileD0);
 
-            float2 ab[kGemvRPT][4];
+            float2 ab[kGemvR][4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const uint4* cs4 = cst + 6 * k;
@@ -330,7 +350,7 @@ q1_gemv_kernel(gq_gemv_desc single, const gq_gemv_desc* __restrict__ descs, int 
                 const float2 D45 = make_float2(__uint_as_float(dd1.x), __uint_as_float(dd1.y));
                 const float2 D67 = make_float2(__uint_as_float(dd1.z), __uint_as_float(dd1.w));
 #pragma unroll
-                for (int j = 0; j < kGemvRPT; ++j) {
+                for (int j = 0; j < kGemvR; ++j) {
                     const uint32_t w = (k == 0) ? wb[j].x : (k == 1) ? wb[j].y : (k == 2) ? wb[j].z : wb[j].w;
                     float2 tv[4];
                     lane_values(w, q0, q1, s0, s1, tv);
@@ -350,18 +370,18 @@ q1_gemv_kernel(gq_gemv_desc single, const gq_gemv_desc* __restrict__ descs, int 
             __syncwarp();                         // every lane has read the stage
             if (lane == 0) {
                 fence_proxy_async_smem();
-                fetch_next(ws, s, single, descs, count, s_tb, total_units, counter);
+                fetch_next(ws, next_unit, s, a, s_tb);
             }
 #pragma unroll
-            for (int j = 0; j < kGemvRPT; ++j) {
+            for (int j = 0; j < kGemvR; ++j) {
                 const float2 dd = make_float2(d0[j], d0[j]);
 #pragma unroll
                 for (int p = 0; p < 4; ++p) acc[j][p] = ffma2(dd, ab[j][p], acc[j][p]);
             }
         }
 #pragma unroll
-        for (int j = 0; j < kGemvRPT; ++j) {
-            const int row = urow0 + lane + 32 * j;
+        for (int j = 0; j < kGemvR; ++j) {
+            const int row = t.row0 + lane + 32 * j;
             if (row < t.rows) t.y[row] = final_reduce(acc[j]);
         }
     }
@@ -541,8 +561,10 @@ cudaError_t launch_q1_pack(const void* raw, int rows, int n, void* packed, cudaS
 
 int gemv_tiles_for(int rows) { return (rows + kTileRows - 1) / kTileRows; }
 
-// Persistent grid: one thread block per SM (cached per device), fewer for small problems.
-static cudaError_t gemv_grid(int total_tiles, int* grid) {
+// Persistent grid (at most one thread block per SM and resident slot, cached per device).  A
+// problem with fewer tiles than warps in a full grid is spread out: one thread block per tile up
+// to the SM count, with only as many warps per block taking part as the tiles need.
+static cudaError_t gemv_grid(int total_tiles, int* grid, int* active_warps) {
     static int cached[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -559,9 +581,28 @@ static cudaError_t gemv_grid(int total_tiles, int* grid) {
         if (e != cudaSuccess) return e;
         cached[dev] = sms * (per_sm > 0 ? per_sm : 1);
     }
-    const int need = (total_tiles * kUnitsPerTile + kGemvWarps - 1) / kGemvWarps;
-    *grid = need < cached[dev] ? need : cached[dev];
+    const int g = total_tiles < cached[dev] ? total_tiles : cached[dev];
+    int act = (total_tiles + g - 1) / g;
+    if (act > kGemvWarps) act = kGemvWarps;
+    *grid = g;
+    *active_warps = act;
     return cudaSuccess;
+}
+
+// The GEMV grid as a programmatic dependent launch of the act_prep_kernel just queued on `s`: its
+// thread blocks start (shared memory set-up, descriptor cache) while act_prep_kernel still runs.
+static cudaError_t launch_gemv_dependent(int grid, cudaStream_t s, const GemvArgs& args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kGemvWarps * 32);
+    cfg.dynamicSmemBytes = kGemvSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, q1_gemv_kernel, args);
 }
 
 // The activation constants, then 16 bytes for the tile counter.
@@ -570,25 +611,27 @@ size_t gemv_workspace_bytes(int n) { return static_cast<size_t>(n / 32) * kConst
 cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int rows, int n, void* workspace,
                            cudaStream_t s) {
     const int tiles = gemv_tiles_for(rows);
-    int grid = 0;
-    cudaError_t e = gemv_grid(tiles, &grid);
+    int grid = 0, active = 0;
+    cudaError_t e = gemv_grid(tiles, &grid, &active);
     if (e != cudaSuccess) return e;
     int* counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + gemv_workspace_bytes(n) - 16);
     gq_gemv_desc d{packed, act, y, workspace, rows, n, 0, 0};
     act_prep_kernel<<<dim3(8, 1), 256, 0, s>>>(d, nullptr, 0, counter);
-    q1_gemv_kernel<<<grid, kGemvWarps * 32, kGemvSmem, s>>>(d, nullptr, 0, tiles, counter);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_gemv_dependent(grid, s, GemvArgs{d, nullptr, 0, tiles, active, counter});
 }
 
 cudaError_t launch_q1_gemv_grouped(const gq_gemv_desc* descs, int count, int total_tiles, int* counter,
                                    cudaStream_t s) {
-    int grid = 0;
-    cudaError_t e = gemv_grid(total_tiles, &grid);
+    int grid = 0, active = 0;
+    cudaError_t e = gemv_grid(total_tiles, &grid, &active);
     if (e != cudaSuccess) return e;
     gq_gemv_desc none{nullptr, nullptr, nullptr, nullptr, 0, 128, 0, 0};
     act_prep_kernel<<<dim3(8, count), 256, 0, s>>>(none, descs, count, counter);
-    q1_gemv_kernel<<<grid, kGemvWarps * 32, kGemvSmem, s>>>(none, descs, count, total_tiles, counter);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_gemv_dependent(grid, s, GemvArgs{none, descs, count, total_tiles, active, counter});
 }
 
 cudaError_t launch_q1_gemm(const void* packed, const void* act, float* y, int rows, int n, int cols, int path,
