@@ -133,6 +133,29 @@ def time_steps(fn, steps, warmup, stream):
     return start.elapsed_time(end) / 1e3
 
 
+def time_graph(fn, calls, warmup, reps=5):
+    """Device time per call of `fn`: `calls` calls captured in one CUDA graph, replayed `reps`
+    times between CUDA events (no host launch overhead between the kernels)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(reps):
+        g.replay()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3 / (reps * calls)
+
+
 # ----------------------------------------------------------------------------- our arm
 def build_sweep(gq, torch, dev):
     items, acts_host, ys = [], [], []
@@ -147,9 +170,9 @@ def build_sweep(gq, torch, dev):
 
 
 def bench_block_q8(gq, torch, dev, hbm_peak, steps=40, warmup=5):
-    """block_q8_matmul_nt 49152 x 960 at m = 1, 4, 16; 4 rotating weight copies (4 x 53 MB > L2)."""
+    """block_q8_matmul_nt 49152 x 960 at m = 1, 4, 16; 4 rotating weight copies (4 x 53 MB > L2);
+    device time from CUDA-graph replay."""
     out = {}
-    stream = torch.cuda.current_stream()
     n, k = 49152, 960
     copies = []
     for c in range(4):
@@ -165,7 +188,7 @@ def bench_block_q8(gq, torch, dev, hbm_peak, steps=40, warmup=5):
             i = it[0] % 4
             it[0] += 1
             gq.block_q8_matmul_nt(xs[i], copies[i][1], copies[i][2], out=ys[i])
-        t = time_steps(g, steps, warmup, stream) / steps
+        t = time_graph(g, steps, warmup)
         wbytes = n * k + n * (k // 32) * 4
         flops = 2.0 * m * n * k + 2.0 * m * n * (k // 32)
         out[f"block_q8_m{m}"] = {"us": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
@@ -174,9 +197,9 @@ def bench_block_q8(gq, torch, dev, hbm_peak, steps=40, warmup=5):
 
 
 def bench_ternary(gq, torch, dev, hbm_peak, steps=80, warmup=8):
-    """Ternary 14336 x 4096 at batch 1, 4, 16; 8 rotating copies (8 x 14.7 MB > L2)."""
+    """Ternary 14336 x 4096 at batch 1, 4, 16; 8 rotating copies (8 x 14.7 MB > L2); device time
+    from CUDA-graph replay."""
     out = {}
-    stream = torch.cuda.current_stream()
     rows, kk = 14336, 4096
     planes = []
     for c in range(8):
@@ -191,7 +214,7 @@ def bench_ternary(gq, torch, dev, hbm_peak, steps=80, warmup=8):
             i = it[0] % 8
             it[0] += 1
             gq.ternary_bitplane_gemv(planes[i][0], planes[i][1], X, out=y)
-        t = time_steps(f, steps, warmup, stream) / steps
+        t = time_graph(f, steps, warmup)
         wbytes = 2 * rows * kk // 8
         out[f"ternary_b{b}"] = {"us": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
                                 "hbm_frac": round(wbytes / t / 1e9 / hbm_peak, 4),
@@ -221,8 +244,9 @@ def bench_prefill(gq, torch, dev, bf16_peak, steps=5, warmup=2, paths=("lut4", "
 
 
 def extras(gq, torch, dev, hbm_peak, bf16_peak):
-    """Secondary kernels, each timed alone with CUDA events (not part of the headline step)."""
-    out = {}
+    """Secondary kernels, each timed alone (not part of the headline step): block_q8 and ternary
+    by CUDA-graph replay of rotating calls (device time), prefill by CUDA events around calls."""
+    out = {"timing": "block_q8, ternary: CUDA-graph replay (device time per call); prefill: CUDA events per call"}
     out.update(bench_block_q8(gq, torch, dev, hbm_peak))
     out.update(bench_ternary(gq, torch, dev, hbm_peak))
     out.update(bench_prefill(gq, torch, dev, bf16_peak))

@@ -3,11 +3,16 @@
 // Order, bit for bit: per (row, col), block b ascending: block_sum = 0; block_sum = block_sum +
 // x*q for t = 0..31 (a rounded multiply, then a rounded add); acc = acc + scale*block_sum.
 //
-// Each thread owns two weight columns and a tile of MT activation rows: the two columns' chains
-// run side by side (two scalar round-to-nearest products, then one packed f32x2 add: each lane
-// one IEEE operation), the activation tile sits transposed in shared memory (one broadcast load
-// feeds four rows), and an int8 becomes an exact f32 as bits 0x4B0000xx (2^23 + q + 128) minus
-// 2^23 + 128.  The products stay scalar on purpose: ptxas contracts a packed mul.rn.f32x2 that
+// The block sums of a column are independent of one another; only the final `acc` chain runs in
+// block order.  For few activation rows (m <= 4) a thread block covers 32 columns: its warps take the 32-blocks in turn (warp w
+// the blocks w, w+W, ...), each lane one column, so a warp's activation reads are broadcasts and
+// each lane reads its column's 32 bytes of the block directly (the next block's bytes load while
+// the current one is summed).  The scaled block sums (scale*block_sum, rounded) go to shared
+// memory for a pass of blocks, then the thread that owns a (row, column) adds them into its acc in
+// block order.  The activations sit transposed in shared memory (one broadcast load feeds up to four
+// rows), staged once for up to 64 KB of them; an int8 becomes an exact f32 as bits 0x4B0000xx
+// (2^23 + q + 128) minus 2^23 + 128.  Pairs of rows share packed f32x2 adds (each lane one IEEE
+// operation); the products stay scalar on purpose: ptxas contracts a packed mul.rn.f32x2 that
 // feeds a packed add.rn.f32x2 into one fused fma.rn.f32x2 (observed on sm_103a), which would
 // change the rounding of every step; a scalar mul.rn is never contracted.
 #include "gq_internal.cuh"
@@ -15,13 +20,32 @@
 namespace gq {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kKC = 256;                 // activation columns staged per pass (8 blocks)
-constexpr float kQBias = 8388736.0f;     // 2^23 + 128
+constexpr int kColsPerCta = 32;           // one column per lane
+// warps per thread block: 4 for small m (16 blocks per SM, so n = 49152 fits in one wave), 8 for
+// m >= 8 (more rows per lane: fewer, fuller blocks)
+template <int MT>
+__host__ __device__ constexpr int warps_of() { return MT >= 8 ? 8 : 4; }
+constexpr int kXBytes = 64 * 1024;        // activations staged at once (transposed)
+constexpr float kQBias = 8388736.0f;      // 2^23 + 128
 
-// two rounded products, kept out of any contraction
-__device__ __forceinline__ float2 mul_pair(float a, float2 b) {
-    return make_float2(__fmul_rn(a, b.x), __fmul_rn(a, b.y));
+template <int MT>
+__host__ __device__ constexpr int x_stride() { return MT; }   // rows of a staged activation column
+
+// blocks per pass: the scaled block sums of a pass (pass x MT x 32 floats) stay within 32 KB
+template <int MT>
+__host__ __device__ constexpr int pass_blocks() { return MT <= 4 ? 64 : (MT <= 8 ? 32 : 16); }
+
+// k values staged per activation pass: a multiple of 32 * pass_blocks within kXBytes
+template <int MT>
+__host__ __device__ constexpr int x_span() {
+    return kXBytes / (x_stride<MT>() * 4) / (32 * pass_blocks<MT>()) * (32 * pass_blocks<MT>());
+}
+
+template <int MT>
+size_t bq8_smem(int k) {
+    const int span = k < x_span<MT>() ? k : x_span<MT>();   // k is a multiple of 32
+    return static_cast<size_t>(span) * x_stride<MT>() * 4 +
+           static_cast<size_t>(pass_blocks<MT>()) * MT * kColsPerCta * 4;
 }
 
 // element j (0..3) of a word already XORed with 0x80808080, as an exact float
@@ -29,13 +53,165 @@ __device__ __forceinline__ float q_of(uint32_t u, int j) {
     return __int_as_float(static_cast<int>(__byte_perm(u, 0x4B000000u, 0x7540u | j))) - kQBias;
 }
 
+// block_sum[r] += x[r] * q for the MT rows (rounded product, then rounded add; pairs of rows
+// through one packed add)
 template <int MT>
-__global__ void __launch_bounds__(kThreads)
+__device__ __forceinline__ void accumulate_rows(float (&bs)[MT], const float* xr, float q) {
+    if constexpr (MT == 1) {
+        bs[0] = __fadd_rn(bs[0], __fmul_rn(xr[0], q));
+    } else if constexpr (MT == 2) {
+        const float2 xv = *reinterpret_cast<const float2*>(xr);
+        const float2 v = fadd2(make_float2(bs[0], bs[1]), make_float2(__fmul_rn(xv.x, q), __fmul_rn(xv.y, q)));
+        bs[0] = v.x;
+        bs[1] = v.y;
+    } else {
+#pragma unroll
+        for (int r = 0; r < MT; r += 4) {
+            const float4 xv = *reinterpret_cast<const float4*>(xr + r);
+            const float2 lo =
+                fadd2(make_float2(bs[r], bs[r + 1]), make_float2(__fmul_rn(xv.x, q), __fmul_rn(xv.y, q)));
+            bs[r] = lo.x;
+            bs[r + 1] = lo.y;
+            if (r + 2 < MT) {
+                const float2 hi =
+                    fadd2(make_float2(bs[r + 2], bs[r + 3]), make_float2(__fmul_rn(xv.z, q), __fmul_rn(xv.w, q)));
+                bs[r + 2] = hi.x;
+                bs[r + 3] = hi.y;
+            }
+        }
+    }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(warps_of<MT>() * 32)
 block_q8_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants, const float* __restrict__ scales,
                 float* __restrict__ y, int m, int k, int n) {
-    __shared__ __align__(16) float xs[kKC][MT < 4 ? 4 : MT];
+    constexpr int MS = x_stride<MT>();
+    constexpr int PB = pass_blocks<MT>();
+    constexpr int kWarps = warps_of<MT>();
+    constexpr int kThreads = kWarps * 32;
+    constexpr int kOwned = (MT * kColsPerCta + kThreads - 1) / kThreads;   // (row, column) pairs per thread
+    extern __shared__ __align__(16) float smem_f[];
+    const int span = k < x_span<MT>() ? k : x_span<MT>();   // all of k, or whole passes of blocks
+    float* xs = smem_f;                              // [span][MS]
+    float* ps = smem_f + span * MS;                  // [PB][MT][32] scaled block sums of a pass
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int col0 = blockIdx.x * kColsPerCta;
+    const int m0 = blockIdx.y * MT;
+    const int nbk = k / 32;
+    const int cl = min(col0 + lane, n - 1);          // past-the-end columns compute column n-1, store nothing
+    const uint4* qc = reinterpret_cast<const uint4*>(quants) + static_cast<size_t>(cl) * (k / 16);
+    const float* sc = scales + static_cast<size_t>(cl) * nbk;
+
+    float acc[kOwned];
+#pragma unroll
+    for (int o = 0; o < kOwned; ++o) acc[o] = 0.0f;
+
+    for (int pb0 = 0; pb0 < nbk; pb0 += PB) {
+        const int npb = min(PB, nbk - pb0);
+        if ((pb0 * 32) % span == 0) {                // the next pass of activations, transposed
+            __syncthreads();
+            const int kc = pb0 * 32, kx = min(span, k - kc);
+            for (int e = threadIdx.x; e < kx * MS; e += kThreads) {
+                const int tt = e / MS, r = e % MS;
+                xs[tt * MS + r] = (r < MT) ? x[static_cast<size_t>(min(m0 + r, m - 1)) * k + kc + tt] : 0.0f;
+            }
+            __syncthreads();
+        }
+        const float* xp = xs + ((pb0 * 32) % span) * MS;
+        // this warp's blocks of the pass: pb0 + warp, pb0 + warp + kWarps, ...; the next two are
+        // in flight while one is summed
+        uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0, f0 = n0, f1 = n0;
+        float nsc = 0.0f, fsc = 0.0f;
+        if (warp < npb) {
+            n0 = __ldg(qc + 2 * (pb0 + warp));
+            n1 = __ldg(qc + 2 * (pb0 + warp) + 1);
+            nsc = __ldg(sc + pb0 + warp);
+        }
+        if (warp + kWarps < npb) {
+            f0 = __ldg(qc + 2 * (pb0 + warp + kWarps));
+            f1 = __ldg(qc + 2 * (pb0 + warp + kWarps) + 1);
+            fsc = __ldg(sc + pb0 + warp + kWarps);
+        }
+        for (int bl = warp; bl < npb; bl += kWarps) {
+            const uint4 w0 = n0, w1 = n1;
+            const float s = nsc;
+            n0 = f0;
+            n1 = f1;
+            nsc = fsc;
+            if (bl + 2 * kWarps < npb) {
+                f0 = __ldg(qc + 2 * (pb0 + bl + 2 * kWarps));
+                f1 = __ldg(qc + 2 * (pb0 + bl + 2 * kWarps) + 1);
+                fsc = __ldg(sc + pb0 + bl + 2 * kWarps);
+            }
+            const uint32_t wq[8] = {w0.x ^ 0x80808080u, w0.y ^ 0x80808080u, w0.z ^ 0x80808080u,
+                                    w0.w ^ 0x80808080u, w1.x ^ 0x80808080u, w1.y ^ 0x80808080u,
+                                    w1.z ^ 0x80808080u, w1.w ^ 0x80808080u};
+            float bs[MT];
+#pragma unroll
+            for (int r = 0; r < MT; ++r) bs[r] = 0.0f;
+            const float* xb = xp + bl * 32 * MS;
+            if constexpr (MT == 1) {
+                // one broadcast float4 per four activations
+#pragma unroll
+                for (int t4 = 0; t4 < 8; ++t4) {
+                    const float4 xv = *reinterpret_cast<const float4*>(xb + 4 * t4);
+                    bs[0] = __fadd_rn(bs[0], __fmul_rn(xv.x, q_of(wq[t4], 0)));
+                    bs[0] = __fadd_rn(bs[0], __fmul_rn(xv.y, q_of(wq[t4], 1)));
+                    bs[0] = __fadd_rn(bs[0], __fmul_rn(xv.z, q_of(wq[t4], 2)));
+                    bs[0] = __fadd_rn(bs[0], __fmul_rn(xv.w, q_of(wq[t4], 3)));
+                }
+            } else {
+#pragma unroll
+                for (int tt = 0; tt < 32; ++tt) accumulate_rows<MT>(bs, xb + tt * MS, q_of(wq[tt >> 2], tt & 3));
+            }
+#pragma unroll
+            for (int r = 0; r < MT; ++r) ps[(bl * MT + r) * kColsPerCta + lane] = __fmul_rn(s, bs[r]);
+        }
+        __syncthreads();
+        // acc = acc + scale*block_sum, block by block in order, for the owned (row, column) pairs
+#pragma unroll
+        for (int o = 0; o < kOwned; ++o) {
+            const int pr = threadIdx.x + o * kThreads;
+            if (pr < MT * kColsPerCta) {
+                const int r = pr / kColsPerCta, c = pr % kColsPerCta;
+                float a = acc[o];
+                for (int bl = 0; bl < npb; ++bl) a = __fadd_rn(a, ps[(bl * MT + r) * kColsPerCta + c]);
+                acc[o] = a;
+            }
+        }
+        __syncthreads();                              // the pass's sums are read before the next pass
+    }
+#pragma unroll
+    for (int o = 0; o < kOwned; ++o) {
+        const int pr = threadIdx.x + o * kThreads;
+        if (pr < MT * kColsPerCta) {
+            const int r = pr / kColsPerCta, c = pr % kColsPerCta;
+            const int row = m0 + r, col = col0 + c;
+            if (row < m && col < n) y[static_cast<size_t>(row) * n + col] = acc[o];
+        }
+    }
+}
+
+// Many activation rows (m >= 8): each thread owns two weight columns and a tile of MT rows, the
+// two columns' chains side by side (two scalar rounded products, then one packed add), so each
+// broadcast activation load feeds two columns; the activation tile is staged transposed in passes
+// of 256 values.
+constexpr int kPairThreads = 256;
+constexpr int kPairKC = 256;
+
+// two rounded products, kept out of any contraction
+__device__ __forceinline__ float2 pair_products(float a, float2 b) {
+    return make_float2(__fmul_rn(a, b.x), __fmul_rn(a, b.y));
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kPairThreads)
+block_q8_pair_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants, const float* __restrict__ scales,
+                float* __restrict__ y, int m, int k, int n) {
+    __shared__ __align__(16) float xs[kPairKC][MT < 4 ? 4 : MT];
     constexpr int MS = MT < 4 ? 4 : MT;
-    const int col0 = (blockIdx.x * kThreads + threadIdx.x) * 2;
+    const int col0 = (blockIdx.x * kPairThreads + threadIdx.x) * 2;
     const int m0 = blockIdx.y * MT;
     const int ca = min(col0, n - 1), cb = min(col0 + 1, n - 1);
     const int nbk = k / 32;
@@ -46,10 +222,10 @@ block_q8_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants
 #pragma unroll
     for (int r = 0; r < MT; ++r) acc[r] = make_float2(0.0f, 0.0f);
 
-    for (int kc = 0; kc < k; kc += kKC) {
-        const int kn = min(kKC, k - kc);
+    for (int kc = 0; kc < k; kc += kPairKC) {
+        const int kn = min(kPairKC, k - kc);
         __syncthreads();
-        for (int e = threadIdx.x; e < kn * MS; e += kThreads) {
+        for (int e = threadIdx.x; e < kn * MS; e += kPairThreads) {
             const int t = e / MS, r = e % MS;
             xs[t][r] = (r < MT) ? x[static_cast<size_t>(min(m0 + r, m - 1)) * k + kc + t] : 0.0f;
         }
@@ -80,10 +256,10 @@ block_q8_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants
 #pragma unroll
                 for (int r = 0; r < MT; r += 4) {
                     const float4 xv = *reinterpret_cast<const float4*>(xr + r);
-                    bs[r] = fadd2(bs[r], mul_pair(xv.x, qq));
-                    if (r + 1 < MT) bs[r + 1] = fadd2(bs[r + 1], mul_pair(xv.y, qq));
-                    if (r + 2 < MT) bs[r + 2] = fadd2(bs[r + 2], mul_pair(xv.z, qq));
-                    if (r + 3 < MT) bs[r + 3] = fadd2(bs[r + 3], mul_pair(xv.w, qq));
+                    bs[r] = fadd2(bs[r], pair_products(xv.x, qq));
+                    if (r + 1 < MT) bs[r + 1] = fadd2(bs[r + 1], pair_products(xv.y, qq));
+                    if (r + 2 < MT) bs[r + 2] = fadd2(bs[r + 2], pair_products(xv.z, qq));
+                    if (r + 3 < MT) bs[r + 3] = fadd2(bs[r + 3], pair_products(xv.w, qq));
                 }
             }
             const float2 sc = make_float2(__ldg(scales + static_cast<size_t>(ca) * nbk + b),
@@ -108,8 +284,23 @@ block_q8_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants
 template <int MT>
 cudaError_t launch_mt(const float* x, const uint32_t* q, const float* s, float* y, int m, int k, int n,
                       cudaStream_t st) {
-    const dim3 grid((n + 2 * kThreads - 1) / (2 * kThreads), (m + MT - 1) / MT);
-    block_q8_kernel<MT><<<grid, kThreads, 0, st>>>(x, q, s, y, m, k, n);
+    if constexpr (MT >= 8) {
+        const dim3 grid((n + 2 * kPairThreads - 1) / (2 * kPairThreads), (m + MT - 1) / MT);
+        block_q8_pair_kernel<MT><<<grid, kPairThreads, 0, st>>>(x, q, s, y, m, k, n);
+    } else {
+        static int configured_dev = -1;
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (configured_dev != dev) {
+            e = cudaFuncSetAttribute(block_q8_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(bq8_smem<MT>(1 << 30)));
+            if (e != cudaSuccess) return e;
+            configured_dev = dev;
+        }
+        const dim3 grid((n + kColsPerCta - 1) / kColsPerCta, (m + MT - 1) / MT);
+        block_q8_kernel<MT><<<grid, warps_of<MT>() * 32, bq8_smem<MT>(k), st>>>(x, q, s, y, m, k, n);
+    }
     return cudaGetLastError();
 }
 

@@ -6,107 +6,138 @@
 // disjoint when P & N = 0, and a position with both bits set contributes 2 - 2 = 0 either way,
 // so this is the same integer for every input -- one LOP3 and one POPC per word and activation.
 //
-// One thread per weight row; 128-row x 32-word tiles of P and N arrive by TMA with the 128-byte
-// swizzle (conflict-free 16-byte reads per row), together with the matching 32 words of every
-// activation row of the batch group, through a 3-stage mbarrier ring.
+// The result is an integer sum, so K can be cut anywhere without changing it.  A thread block
+// covers `rt` rows (a multiple of 32, sized so that the row tiles fill the GPU once) and up to
+// four 1024-bit K chunks: all of its P, N and X chunks are requested at once by TMA (128-byte
+// swizzle for P/N: conflict-free 16-byte reads per row), and four warp groups -- one per chunk,
+// one thread per row -- count their chunk and add into shared-memory totals.  K beyond four
+// chunks goes to more thread blocks of the same rows, which add their totals into y (zeroed on
+// the stream first); with K <= 4096 y is written once.
 #include "gq_internal.cuh"
 
 namespace gq {
 namespace {
 
-constexpr int kRows = 128;
-constexpr int kWords = 32;          // words per tile row (128 bytes)
-constexpr int kBG = 16;             // activations per pass
-constexpr int kStages = 3;
-constexpr int kTileBytes = kRows * kWords * 4;     // 16 KB per plane
-constexpr int kXBytes = kBG * kWords * 4;          // 2 KB
+constexpr int kWords = 32;                 // words per chunk row (1024 bits, 128 bytes)
+constexpr int kChunksPerCta = 4;           // K chunks per thread block, one warp group each
+constexpr int kChunkRowBytes = kWords * 4;
 
-struct __align__(1024) TernSmem {
-    uint8_t P[kStages][kTileBytes];
-    uint8_t N[kStages][kTileBytes];
-    uint8_t X[kStages][kXBytes];
-    uint64_t bars[kStages];
+struct TernLayout {
+    int rt, batch;
+    uint32_t p_off, n_off, x_off, red_off, pn_off, bar_off, bytes;
 };
 
-__global__ void __launch_bounds__(kRows)
-ternary_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmN,
-               const __grid_constant__ CUtensorMap tmX, int32_t* __restrict__ y, int rows, int k, int batch) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    TernSmem& sm = *reinterpret_cast<TernSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int r = threadIdx.x;
-    const int row0 = blockIdx.x * kRows;
-    const int b0 = blockIdx.y * kBG;
-    const int nb = min(kBG, batch - b0);
-    const int chunks = k / (32 * kWords);
-    const uint32_t stage_bytes = 2 * kTileBytes + static_cast<uint32_t>(kBG) * kWords * 4;
+// Shared memory of one thread block (offsets from a 1024-aligned base).
+__host__ __device__ inline TernLayout tern_layout(int rt, int batch) {
+    TernLayout L{rt, batch, 0, 0, 0, 0, 0, 0, 0};
+    const uint32_t plane = static_cast<uint32_t>(kChunksPerCta) * rt * kChunkRowBytes;   // 1024-multiple
+    L.p_off = 0;
+    L.n_off = plane;
+    L.x_off = 2 * plane;
+    L.red_off = L.x_off + static_cast<uint32_t>(kChunksPerCta) * batch * kChunkRowBytes;
+    L.pn_off = L.red_off + static_cast<uint32_t>(batch) * rt * 4;
+    L.bar_off = (L.pn_off + static_cast<uint32_t>(rt) * 4 + 7) & ~7u;
+    L.bytes = L.bar_off + kChunksPerCta * 8;
+    return L;
+}
 
-    if (r == 0) {
+constexpr int kMaxThreads = 512;          // four per row: up to 128 rows, 128 registers
+
+__global__ void __launch_bounds__(kMaxThreads)
+ternary_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmN,
+               const __grid_constant__ CUtensorMap tmX, int32_t* __restrict__ y, int rows, int k, int batch,
+               int rt, int accumulate) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const TernLayout L = tern_layout(rt, batch);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
+    int* red = reinterpret_cast<int*>(base + L.red_off);      // [batch][rt]
+    int* pnr = reinterpret_cast<int*>(base + L.pn_off);       // [rt]
+    const int g = threadIdx.x / rt, r = threadIdx.x - g * rt;
+    const int row0 = blockIdx.x * rt;
+    const int c0 = blockIdx.y * kChunksPerCta;
+    const int chunks = k / (32 * kWords);
+    const int nch = min(kChunksPerCta, chunks - c0);
+    const uint32_t chunk_bytes = 2u * rt * kChunkRowBytes + static_cast<uint32_t>(batch) * kChunkRowBytes;
+
+    if (threadIdx.x == 0) {
         prefetch_tmap(&tmP);
         prefetch_tmap(&tmN);
         prefetch_tmap(&tmX);
-        for (int s = 0; s < kStages; ++s) mbar_init(&sm.bars[s], 1);
+        for (int c = 0; c < nch; ++c) mbar_init(&bars[c], 1);
         fence_barrier_init();
-        for (int s = 0; s < kStages && s < chunks; ++s) {
-            mbar_arrive_expect_tx(&sm.bars[s], stage_bytes);
-            tma_load_2d(sm.P[s], &tmP, s * kWords, row0, &sm.bars[s]);
-            tma_load_2d(sm.N[s], &tmN, s * kWords, row0, &sm.bars[s]);
-            tma_load_2d(sm.X[s], &tmX, s * kWords, b0, &sm.bars[s]);
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t po = static_cast<uint32_t>(c) * rt * kChunkRowBytes;
+            mbar_arrive_expect_tx(&bars[c], chunk_bytes);
+            tma_load_2d(base + L.p_off + po, &tmP, (c0 + c) * kWords, row0, &bars[c]);
+            tma_load_2d(base + L.n_off + po, &tmN, (c0 + c) * kWords, row0, &bars[c]);
+            tma_load_2d(base + L.x_off + static_cast<uint32_t>(c) * batch * kChunkRowBytes, &tmX, (c0 + c) * kWords, 0,
+                        &bars[c]);
+        }
+    }
+    for (int i = threadIdx.x; i < batch * rt; i += blockDim.x) red[i] = 0;
+    for (int i = threadIdx.x; i < rt; i += blockDim.x) pnr[i] = 0;
+    __syncthreads();
+
+    if (g < nch) {
+        if (!mbar_wait(&bars[g], 0)) {
+            // let the copy land (bounded) before the thread block can exit
+            if (r == 0) {
+                report_error(kErrWaitTimeout);
+                if (!mbar_wait(&bars[g], 0)) report_error(kErrDrainTimeout);
+            }
+        } else {
+            const uint8_t* Pt = base + L.p_off + static_cast<uint32_t>(g) * rt * kChunkRowBytes;
+            const uint8_t* Nt = base + L.n_off + static_cast<uint32_t>(g) * rt * kChunkRowBytes;
+            const uint4* Xt =
+                reinterpret_cast<const uint4*>(base + L.x_off + static_cast<uint32_t>(g) * batch * kChunkRowBytes);
+            // the row's 32 P and N words of this chunk stay in registers for every activation
+            uint4 p4[8], n4[8];
+            int pn = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                p4[j] = *reinterpret_cast<const uint4*>(Pt + swz128(r, j));
+                n4[j] = *reinterpret_cast<const uint4*>(Nt + swz128(r, j));
+                pn += __popc(p4[j].x) + __popc(p4[j].y) + __popc(p4[j].z) + __popc(p4[j].w);
+                pn += __popc(n4[j].x) + __popc(n4[j].y) + __popc(n4[j].z) + __popc(n4[j].w);
+            }
+            atomicAdd(&pnr[r], pn);
+            for (int b = 0; b < batch; ++b) {
+                int cnt = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 x4 = Xt[b * 8 + j];
+                    cnt += __popc((p4[j].x & x4.x) | (n4[j].x & ~x4.x)) + __popc((p4[j].y & x4.y) | (n4[j].y & ~x4.y)) +
+                           __popc((p4[j].z & x4.z) | (n4[j].z & ~x4.z)) + __popc((p4[j].w & x4.w) | (n4[j].w & ~x4.w));
+                }
+                atomicAdd(&red[b * rt + r], cnt);
+            }
         }
     }
     __syncthreads();
-
-    int cnt[kBG];
-#pragma unroll
-    for (int b = 0; b < kBG; ++b) cnt[b] = 0;
-    int pn = 0;
-
-    for (int c = 0; c < chunks; ++c) {
-        const int s = c % kStages;
-        const bool ok = __syncthreads_and(mbar_wait(&sm.bars[s], static_cast<uint32_t>(c / kStages) & 1u));
-        if (!ok) {
-            if (r == 0) {
-                report_error(kErrWaitTimeout);
-                const int last = (c + kStages < chunks ? c + kStages : chunks);
-                for (int cc = c; cc < last; ++cc)
-                    if (!mbar_wait(&sm.bars[cc % kStages], static_cast<uint32_t>(cc / kStages) & 1u))
-                        report_error(kErrDrainTimeout);
-            }
-            __syncthreads();
-            return;
-        }
-        const uint8_t* Pt = sm.P[s];
-        const uint8_t* Nt = sm.N[s];
-        const uint32_t* Xt = reinterpret_cast<const uint32_t*>(sm.X[s]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint4 p4 = *reinterpret_cast<const uint4*>(Pt + swz128(r, j));
-            const uint4 n4 = *reinterpret_cast<const uint4*>(Nt + swz128(r, j));
-            pn += __popc(p4.x) + __popc(p4.y) + __popc(p4.z) + __popc(p4.w);
-            pn += __popc(n4.x) + __popc(n4.y) + __popc(n4.z) + __popc(n4.w);
-#pragma unroll
-            for (int b = 0; b < kBG; ++b) {
-                if (b < nb) {
-                    const uint4 x4 = *reinterpret_cast<const uint4*>(Xt + b * kWords + 4 * j);
-                    cnt[b] += __popc((p4.x & x4.x) | (n4.x & ~x4.x)) + __popc((p4.y & x4.y) | (n4.y & ~x4.y)) +
-                              __popc((p4.z & x4.z) | (n4.z & ~x4.z)) + __popc((p4.w & x4.w) | (n4.w & ~x4.w));
-                }
+    if (g == 0) {
+        const int row = row0 + r;
+        if (row < rows) {
+            for (int b = 0; b < batch; ++b) {
+                const int v = 2 * red[b * rt + r] - pnr[r];
+                int32_t* dst = y + static_cast<size_t>(b) * rows + row;
+                if (accumulate) atomicAdd(dst, v);
+                else *dst = v;
             }
         }
-        __syncthreads();   // stage s fully read
-        if (r == 0 && c + kStages < chunks) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&sm.bars[s], stage_bytes);
-            tma_load_2d(sm.P[s], &tmP, (c + kStages) * kWords, row0, &sm.bars[s]);
-            tma_load_2d(sm.N[s], &tmN, (c + kStages) * kWords, row0, &sm.bars[s]);
-            tma_load_2d(sm.X[s], &tmX, (c + kStages) * kWords, b0, &sm.bars[s]);
-        }
     }
-    const int row = row0 + r;
-    if (row < rows) {
-#pragma unroll
-        for (int b = 0; b < kBG; ++b)
-            if (b < nb) y[static_cast<size_t>(b0 + b) * rows + row] = 2 * cnt[b] - pn;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
     }
+    return cached[dev];
 }
 
 }  // namespace
@@ -115,22 +146,41 @@ GQ_ERROR_ACCESSOR(ternary)
 
 cudaError_t launch_ternary(const uint32_t* P, const uint32_t* N, const uint32_t* X, int32_t* y, int rows, int k,
                            int batch, cudaStream_t s) {
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int chunks = k / (32 * kWords);
+    const int slices = (chunks + kChunksPerCta - 1) / kChunksPerCta;
+    // rows per thread block: the row tiles x K slices fill the GPU about once, within the limits of
+    // threads (four per row) and shared memory
+    int max_rt = kMaxThreads / kChunksPerCta;
+    while (max_rt > 32 && tern_layout(max_rt, batch).bytes + 1024 > 227u * 1024u) max_rt -= 32;
+    const int want_tiles = sms / slices > 0 ? sms / slices : 1;
+    int rt = ((rows + want_tiles - 1) / want_tiles + 31) / 32 * 32;
+    if (rt < 32) rt = 32;
+    if (rt > max_rt) rt = max_rt;
+    const size_t smem = tern_layout(rt, batch).bytes + 1024;
+
     CUtensorMap tmP, tmN, tmX;
     const uint64_t words = static_cast<uint64_t>(k) / 32;
-    if (!make_tmap_2d(&tmP, P, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, words, rows, words * 4, kWords, kRows, true) ||
-        !make_tmap_2d(&tmN, N, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, words, rows, words * 4, kWords, kRows, true) ||
-        !make_tmap_2d(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, words, batch, words * 4, kWords, kBG, false))
+    if (!make_tmap_2d(&tmP, P, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, words, rows, words * 4, kWords, rt, true) ||
+        !make_tmap_2d(&tmN, N, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, words, rows, words * 4, kWords, rt, true) ||
+        !make_tmap_2d(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, words, batch, words * 4, kWords, batch, false))
         return cudaErrorInvalidValue;
-    const size_t smem = sizeof(TernSmem) + 1024;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(ternary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+    if (slices > 1) {
+        const cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(batch) * rows * sizeof(int32_t), s);
         if (e != cudaSuccess) return e;
-        configured = true;
     }
-    const dim3 grid((rows + kRows - 1) / kRows, (batch + kBG - 1) / kBG);
-    ternary_kernel<<<grid, kRows, smem, s>>>(tmP, tmN, tmX, y, rows, k, batch);
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_dev != dev) {
+        e = cudaFuncSetAttribute(ternary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    const dim3 grid((rows + rt - 1) / rt, slices);
+    ternary_kernel<<<grid, kChunksPerCta * rt, smem, s>>>(tmP, tmN, tmX, y, rows, k, batch, rt, slices > 1);
     return cudaGetLastError();
 }
 
