@@ -12,12 +12,17 @@
 // Thread block (one per SM): 128 weight rows x 128 tokens, K in stages of 64 (two 32-blocks).
 //   warp 0      : TMA producer of the activation tiles (f16, interleaved, 128-byte swizzle)
 //   warp 1      : TMEM allocator and MMA issuer (one elected thread)
-//   warps 2-5   : weight producers -- expand sign bits to +-1 f16 in the same swizzled K-major
+//   warps 2-3   : weight producers -- expand sign bits to +-1 f16 in the same swizzled K-major
 //                 layout (pairs (u, u+16) of a 32-block in one 32-bit word, the order the
-//                 quantizer's MMA operand uses)
-//   warps 6-13  : epilogue -- per 32-block, tcgen05.ld of the 128x128 f32 block sums (each warp
-//                 its 32 TMEM lanes x 64 columns), p = dx*S, acc = fma(w_s, p, acc) in registers
-// Four smem stages (A 16 KB + B 16 KB each) and four TMEM accumulators of 128 columns.  Every
+//                 quantizer's MMA operand uses), two rows per thread
+//   warps 4-19  : epilogue -- per 32-block, one tcgen05.ld of the 128x128 f32 block sums (each
+//                 warp its 32 TMEM lanes x 32 columns), p = dx*S, acc = fma(w_s, p, acc) in
+//                 registers; four epilogue warps per SMSP overlap their TMEM load latencies
+// Four smem stages (A 16 KB + B 16 KB each) and four TMEM accumulators of 128 columns.  The weight
+// producers also bring each stage's row scales (2 x 128 f32) into an 8-slot ring, so the epilogue
+// reads them from shared memory.  Slot k % 8 is written again for stage k + 8 only after the MMAs
+// of stage k + 4 completed, which needs every epilogue warp past stage k + 2: the slot's barrier
+// cannot run a phase ahead of an epilogue warp that still has to wait on it.  Every
 // wait is bounded (~1 s); a role that gives up raises an abort flag the others honour, and the
 // block drains its copies and MMAs and frees TMEM before it exits.
 #include "gq_internal.cuh"
@@ -36,8 +41,11 @@ constexpr int kTmemCols = 512;
 constexpr int kTileA = BM * BK * 2;    // 16 KB
 constexpr int kTileB = BN * BK * 2;    // 16 KB
 
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpA0 = 2, kNumAWarps = 4, kWarpE0 = 6, kNumEWarps = 8;
-constexpr int kThreads = (kWarpE0 + kNumEWarps) * 32;   // 448
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpA0 = 2, kNumAWarps = 2, kWarpE0 = 4, kNumEWarps = 16;
+constexpr int kThreads = (kWarpE0 + kNumEWarps) * 32;   // 640
+constexpr int kARowsPerThread = BM / (kNumAWarps * 32);  // 2
+constexpr int kWSlots = 2 * kStagesM;                   // row-scale ring slots
+constexpr int kECols = BN / (kNumEWarps / 4);           // 32 token columns per epilogue warp
 
 // instruction descriptor: D f32, A/B f16, both K-major, N = 128, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0u << 16) |
@@ -47,6 +55,7 @@ struct Bars {
     uint64_t fullA[kStagesM], fullB[kStagesM];
     uint64_t done[kStagesM];          // a stage's MMAs complete: smem stage free, block sums ready
     uint64_t tempty[2];               // a TMEM pair drained by the epilogue
+    uint64_t wfull[2 * kStagesM];     // a row-scale slot written by the producers
     uint64_t final_;
     uint32_t tmem_base;
     int abort;
@@ -80,6 +89,8 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // 32 lanes x 16 columns of f32 from TMEM into registers (this warp's lane quadrant).
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
     uint32_t r[16];
@@ -93,7 +104,6 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Bounded wait that also gives up when another role has raised the abort flag.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -120,7 +130,8 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
     uint8_t* sA = base;                                   // [kStagesM][kTileA]
     uint8_t* sB = base + kStagesM * kTileA;               // [kStagesM][kTileB]
     Bars* bars = reinterpret_cast<Bars*>(sB + kStagesM * kTileB);
-    float* sdx = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + ((sizeof(Bars) + 15) & ~size_t(15)));
+    float* sws = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + ((sizeof(Bars) + 15) & ~size_t(15)));
+    float* sdx = sws + kWSlots * 2 * BM;                  // [slot][bi][row] row scales, then the dx table
     volatile int* abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -135,6 +146,7 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
             mbar_init(&bars->done[s], 1);
         }
         for (int p = 0; p < kPairs; ++p) mbar_init(&bars->tempty[p], kNumEWarps);
+        for (int w = 0; w < kWSlots; ++w) mbar_init(&bars->wfull[w], kNumAWarps);
         mbar_init(&bars->final_, 1);
         bars->abort = 0;
         fence_barrier_init();
@@ -193,19 +205,33 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
             tc_commit(&bars->final_);
         }
     } else if (warp < kWarpE0) {
-        // ---------------- weight producers: +-1 f16, swizzled K-major, one row per thread.  The
-        // row's two sign words per stage are loaded 8 bytes at a time, eight stages ahead (rows
-        // are 8-byte aligned: K is a multiple of 64 and the array 16-byte aligned).
-        const int r = threadIdx.x - kWarpA0 * 32;                 // 0..127
-        const int n = min(n0 + r, N - 1);
-        const uint2* srow2 = reinterpret_cast<const uint2*>(signs + static_cast<size_t>(n) * nbk);
-        uint2 pf[8];
+        // ---------------- weight producers: +-1 f16, swizzled K-major, rows r and r + 64 per
+        // thread.  A row's two sign words and two scales per stage are loaded three stages
+        // ahead, 8 bytes each (rows are 8-byte aligned: K is a multiple of 64, the arrays 16-byte
+        // aligned).
+        const int r0 = threadIdx.x - kWarpA0 * 32;                // 0..63
+        const uint2* srow2[kARowsPerThread];
+        const float2* wrow2[kARowsPerThread];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) pf[i] = (i < stages) ? __ldg(srow2 + i) : make_uint2(0u, 0u);
+        for (int i = 0; i < kARowsPerThread; ++i) {
+            const int n = min(n0 + r0 + i * 64, N - 1);
+            srow2[i] = reinterpret_cast<const uint2*>(signs + static_cast<size_t>(n) * nbk);
+            wrow2[i] = reinterpret_cast<const float2*>(ws + static_cast<size_t>(n) * nbk);
+        }
+        constexpr int kAhead = 3;
+        uint2 pf[kARowsPerThread][kAhead];
+        float2 pw[kARowsPerThread][kAhead];
+#pragma unroll
+        for (int i = 0; i < kARowsPerThread; ++i)
+#pragma unroll
+            for (int a = 0; a < kAhead; ++a) {
+                pf[i][a] = (a < stages) ? __ldg(srow2[i] + a) : make_uint2(0u, 0u);
+                pw[i][a] = (a < stages) ? __ldg(wrow2[i] + a) : make_float2(0.0f, 0.0f);
+            }
         bool live = true;
-        for (int k0 = 0; k0 < stages && live; k0 += 8) {
+        for (int k0 = 0; k0 < stages && live; k0 += kAhead) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < kAhead; ++kk) {
                 const int k = k0 + kk;
                 if (k >= stages) break;
                 const int s = k % kStagesM;
@@ -214,27 +240,39 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
                     live = false;
                     break;
                 }
-                const uint32_t w2[2] = {pf[kk].x, pf[kk].y};
-                pf[kk] = (k + 8 < stages) ? __ldg(srow2 + k + 8) : make_uint2(0u, 0u);
-                uint8_t* tileA = sA + s * kTileA + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-                for (int bi = 0; bi < 2; ++bi) {
-                    const uint32_t w = w2[bi];
+                for (int i = 0; i < kARowsPerThread; ++i) {
+                    const int r = r0 + i * 64;
+                    const uint32_t w2[2] = {pf[i][kk].x, pf[i][kk].y};
+                    pf[i][kk] = (k + kAhead < stages) ? __ldg(srow2[i] + k + kAhead) : make_uint2(0u, 0u);
+                    float* wslot = sws + (k % kWSlots) * 2 * BM;
+                    wslot[r] = pw[i][kk].x;
+                    wslot[BM + r] = pw[i][kk].y;
+                    pw[i][kk] = (k + kAhead < stages) ? __ldg(wrow2[i] + k + kAhead) : make_float2(0.0f, 0.0f);
+                    uint8_t* tileA = sA + s * kTileA + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        uint32_t hw[4];
+                    for (int bi = 0; bi < 2; ++bi) {
+                        const uint32_t w = w2[bi];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int u = c4 * 4 + e;    // pair (u, u+16): bits u and u+16 -> signs of two f16
-                            hw[e] = ((w << (15 - u)) & 0x80008000u) ^ 0xBC00BC00u;
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            uint32_t hw[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int u = c4 * 4 + e;    // pair (u, u+16): bits u and u+16 -> signs of two f16
+                                hw[e] = ((w << (15 - u)) & 0x80008000u) ^ 0xBC00BC00u;
+                            }
+                            const int chunk = bi * 4 + c4;
+                            *reinterpret_cast<uint4*>(tileA + ((chunk ^ (r & 7)) << 4)) =
+                                make_uint4(hw[0], hw[1], hw[2], hw[3]);
                         }
-                        const int chunk = bi * 4 + c4;
-                        *reinterpret_cast<uint4*>(tileA + ((chunk ^ (r & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->fullA[s]);
+                if (lane == 0) {
+                    mbar_arrive(&bars->fullA[s]);
+                    mbar_arrive(&bars->wfull[k % kWSlots]);
+                }
             }
         }
     } else {
@@ -270,52 +308,49 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kNumEWarps * 32) : "memory");
         const int q = warp & 3;                        // TMEM lane quadrant of this warp
-        const int h = (warp - kWarpE0) >> 2;           // column half
+        const int h = (warp - kWarpE0) >> 2;           // column quarter
         const int r = q * 32 + lane;                   // row of the tile = TMEM lane
         const int n = n0 + r;
-        const float* wrow = ws + static_cast<size_t>(min(n, N - 1)) * nbk;
-        float acc[64];
+        float acc[kECols];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < kECols; ++j) acc[j] = 0.0f;
         bool ok = true;
-        float wnx0 = __ldg(wrow), wnx1 = __ldg(wrow + 1);
         for (int k = 0; k < stages; ++k) {
             const int s = k % kStagesM;
             const int pair = k % kPairs;
-            const float wb0 = wnx0, wb1 = wnx1;
-            if (k + 1 < stages) {
-                wnx0 = __ldg(wrow + 2 * k + 2);
-                wnx1 = __ldg(wrow + 2 * k + 3);
-            }
-            if (!wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStagesM) & 1u, abort)) {
+            // done[s]: the stage's block sums are in TMEM; wfull: its row scales are in the ring
+            if (!wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStagesM) & 1u, abort) ||
+                !wait_or_abort(&bars->wfull[k % kWSlots], static_cast<uint32_t>(k / kWSlots) & 1u, abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const float* wslot = sws + (k % kWSlots) * 2 * BM;
+            const float wb0 = wslot[r], wb1 = wslot[BM + r];
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi) {
                 const int b = 2 * k + bi;
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>((pair * 2 + bi) * BN + h * 64);
-                const float4* dxr = reinterpret_cast<const float4*>(sdx + b * BN + h * 64);
+                                       static_cast<uint32_t>((pair * 2 + bi) * BN + h * kECols);
+                const float4* dxr = reinterpret_cast<const float4*>(sdx + b * BN + h * kECols);
                 const float wsc = bi ? wb1 : wb0;
                 const float2 w2 = make_float2(wsc, wsc);
-                // four 16-column parts, the load of part p+1 in flight while part p is applied
-                float Sa[16], Sb[16];
-                tc_ld16(taddr, Sa);
-                tc_wait_ld();
+                // two halves of 16 columns: the half's token scales (shared memory) and block sums
+                // (TMEM) are requested together, so their latencies overlap
 #pragma unroll
-                for (int part = 0; part < 4; ++part) {
-                    float* S = (part & 1) ? Sb : Sa;
-                    float* Snext = (part & 1) ? Sa : Sb;
-                    if (part < 3) tc_ld16(taddr + 16 * (part + 1), Snext);
+                for (int hf = 0; hf < kECols / 16; ++hf) {
+                    float4 dd[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dd[i] = dxr[hf * 4 + i];
+                    float S[16];
+                    tc_ld16(taddr + 16 * hf, S);
+                    tc_wait_ld();
 #pragma unroll
                     for (int j4 = 0; j4 < 4; ++j4) {
-                        const int j = part * 16 + 4 * j4;
-                        const float4 dd = dxr[part * 4 + j4];
+                        const int j = hf * 16 + 4 * j4;
                         // p = dx * S (exact), then acc = fma(w_s, p, acc): two separate IEEE steps per column
-                        const float2 p01 = fmul2(make_float2(dd.x, dd.y), make_float2(S[4 * j4], S[4 * j4 + 1]));
-                        const float2 p23 = fmul2(make_float2(dd.z, dd.w), make_float2(S[4 * j4 + 2], S[4 * j4 + 3]));
+                        const float2 p01 = fmul2(make_float2(dd[j4].x, dd[j4].y), make_float2(S[4 * j4], S[4 * j4 + 1]));
+                        const float2 p23 = fmul2(make_float2(dd[j4].z, dd[j4].w), make_float2(S[4 * j4 + 2], S[4 * j4 + 3]));
                         const float2 a01 = ffma2(w2, p01, make_float2(acc[j], acc[j + 1]));
                         const float2 a23 = ffma2(w2, p23, make_float2(acc[j + 2], acc[j + 3]));
                         acc[j] = a01.x;
@@ -323,7 +358,6 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
                         acc[j + 2] = a23.x;
                         acc[j + 3] = a23.y;
                     }
-                    if (part < 3) tc_wait_ld();
                 }
             }
             tc_fence_before();
@@ -332,8 +366,8 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
         }
         if (ok && n < N) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const int m = m0 + h * 64 + j;
+            for (int j = 0; j < kECols; ++j) {
+                const int m = m0 + h * kECols + j;
                 if (m < M) y[static_cast<size_t>(m) * N + n] = acc[j];
             }
         }
@@ -370,7 +404,7 @@ cudaError_t launch_prefill_mma(const uint32_t* signs, const float* ws, const uin
         return cudaErrorInvalidValue;
     const int nbk = K / 32;
     const size_t smem = 1024 + static_cast<size_t>(kStagesM) * (kTileA + kTileB) + ((sizeof(Bars) + 15) & ~size_t(15)) +
-                        static_cast<size_t>(nbk) * BN * sizeof(float);
+                        static_cast<size_t>(kWSlots) * 2 * BM * sizeof(float) + static_cast<size_t>(nbk) * BN * sizeof(float);
     if (smem > 227 * 1024) return cudaErrorNotSupported;
     static size_t configured = 0;
     if (smem > configured) {
