@@ -60,7 +60,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "25"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -243,6 +243,35 @@ def bench_prefill(gq, torch, dev, bf16_peak, steps=5, warmup=2, paths=("lut4", "
     return {"prefill_512x4096x14336": res}
 
 
+def bench_gemv_shapes(gq, torch, dev, hbm_peak, items, wbytes):
+    """The decode GEMV outside the grouped launch: the 256 x 1024 case per call, and the whole
+    BitNet sweep as 210 single-matrix calls captured in one CUDA graph, per token; device time
+    from graph replay."""
+    out = {}
+    rows, n = 256, 1024
+    w = wl.q1_0_weights(wl.Rng(0), rows, n, scales="uniform")
+    a = wl.q8_0_acts(wl.Rng(0), 1, n, scales="uniform", quants="uniform")
+    packed = gq.q1_0_pack(torch.from_numpy(w).to(dev), rows, n)
+    act = torch.from_numpy(a).to(dev)
+    y = torch.empty(rows, dtype=torch.float32, device=dev)
+    ws = torch.empty(gq.workspace_bytes(n), dtype=torch.uint8, device=dev)
+    t = time_graph(lambda: gq.q1_q8_gemv(packed, act, rows, n, out=y, workspace=ws), 50, 5)
+    out["gemv_256x1024"] = {"us_per_call": round(t * 1e6, 2), "weights_bytes": rows * (n // 128) * 18}
+    wss = [torch.empty(gq.workspace_bytes(nn), dtype=torch.uint8, device=dev) for _, _, _, _, nn in items]
+
+    def sweep():
+        for (pk, ac, yy, r, nn), wsp in zip(items, wss):
+            gq.q1_q8_gemv(pk, ac, r, nn, out=yy, workspace=wsp)
+    t = time_graph(sweep, 1, 2, reps=10)
+    # a matrix with fewer 128-row tiles than SMs takes the one-launch block-parallel kernel,
+    # a larger one the constants launch plus the persistent GEMV
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    launches = sum(1 if (r + 127) // 128 < sms else 2 for _, _, _, r, _ in items)
+    out["sweep_per_matrix_graph"] = {"us_per_token": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
+                                     "hbm_frac": round(wbytes / t / 1e9 / hbm_peak, 4), "launches_per_token": launches}
+    return out
+
+
 def extras(gq, torch, dev, hbm_peak, bf16_peak):
     """Secondary kernels, each timed alone (not part of the headline step): block_q8 and ternary
     by CUDA-graph replay of rotating calls (device time), prefill by CUDA events around calls."""
@@ -315,19 +344,20 @@ def run_ours(args, rank, world, dist):
         for (packed, act, y, r, n), h in zip(items, y_pin):
             h.copy_(y, non_blocking=True)
         stream.synchronize()
+    e2e_steps = min(args.steps, 200)          # host copies make a step ~milliseconds: a rate needs fewer
     for _ in range(args.warmup):
         e2e_step()
     if dist:
         dist.barrier()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(e2e_steps):
         e2e_step()
     te = time.perf_counter() - t0
     if dist:
         tt = torch.tensor([te], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         te = float(tt.item())
-    e2e_value = world * wbytes * args.steps / te / 1e9
+    e2e_value = world * wbytes * e2e_steps / te / 1e9
 
     khash = kernel_hash("q1.cu", "gq_internal.cuh")
     line = {
@@ -344,14 +374,16 @@ def run_ours(args, rank, world, dist):
                      "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peak_src} (hbm_gbs, copy)",
                      "traffic": recorded_traffic("gemv_bitnet_sweep.traffic.json", khash),
                      "algorithmic_bytes_per_launch": wbytes + abytes + ybytes, "kernel_source_hash": khash},
-        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": abytes, "d2h_bytes_per_step": ybytes},
-        "gpu_launches": args.steps,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": abytes, "d2h_bytes_per_step": ybytes,
+                "steps": e2e_steps},
+        "gpu_launches": 2 * args.steps,     # per step: the activation-constants kernel and the GEMV
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     if rank == 0 and not args.no_extras:
         line["kernels"] = extras(gq, torch, dev, hbm_peak, bf16_peak)
+        line["kernels"].update(bench_gemv_shapes(gq, torch, dev, hbm_peak, items, wbytes))
     if gq.device_error() != 0:
         line["device_error"] = True
     return line
@@ -407,7 +439,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")

@@ -391,6 +391,103 @@ q1_gemv_kernel(GemvArgs a) {
 constexpr size_t kGemvSmem = sizeof(WarpSmem) * kGemvWarps + kCachedDescs * sizeof(int);
 
 // --------------------------------------------------------------------------------------------
+// Decode GEMV for a problem that leaves SMs idle (a single matrix with fewer 128-row tiles than
+// the GPU has SMs): one launch, no workspace.  Only acc = fma(d0, ab, acc) runs in block order;
+// the lane sums ab of different blocks are independent.  A thread block covers 32 rows: its
+// kSmallWarps warps take the blocks in turn (warp w the blocks w, w + 16, ...), each lane one
+// row; a warp builds its block's activation constants itself (one (sub-block, lane) item per
+// lane), reads the rows' 16-byte sign words and d0 directly, and leaves ab and d0 in shared
+// memory; warp 0 then runs each row's chain over the pass's blocks in order.
+// --------------------------------------------------------------------------------------------
+constexpr int kSmallWarps = 16;
+constexpr int kSmallPass = 32;            // blocks per pass through shared memory (42 KB static)
+
+__global__ void __launch_bounds__(kSmallWarps * 32)
+q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ act, float* __restrict__ y,
+                     int rows, int nb) {
+    __shared__ __align__(16) float4 s_ab[kSmallPass][2][32];            // ab of (block, row): two float4
+    __shared__ float s_d0[kSmallPass][32];
+    __shared__ __align__(16) uint32_t s_cst[kSmallWarps][4 * kConstWords];  // a warp's current block
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = blockIdx.x * 32;
+    const int rq = row0 % kTileRows;                                     // rows within their tile
+    const uint8_t* tile_base = packed + static_cast<size_t>(row0 / kTileRows) * nb * kChunkBytes;
+    // the cta's rows sit in a whole packed tile (packing pads the last tile), so every read below
+    // stays inside the packed buffer; rows >= `rows` are computed and not stored
+    float2 acc[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) acc[p] = make_float2(0.0f, 0.0f);
+
+    for (int p0 = 0; p0 < nb; p0 += kSmallPass) {
+        const int np = min(kSmallPass, nb - p0);
+        for (int bl = warp; bl < np; bl += kSmallWarps) {
+            const int b = p0 + bl;
+            const uint8_t* ch = tile_base + static_cast<size_t>(b) * kChunkBytes;
+            const uint4 wb = *reinterpret_cast<const uint4*>(ch + (rq + lane) * 16);
+            const float d0 = f16_to_f32(*reinterpret_cast<const uint16_t*>(ch + kTileRows * 16 + (rq + lane) * 2));
+            {
+                const int k = lane >> 3, l = lane & 7;
+                uint32_t qt, seed;
+                float d1s;
+                act_lane_consts(reinterpret_cast<const uint16_t*>(act + static_cast<size_t>(4 * b + k) * 34), l, qt,
+                                seed, d1s);
+                s_cst[warp][k * kConstWords + l] = qt;
+                s_cst[warp][k * kConstWords + 8 + l] = seed;
+                s_cst[warp][k * kConstWords + 16 + l] = __float_as_uint(d1s);
+            }
+            __syncwarp();
+            const uint4* cst = reinterpret_cast<const uint4*>(s_cst[warp]);
+            float2 ab[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4* cs4 = cst + 6 * k;
+                const uint4 q0 = cs4[0], q1 = cs4[1], s0 = cs4[2], s1 = cs4[3];
+                const uint4 dd0 = cs4[4], dd1 = cs4[5];
+                const float2 D01 = make_float2(__uint_as_float(dd0.x), __uint_as_float(dd0.y));
+                const float2 D23 = make_float2(__uint_as_float(dd0.z), __uint_as_float(dd0.w));
+                const float2 D45 = make_float2(__uint_as_float(dd1.x), __uint_as_float(dd1.y));
+                const float2 D67 = make_float2(__uint_as_float(dd1.z), __uint_as_float(dd1.w));
+                const uint32_t w = (k == 0) ? wb.x : (k == 1) ? wb.y : (k == 2) ? wb.z : wb.w;
+                float2 tv[4];
+                lane_values(w, q0, q1, s0, s1, tv);
+                if (k == 0) {
+                    ab[0] = fmul2(D01, tv[0]);
+                    ab[1] = fmul2(D23, tv[1]);
+                    ab[2] = fmul2(D45, tv[2]);
+                    ab[3] = fmul2(D67, tv[3]);
+                } else {
+                    ab[0] = ffma2(D01, tv[0], ab[0]);
+                    ab[1] = ffma2(D23, tv[1], ab[1]);
+                    ab[2] = ffma2(D45, tv[2], ab[2]);
+                    ab[3] = ffma2(D67, tv[3], ab[3]);
+                }
+            }
+            s_ab[bl][0][lane] = make_float4(ab[0].x, ab[0].y, ab[1].x, ab[1].y);
+            s_ab[bl][1][lane] = make_float4(ab[2].x, ab[2].y, ab[3].x, ab[3].y);
+            s_d0[bl][lane] = d0;
+            __syncwarp();                      // the warp's constants are read before the next block
+        }
+        __syncthreads();
+        if (warp == 0) {
+            for (int bl = 0; bl < np; ++bl) {
+                const float d0 = s_d0[bl][lane];
+                const float4 lo = s_ab[bl][0][lane], hi = s_ab[bl][1][lane];
+                const float2 dd = make_float2(d0, d0);
+                acc[0] = ffma2(dd, make_float2(lo.x, lo.y), acc[0]);
+                acc[1] = ffma2(dd, make_float2(lo.z, lo.w), acc[1]);
+                acc[2] = ffma2(dd, make_float2(hi.x, hi.y), acc[2]);
+                acc[3] = ffma2(dd, make_float2(hi.z, hi.w), acc[3]);
+            }
+        }
+        __syncthreads();                       // the pass is consumed before the next overwrites it
+    }
+    if (warp == 0) {
+        const int row = row0 + lane;
+        if (row < rows) y[row] = final_reduce(acc);
+    }
+}
+
+// --------------------------------------------------------------------------------------------
 // Token-tiled GEMM ([P1] Q1_MM4_WGSL: each weight word decoded once for T tokens, past the last
 // token the column is clamped, computed and never stored).  One thread block = one 128-row tile
 // (4 warps x 32 rows, one row per lane) x kTok tokens; all blocks of the tile stream through a
@@ -611,6 +708,21 @@ size_t gemv_workspace_bytes(int n) { return static_cast<size_t>(n / 32) * kConst
 cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int rows, int n, void* workspace,
                            cudaStream_t s) {
     const int tiles = gemv_tiles_for(rows);
+    static int sm_cached[64] = {0};
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (sm_cached[dev] == 0) {
+        e0 = cudaDeviceGetAttribute(&sm_cached[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e0 != cudaSuccess) return e0;
+    }
+    if (tiles < sm_cached[dev]) {
+        // fewer tiles than SMs: the block-parallel kernel (one launch, no workspace)
+        q1_gemv_small_kernel<<<(rows + 31) / 32, kSmallWarps * 32, 0, s>>>(
+            static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(act), y, rows, n / 128);
+        return cudaGetLastError();
+    }
     int grid = 0, active = 0;
     cudaError_t e = gemv_grid(tiles, &grid, &active);
     if (e != cudaSuccess) return e;

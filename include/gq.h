@@ -103,10 +103,11 @@ size_t gq_q1_q8_workspace_bytes(int n);
 /* Decode GEMV ([P1] Q1_DOT_WGSL semantics): y[r] for r < rows.
  *   packed_w_device from gq_q1_0_pack(rows, n); act_device: n/32 Q8_0 blocks (34 bytes each,
  *   2-byte aligned); y_device: rows f32; workspace_device: gq_q1_q8_workspace_bytes(n) bytes,
- *   16-byte aligned, overwritten by the call (two launches on `stream`: the activation's
- *   constants into the workspace, then the GEMV, which hands 128-row tiles to its warps through
- *   a counter at the end of the workspace).  Calls that share a workspace must not overlap on
- *   the GPU.
+ *   16-byte aligned, which the call may overwrite.  A matrix with fewer 128-row tiles than the
+ *   GPU has SMs takes one launch that builds the activation's constants itself and leaves the
+ *   workspace untouched; a larger one takes two launches on `stream` (the constants into the
+ *   workspace, then the GEMV, which hands 128-row tiles to its warps through a counter at the
+ *   end of the workspace).  Calls that share a workspace must not overlap on the GPU.
  * Errors: as gq_q1_0_pack, plus GQ_EINVAL_PTR if act_device is odd, y_device not 4-aligned or
  * the workspace NULL or not 16-aligned. */
 int q1_q8_gemv(const void* packed_w_device, const void* act_device, float* y_device,

@@ -27,7 +27,9 @@ def gemv(gq, w, a, rows, n):
     (129, 640, "page", 3),          # a ragged second tile
     (300, 2560, "page", 4),
     (1000, 6912, "uniform", 5),
-    (77, 16384, "page", 6),         # the largest n the GEMV takes
+    (77, 16384, "page", 6),         # 128 blocks: four passes of the block-parallel kernel
+    (2560, 2560, "uniform", 8),     # a BitNet-2B attention projection
+    (19500, 256, "page", 7),        # 153 tiles: more than the GPU's SMs, the persistent kernel
 ])
 def test_gemv_bit_exact(gq, rows, n, dist, seed):
     rng = wl.Rng(1000 + seed)
