@@ -222,6 +222,28 @@ def bench_ternary(gq, torch, dev, hbm_peak, steps=80, warmup=8):
     return out
 
 
+def bench_w1a32(gq, torch, dev, hbm_peak, steps=40, warmup=5):
+    """Bonsai decode GEMV over f32 activations, 14336 x 4096 at one token; 10 rotating weight
+    copies (10 x 14.7 MB > L2); device time from CUDA-graph replay."""
+    N, K = 14336, 4096
+    copies = []
+    for c in range(10):
+        signs, ws, _ = wl.prefill_inputs(wl.Rng(70 + c), 1, K, N)
+        copies.append((torch.from_numpy(signs.view(np.int32)).to(dev), torch.from_numpy(ws).to(dev)))
+    x = torch.from_numpy(wl.f32_normal(wl.Rng(80), K).reshape(1, K)).to(dev)
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    it = [0]
+
+    def f():
+        i = it[0] % len(copies)
+        it[0] += 1
+        gq.q1s32_f32_gemv(copies[i][0], copies[i][1], x, out=y)
+    t = time_graph(f, steps, warmup)
+    wbytes = N * (K // 32) * 8
+    return {"w1a32_gemv_14336x4096": {"us": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
+                                      "hbm_frac": round(wbytes / t / 1e9 / hbm_peak, 4)}}
+
+
 def bench_prefill(gq, torch, dev, bf16_peak, steps=5, warmup=2, paths=("lut4", "mma")):
     """Prefill M=512, K=4096, N=14336: quantize, then the GEMM on each path."""
     stream = torch.cuda.current_stream()
@@ -275,9 +297,10 @@ def bench_gemv_shapes(gq, torch, dev, hbm_peak, items, wbytes):
 def extras(gq, torch, dev, hbm_peak, bf16_peak):
     """Secondary kernels, each timed alone (not part of the headline step): block_q8 and ternary
     by CUDA-graph replay of rotating calls (device time), prefill by CUDA events around calls."""
-    out = {"timing": "block_q8, ternary: CUDA-graph replay (device time per call); prefill: CUDA events per call"}
+    out = {"timing": "block_q8, ternary, w1a32: CUDA-graph replay (device time per call); prefill: CUDA events per call"}
     out.update(bench_block_q8(gq, torch, dev, hbm_peak))
     out.update(bench_ternary(gq, torch, dev, hbm_peak))
+    out.update(bench_w1a32(gq, torch, dev, hbm_peak))
     out.update(bench_prefill(gq, torch, dev, bf16_peak))
     return out
 
@@ -292,6 +315,8 @@ def run_only(args):
         res = bench_block_q8(gq, torch, dev, hbm_peak, steps=args.steps, warmup=args.warmup)
     elif args.only == "ternary":
         res = bench_ternary(gq, torch, dev, hbm_peak, steps=args.steps, warmup=args.warmup)
+    elif args.only == "w1a32":
+        res = bench_w1a32(gq, torch, dev, hbm_peak, steps=args.steps, warmup=args.warmup)
     elif args.only == "prefill_mma":
         res = bench_prefill(gq, torch, dev, bf16_peak, steps=args.steps, warmup=args.warmup, paths=("mma",))
     else:
@@ -446,7 +471,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
-    ap.add_argument("--only", choices=["block_q8", "ternary", "prefill_lut4", "prefill_mma"], default=None,
+    ap.add_argument("--only", choices=["block_q8", "ternary", "w1a32", "prefill_lut4", "prefill_mma"], default=None,
                     help="time one secondary kernel on its workload and print only that")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -55,6 +55,7 @@ def lib():
             "q1_q8_gemv": (I, [P, P, P, I, I, P, P]),
             "q1_q8_gemv_noalloc": (I, [P, P, P, I, I, P]),
             "gq_gemv_group_plan": (I, [P, I, P]),
+            "q1s32_f32_gemv": (I, [P, P, P, P, I, I, I, P]),
             "q1_q8_gemv_grouped": (I, [P, I, I, P, P]),
             "q1_q8_gemm": (I, [P, P, P, I, I, I, I, P]),
             "block_q8_matmul_nt": (I, [P, P, P, P, I, I, I, P]),
@@ -183,6 +184,22 @@ class GroupedGemv:
     def __call__(self):
         _check(lib().q1_q8_gemv_grouped(_ptr(self.descs), self.count, self.tiles, _ptr(self.counter), _stream()),
                "q1_q8_gemv_grouped")
+
+
+def q1s32_f32_gemv(signs: torch.Tensor, wscale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None):
+    """Bonsai decode GEMV: signs [N, K/32] int32 (u32 bits), wscale [N, K/32] f32, x [M, K] f32 ->
+    y [M, N] f32."""
+    N, nbk = signs.shape
+    M, K = x.shape
+    _need(signs, torch.int32, N * nbk, "signs")
+    _need(wscale, torch.float32, N * nbk, "wscale")
+    _need(x, torch.float32, M * K, "x")
+    if K != 32 * nbk:
+        raise GQError("q1s32_f32_gemv: x has K columns, signs K/32 words per row")
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if out is None else out
+    _need(y, torch.float32, M * N, "out")
+    _check(lib().q1s32_f32_gemv(_ptr(signs), _ptr(wscale), _ptr(x), _ptr(y), N, K, M, _stream()), "q1s32_f32_gemv")
+    return y
 
 
 def q1_q8_gemm(packed: torch.Tensor, act: torch.Tensor, rows: int, n: int, cols: int, path: int = PATH_AUTO,

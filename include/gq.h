@@ -165,6 +165,19 @@ int gq_gemv_group_plan(gq_gemv_desc* descs_host, int count, int* total_tiles);
 int q1_q8_gemv_grouped(const gq_gemv_desc* descs_device, int count, int total_tiles, int* counter_device,
                        gq_stream_t stream);
 
+/* Bonsai decode GEMV over f32 activations ([P3] decode/prefill figure, llama-decode-q1-proj.wgsl):
+ *   y[m * N + n] = sum_b wscale[n * K/32 + b] * sum_t s(n, 32 b + t) * x[m * K + 32 b + t]
+ * with s = +1.0 where bit t of signs[n * K/32 + b] is set, -1.0 where it is clear (the same
+ * weight arrays as q1s32_q8_gemm).  The page does not fix the order of the float operations; this
+ * sums each 32-block in order, accumulates acc = fma(scale, block_sum, acc) per lane, then adds the
+ * warp's lanes: the result is within a small multiple of 2^-24 * sum |terms| of the exact value.
+ *   signs_device: N * K/32 u32; wscale_device: N * K/32 f32; x_device: M * K f32; y_device: M * N
+ *   f32; all 4-byte aligned.  One launch on `stream`.
+ * Errors: GQ_EINVAL_SHAPE unless N >= 1, 1 <= M <= 65535, 32 <= K <= 65536 and K % 32 == 0;
+ *         GQ_EINVAL_PTR for a NULL or misaligned pointer; GQ_ECUDA. */
+int q1s32_f32_gemv(const uint32_t* signs_device, const float* wscale_device, const float* x_device,
+                   float* y_device, int N, int K, int M, gq_stream_t stream);
+
 /* Prefill GEMM over `cols` Q8_0 activation vectors ([P1] Q1_MM_WGSL / Q1_MM4_WGSL): every
  * (row, column) is the GEMV chain above, stored at y[c * rows + r].
  *   act_device: cols * (n/32) Q8_0 blocks, column after column (2-byte aligned).

@@ -54,6 +54,7 @@ def lib():
                 ("gqo_ternary_identity", [P, P, P, P, I, I, I]),
                 ("gqo_quantize_q8_0", [P, I, I, P, P]),
                 ("gqo_prefill_q1s32", [P, P, P, P, P, I, I, I]),
+                ("gqo_q1s32_f32_gemv_f64", [P, P, P, P, I, I, I]),
                 ("gqo_f16_to_f32_array", [P, P, S]),
                 ("gqo_f32_to_f16_array", [P, P, S]),
                 ("gqo_fma_emulated_array", [P, P, P, P, S]),
@@ -172,4 +173,15 @@ def prefill_q1s32(signs, ws, xd, xq, M: int, N: int, K: int) -> np.ndarray:
     assert xd.size == M * K // 32 and xq.size == M * K
     y = np.empty(M * N, dtype=np.float32)
     lib().gqo_prefill_q1s32(_p(signs), _p(ws), _p(xd), _p(xq), _p(y), M, N, K)
+    return y.reshape(M, N)
+
+
+def q1s32_f32_gemv(signs, ws, x, M: int, N: int, K: int) -> np.ndarray:
+    """Bonsai decode GEMV over f32 activations, the f64 definition: y[m, n] (float64)."""
+    signs = np.ascontiguousarray(signs, dtype=np.uint32).reshape(-1)
+    ws = np.ascontiguousarray(ws, dtype=np.float32).reshape(-1)
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    assert signs.size == N * K // 32 and ws.size == signs.size and x.size == M * K
+    y = np.empty(M * N, dtype=np.float64)
+    lib().gqo_q1s32_f32_gemv_f64(_p(signs), _p(ws), _p(x), _p(y), M, N, K)
     return y.reshape(M, N)

@@ -26,6 +26,8 @@
  *    bit 0 -> -q with the int8 wrapping negate), p = d_x * S (exact), acc = fma(w_s, p, acc),
  *    blocks in ascending order from +0.
  *  - block_q8_matmul_nt: products and sums are separate RN operations, as written in the WGSL.
+ *  - Bonsai decode GEMV over f32 activations: the page leaves the float order open, so the
+ *    oracle is the f64 definition and the GPU result is checked within a stated bound.
  *
  * Parity status: every function here is pinned by tests against closed forms, brute force or
  * library routines (see tests/test_oracle_*.py).  Bit-level agreement with bankML's own
@@ -303,6 +305,31 @@ void gqo_prefill_q1s32(const uint32_t* signs, const float* ws, const uint16_t* x
                 }
                 float p = gqo_f16_to_f32(xd[(size_t)m * nbk + b]) * (float)S;
                 acc = fmaf(ws[(size_t)n * nbk + b], p, acc);
+            }
+            y[(size_t)m * N + n] = acc;
+        }
+}
+
+/* [P3] Bonsai decode GEMV over f32 activations (llama-decode-q1-proj.wgsl in the decode/prefill
+ * figure): each weight is +1.0 (bit 1) or -1.0 (bit 0), a 32-weight block carries one f32 scale,
+ * and the page accumulates dot(x4, s4) per four weights into acc with the block's scale.  The
+ * page does not fix the order of the float operations, so this is the plain definition in f64:
+ *   y[m * N + n] = sum_b ws[n, b] * sum_t s(n, 32 b + t) * x[m, 32 b + t],
+ * every product and sum in binary64, blocks and weights in ascending order. */
+void gqo_q1s32_f32_gemv_f64(const uint32_t* signs, const float* ws, const float* x, double* y, int M, int N,
+                            int K) {
+    int nbk = K / QK8_0;
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int b = 0; b < nbk; b++) {
+                uint32_t word = signs[(size_t)n * nbk + b];
+                double d = 0.0;
+                for (int t = 0; t < QK8_0; t++) {
+                    double xv = (double)x[(size_t)m * K + (size_t)b * QK8_0 + t];
+                    d += ((word >> t) & 1u) ? xv : -xv;
+                }
+                acc += (double)ws[(size_t)n * nbk + b] * d;
             }
             y[(size_t)m * N + n] = acc;
         }

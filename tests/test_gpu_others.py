@@ -158,3 +158,49 @@ def test_prefill_mma_full_size_sampled(gq):
     want = oracle.prefill_q1s32(signs[ns], ws[ns], d[ms], q[ms], ms.size, ns.size, K)
     assert_same_bits(y[np.ix_(ms, ns)], want, "mma full sampled")
     assert gq.device_error() == 0
+
+
+# ----------------------------------------------------------------------------- Bonsai W1A32 decode
+
+def _w1a32_bound(ws, x):
+    """The kernel's order (32-term block sums, fma per block, 5-level lane butterfly) has depth
+    < 64, so |got - exact| <= 64 * 2^-24 * sum |terms| (gamma_n bound); the f64 oracle is far tighter."""
+    M, K = x.shape
+    N, nbk = ws.shape
+    ax = np.abs(x.astype(np.float64)).reshape(M, nbk, 32).sum(axis=2)       # [M, nbk]
+    terms = ax @ np.abs(ws.astype(np.float64)).T                             # [M, N]
+    return 64 * 2.0 ** -24 * terms
+
+
+def test_w1a32_exact_special_case(gq):
+    """Integer activations and power-of-two scales: every partial sum is exact in f32, so the GPU
+    result equals the exact value bit for bit, whatever the order."""
+    M, N, K = 2, 77, 1024
+    rng = wl.Rng(33)
+    signs = rng.u32(N * K // 32).reshape(N, K // 32)
+    ws = (2.0 ** -(2 + (rng.u32(N * K // 32) % 5).astype(np.int64))).astype(np.float32).reshape(N, K // 32)
+    x = ((rng.u32(M * K) % 17).astype(np.int64) - 8).astype(np.float32).reshape(M, K)
+    y = gq.q1s32_f32_gemv(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x)).cpu().numpy()
+    want = oracle.q1s32_f32_gemv(signs, ws, x, M, N, K)
+    assert np.array_equal(y.astype(np.float64), want)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 32), (1, 33, 96), (3, 130, 1024), (1, 300, 8224), (2, 64, 4096)])
+def test_w1a32_within_bound(gq, M, N, K):
+    signs, ws, x = wl.prefill_inputs(wl.Rng(M + N + K), M, K, N)
+    y = gq.q1s32_f32_gemv(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x)).cpu().numpy()
+    want = oracle.q1s32_f32_gemv(signs, ws, x, M, N, K)
+    err = np.abs(y.astype(np.float64) - want)
+    assert np.all(err <= _w1a32_bound(ws, x)), f"max err {err.max()}"
+    # and the pages' tolerance where the result is not a cancellation
+    big = np.abs(want) > 1e-2 * _w1a32_bound(ws, x) / (64 * 2.0 ** -24)
+    assert np.all(err[big] <= 1e-4 * np.abs(want[big]) + 1e-6)
+
+
+def test_w1a32_full_size(gq):
+    """The 14336 x 4096 Bonsai projection at one token, every row against the f64 oracle."""
+    M, N, K = 1, 14336, 4096
+    signs, ws, x = wl.prefill_inputs(wl.Rng(5), M, K, N)
+    y = gq.q1s32_f32_gemv(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x)).cpu().numpy()
+    want = oracle.q1s32_f32_gemv(signs, ws, x, M, N, K)
+    assert np.all(np.abs(y.astype(np.float64) - want) <= _w1a32_bound(ws, x))

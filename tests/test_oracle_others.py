@@ -212,3 +212,65 @@ def test_prefill_single_rounding_and_wrap():
     xq[0, 64:68] = -128
     y = oracle.prefill_q1s32(signs, ws, xd, xq, 1, 1, K)
     assert hex(int(y.view(np.uint32)[0, 0])) == "0x39fe0000"
+
+
+# ----------------------------------------------------------------------------- Bonsai W1A32 decode
+# [P3] decode/prefill figure, llama-decode-q1-proj.wgsl: weight = +1 (bit 1) or -1 (bit 0), one f32
+# scale per 32 weights, f32 activations; the oracle is the f64 definition.
+
+def _w1a32_exact(signs, ws, x, M, N, K):
+    """Exact rational y[m][n] = sum_b ws * sum_t s * x (every f32 input is an exact rational)."""
+    nbk = K // 32
+    out = [[Fraction(0)] * N for _ in range(M)]
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for b in range(nbk):
+                word = int(signs[n, b])
+                d = Fraction(0)
+                for t in range(32):
+                    xv = Fraction(float(x[m, 32 * b + t]))
+                    d += xv if (word >> t) & 1 else -xv
+                acc += Fraction(float(ws[n, b])) * d
+            out[m][n] = acc
+    return out
+
+
+def test_w1a32_within_f64_bound_of_exact():
+    M, N, K = 2, 5, 96
+    signs, ws, x = wl.prefill_inputs(wl.Rng(31), M, K, N)
+    got = oracle.q1s32_f32_gemv(signs, ws, x, M, N, K)
+    exact = _w1a32_exact(signs, ws, x, M, N, K)
+    nbk = K // 32
+    for m in range(M):
+        for n in range(N):
+            terms = sum(abs(float(ws[n, b])) * sum(abs(float(x[m, 32 * b + t])) for t in range(32)) for b in range(nbk))
+            bound = (K + nbk + 2) * 2.0 ** -53 * terms
+            assert abs(Fraction(float(got[m, n])) - exact[m][n]) <= Fraction(bound)
+
+
+def test_w1a32_exact_special_case():
+    """Integer activations in [-8, 8] and power-of-two scales: every partial sum is exact in f64 (and
+    in f32), so the oracle equals the exact value bit for bit."""
+    M, N, K = 3, 7, 160
+    rng = wl.Rng(32)
+    signs = rng.u32(N * K // 32).reshape(N, K // 32)
+    ws = (2.0 ** -(2 + (rng.u32(N * K // 32) % 5).astype(np.int64))).astype(np.float32).reshape(N, K // 32)
+    x = ((rng.u32(M * K) % 17).astype(np.int64) - 8).astype(np.float32).reshape(M, K)
+    got = oracle.q1s32_f32_gemv(signs, ws, x, M, N, K)
+    exact = _w1a32_exact(signs, ws, x, M, N, K)
+    for m in range(M):
+        for n in range(N):
+            assert Fraction(float(got[m, n])) == exact[m][n]
+
+
+def test_w1a32_sign_convention():
+    """One block: all bits set gives +ws * sum(x), none gives -ws * sum(x), a single set bit t gives
+    ws * (2 x_t - sum(x))."""
+    K = 32
+    x = np.arange(1, 33, dtype=np.float32).reshape(1, K)
+    total = float(x.sum())
+    ws = np.array([[0.5]], dtype=np.float32)
+    for word, want in [(0xFFFFFFFF, 0.5 * total), (0x0, -0.5 * total), (1 << 5, 0.5 * (2 * 6.0 - total))]:
+        got = oracle.q1s32_f32_gemv(np.array([[word]], dtype=np.uint32), ws, x, 1, 1, K)
+        assert got[0, 0] == want
