@@ -223,8 +223,9 @@ def bench_ternary(gq, torch, dev, hbm_peak, steps=80, warmup=8):
 
 
 def bench_w1a32(gq, torch, dev, hbm_peak, steps=40, warmup=5):
-    """Bonsai decode GEMV over f32 activations, 14336 x 4096 at one token; 10 rotating weight
-    copies (10 x 14.7 MB > L2); device time from CUDA-graph replay."""
+    """Bonsai 1-bit weights x f32 activations.  Decode: 14336 x 4096 at one token, 10 rotating
+    weight copies (10 x 14.7 MB > L2), both paths, device time from CUDA-graph replay.  Prefill:
+    512 tokens through the LUT4 path (and FMA for comparison)."""
     N, K = 14336, 4096
     copies = []
     for c in range(10):
@@ -232,16 +233,30 @@ def bench_w1a32(gq, torch, dev, hbm_peak, steps=40, warmup=5):
         copies.append((torch.from_numpy(signs.view(np.int32)).to(dev), torch.from_numpy(ws).to(dev)))
     x = torch.from_numpy(wl.f32_normal(wl.Rng(80), K).reshape(1, K)).to(dev)
     y = torch.empty((1, N), dtype=torch.float32, device=dev)
-    it = [0]
-
-    def f():
-        i = it[0] % len(copies)
-        it[0] += 1
-        gq.q1s32_f32_gemv(copies[i][0], copies[i][1], x, out=y)
-    t = time_graph(f, steps, warmup)
     wbytes = N * (K // 32) * 8
-    return {"w1a32_gemv_14336x4096": {"us": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
-                                      "hbm_frac": round(wbytes / t / 1e9 / hbm_peak, 4)}}
+    dec = {}
+    for name, path in (("lut4", gq.PATH_LUT4), ("fma", gq.PATH_FMA)):
+        it = [0]
+
+        def f():
+            i = it[0] % len(copies)
+            it[0] += 1
+            gq.q1s32_f32_gemm(copies[i][0], copies[i][1], x, path=path, out=y)
+        t = time_graph(f, steps, warmup)
+        dec[f"{name}_us"] = round(t * 1e6, 2)
+        dec[f"{name}_weight_GBps"] = round(wbytes / t / 1e9, 1)
+        dec[f"{name}_hbm_frac"] = round(wbytes / t / 1e9 / hbm_peak, 4)
+    M = 512
+    xp = torch.from_numpy(wl.f32_normal(wl.Rng(81), M * K).reshape(M, K)).to(dev)
+    yp = torch.empty((M, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    pre = {}
+    for name, path, n in (("lut4", gq.PATH_LUT4, 10), ("fma", gq.PATH_FMA, 2)):
+        t = time_steps(lambda: gq.q1s32_f32_gemm(copies[0][0], copies[0][1], xp, path=path, out=yp), n, 2,
+                       stream) / n
+        pre[f"{name}_us"] = round(t * 1e6, 1)
+        pre[f"{name}_Glookups_per_s"] = round(M * N * K / 4 / t / 1e9, 1)
+    return {"w1a32_decode_14336x4096": dec, "w1a32_prefill_512x4096x14336": pre}
 
 
 def bench_prefill(gq, torch, dev, bf16_peak, steps=5, warmup=2, paths=("lut4", "mma")):

@@ -15,13 +15,13 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "lib", "GQError", "PATH_AUTO", "PATH_DP4A", "PATH_LUT4", "PATH_MMA",
+    "lib", "GQError", "PATH_AUTO", "PATH_DP4A", "PATH_LUT4", "PATH_MMA", "PATH_FMA",
     "q1_0_packed_bytes", "q1_0_pack", "q1_q8_gemv", "q1_q8_gemv_noalloc", "GroupedGemv", "q1_q8_gemm",
     "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm",
     "device_error", "version",
 ]
 
-PATH_AUTO, PATH_DP4A, PATH_LUT4, PATH_MMA = 0, 1, 2, 3
+PATH_AUTO, PATH_DP4A, PATH_LUT4, PATH_MMA, PATH_FMA = 0, 1, 2, 3, 4
 _LIB = None
 
 
@@ -55,7 +55,7 @@ def lib():
             "q1_q8_gemv": (I, [P, P, P, I, I, P, P]),
             "q1_q8_gemv_noalloc": (I, [P, P, P, I, I, P]),
             "gq_gemv_group_plan": (I, [P, I, P]),
-            "q1s32_f32_gemv": (I, [P, P, P, P, I, I, I, P]),
+            "q1s32_f32_gemm": (I, [P, P, P, P, I, I, I, I, P]),
             "q1_q8_gemv_grouped": (I, [P, I, I, P, P]),
             "q1_q8_gemm": (I, [P, P, P, I, I, I, I, P]),
             "block_q8_matmul_nt": (I, [P, P, P, P, I, I, I, P]),
@@ -186,19 +186,22 @@ class GroupedGemv:
                "q1_q8_gemv_grouped")
 
 
-def q1s32_f32_gemv(signs: torch.Tensor, wscale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None):
-    """Bonsai decode GEMV: signs [N, K/32] int32 (u32 bits), wscale [N, K/32] f32, x [M, K] f32 ->
-    y [M, N] f32."""
+def q1s32_f32_gemm(signs: torch.Tensor, wscale: torch.Tensor, x: torch.Tensor, path: int = PATH_AUTO,
+                   out: torch.Tensor | None = None):
+    """Bonsai 1-bit weights times f32 activations: signs [N, K/32] int32 (u32 bits), wscale
+    [N, K/32] f32, x [M, K] f32 (16-byte aligned) -> y [M, N] f32.  path: PATH_LUT4 (AUTO) or
+    PATH_FMA."""
     N, nbk = signs.shape
     M, K = x.shape
     _need(signs, torch.int32, N * nbk, "signs")
     _need(wscale, torch.float32, N * nbk, "wscale")
     _need(x, torch.float32, M * K, "x")
     if K != 32 * nbk:
-        raise GQError("q1s32_f32_gemv: x has K columns, signs K/32 words per row")
+        raise GQError("q1s32_f32_gemm: x has K columns, signs K/32 words per row")
     y = torch.empty((M, N), dtype=torch.float32, device=x.device) if out is None else out
     _need(y, torch.float32, M * N, "out")
-    _check(lib().q1s32_f32_gemv(_ptr(signs), _ptr(wscale), _ptr(x), _ptr(y), N, K, M, _stream()), "q1s32_f32_gemv")
+    _check(lib().q1s32_f32_gemm(_ptr(signs), _ptr(wscale), _ptr(x), _ptr(y), M, N, K, path, _stream()),
+           "q1s32_f32_gemm")
     return y
 
 

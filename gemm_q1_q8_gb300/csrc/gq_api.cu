@@ -129,12 +129,15 @@ int block_q8_matmul_nt(const float* x, const uint32_t* quants, const float* scal
     return cuda_status(gq::launch_block_q8(x, quants, scales, y, m, k, n, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int q1s32_f32_gemv(const uint32_t* signs, const float* wscale, const float* x, float* y, int N, int K, int M,
+int q1s32_f32_gemm(const uint32_t* signs, const float* wscale, const float* x, float* y, int M, int N, int K, int path,
                    gq_stream_t stream) {
     if (N < 1 || M < 1 || M > 65535 || K < 32 || K % 32 != 0 || K > kMaxK) return GQ_EINVAL_SHAPE;
+    if (path == GQ_PATH_AUTO) path = GQ_PATH_LUT4;
+    if (path != GQ_PATH_LUT4 && path != GQ_PATH_FMA) return GQ_EUNSUPPORTED;
     if (!signs || !wscale || !x || !y) return GQ_EINVAL_PTR;
-    if (!aligned(signs, 4) || !aligned(wscale, 4) || !aligned(x, 4) || !aligned(y, 4)) return GQ_EINVAL_PTR;
-    return cuda_status(gq::launch_q1s32_f32_gemv(signs, wscale, x, y, N, K, M, reinterpret_cast<cudaStream_t>(stream)));
+    if (!aligned(signs, 4) || !aligned(wscale, 4) || !aligned(x, 16) || !aligned(y, 4)) return GQ_EINVAL_PTR;
+    return cuda_status(
+        gq::launch_q1s32_f32(signs, wscale, x, y, M, N, K, path, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int ternary_bitplane_gemv(const uint32_t* P, const uint32_t* N, const uint32_t* X, int32_t* y, int rows, int k,

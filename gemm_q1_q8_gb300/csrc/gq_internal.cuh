@@ -153,8 +153,8 @@ cudaError_t launch_q1_pack(const void* raw, int rows, int n, void* packed, cudaS
 cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int rows, int n, void* workspace,
                            cudaStream_t s);
 size_t gemv_workspace_bytes(int n);
-cudaError_t launch_q1s32_f32_gemv(const uint32_t* signs, const float* ws, const float* x, float* y, int N, int K,
-                                  int M, cudaStream_t s);
+cudaError_t launch_q1s32_f32(const uint32_t* signs, const float* ws, const float* x, float* y, int M, int N, int K,
+                             int path, cudaStream_t s);   // path: GQ_PATH_FMA or GQ_PATH_LUT4
 cudaError_t launch_q1_gemv_grouped(const gq_gemv_desc* descs, int count, int total_tiles, int* counter,
                                    cudaStream_t s);
 int gemv_tiles_for(int rows);

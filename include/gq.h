@@ -51,7 +51,8 @@ enum gq_path {
     GQ_PATH_AUTO = 0,      /* the library picks by shape                                    */
     GQ_PATH_DP4A = 1,      /* integer dot products (dp4a) on the CUDA cores                 */
     GQ_PATH_LUT4 = 2,      /* 16-entry subset-sum tables per 4 activations, nibble lookups  */
-    GQ_PATH_MMA = 3        /* tcgen05 tensor-core MMA (kind::f16) with a fixed-order epilogue */
+    GQ_PATH_MMA = 3,       /* tcgen05 tensor-core MMA (kind::f16) with a fixed-order epilogue */
+    GQ_PATH_FMA = 4        /* weights expanded to +-1.0 and multiply-added on the CUDA cores  */
 };
 
 /* Library version string (static storage). */
@@ -165,18 +166,28 @@ int gq_gemv_group_plan(gq_gemv_desc* descs_host, int count, int* total_tiles);
 int q1_q8_gemv_grouped(const gq_gemv_desc* descs_device, int count, int total_tiles, int* counter_device,
                        gq_stream_t stream);
 
-/* Bonsai decode GEMV over f32 activations ([P3] decode/prefill figure, llama-decode-q1-proj.wgsl):
+/* Bonsai 1-bit weights times f32 activations ([P3] decode/prefill figure: the decode kernel
+ * llama-decode-q1-proj.wgsl and the prefill kernel binary-lut4-matmul.wgsl):
  *   y[m * N + n] = sum_b wscale[n * K/32 + b] * sum_t s(n, 32 b + t) * x[m * K + 32 b + t]
  * with s = +1.0 where bit t of signs[n * K/32 + b] is set, -1.0 where it is clear (the same
- * weight arrays as q1s32_q8_gemm).  The page does not fix the order of the float operations; this
- * sums each 32-block in order, accumulates acc = fma(scale, block_sum, acc) per lane, then adds the
- * warp's lanes: the result is within a small multiple of 2^-24 * sum |terms| of the exact value.
- *   signs_device: N * K/32 u32; wscale_device: N * K/32 f32; x_device: M * K f32; y_device: M * N
- *   f32; all 4-byte aligned.  One launch on `stream`.
+ * weight arrays as q1s32_q8_gemm).  The page does not fix the order of the float operations, so
+ * neither path is defined bit for bit; each result lies within c * 2^-24 * sum_b |wscale| *
+ * sum_t |x| of the exact value, c = 32 + ceil(nb/8) for LUT4 at M <= 4 with K % 128 == 0,
+ * c = 12 + nb for the other LUT4 cases and c = 40 + ceil(nb/32) for FMA (nb = K/32).  Results are
+ * deterministic: the same inputs and path give the same bits on every call.
+ *   path GQ_PATH_FMA: the decode formulation -- signs expanded to +-1, each block summed in
+ *        order, acc = fma(scale, block_sum, acc), lanes added by a butterfly.
+ *   path GQ_PATH_LUT4: per token and 4 activations a table of the 16 signed sums, indexed by the
+ *        weight nibble; block sum = the 8 lookups in order; acc = fma(scale, block_sum, acc).
+ *   path GQ_PATH_AUTO: LUT4.
+ *   signs_device: N * K/32 u32; wscale_device: N * K/32 f32 (both 4-byte aligned; rows that
+ *   start on 16 bytes are read with 16-byte loads); x_device: M * K f32, 16-byte aligned;
+ *   y_device: M * N f32, 4-byte aligned.  One launch on `stream`; no workspace.
  * Errors: GQ_EINVAL_SHAPE unless N >= 1, 1 <= M <= 65535, 32 <= K <= 65536 and K % 32 == 0;
- *         GQ_EINVAL_PTR for a NULL or misaligned pointer; GQ_ECUDA. */
-int q1s32_f32_gemv(const uint32_t* signs_device, const float* wscale_device, const float* x_device,
-                   float* y_device, int N, int K, int M, gq_stream_t stream);
+ *         GQ_EUNSUPPORTED for another path; GQ_EINVAL_PTR for a NULL or misaligned pointer;
+ *         GQ_ECUDA. */
+int q1s32_f32_gemm(const uint32_t* signs_device, const float* wscale_device, const float* x_device,
+                   float* y_device, int M, int N, int K, int path, gq_stream_t stream);
 
 /* Prefill GEMM over `cols` Q8_0 activation vectors ([P1] Q1_MM_WGSL / Q1_MM4_WGSL): every
  * (row, column) is the GEMV chain above, stored at y[c * rows + r].

@@ -74,11 +74,14 @@ X = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
     (lambda L: L.q1s32_q8_gemm(X, X, X, X, N, X, 8, 8, 96, 2, N), 1),
     (lambda L: L.q1s32_q8_gemm(X, X, X, X, N, X, 8, 8, 128, 1, N), 3),
     (lambda L: L.q1s32_q8_gemm(X, X, X, X, N, X, 8, 8, 128, 3, N), 2),
-    (lambda L: L.q1s32_f32_gemv(X, X, X, X, 8, 48, 1, N), 1),
-    (lambda L: L.q1s32_f32_gemv(X, X, X, X, 8, 64, 0, N), 1),
-    (lambda L: L.q1s32_f32_gemv(X, X, X, X, 0, 64, 1, N), 1),
-    (lambda L: L.q1s32_f32_gemv(X, N, X, X, 8, 64, 1, N), 2),
-    (lambda L: L.q1s32_f32_gemv(X, X, ctypes.c_void_p(0x1002), X, 8, 64, 1, N), 2),
+    (lambda L: L.q1s32_f32_gemm(X, X, X, X, 1, 8, 48, 0, N), 1),
+    (lambda L: L.q1s32_f32_gemm(X, X, X, X, 0, 8, 64, 0, N), 1),
+    (lambda L: L.q1s32_f32_gemm(X, X, X, X, 1, 0, 64, 0, N), 1),
+    (lambda L: L.q1s32_f32_gemm(X, X, X, X, 1, 8, 64, 1, N), 3),
+    (lambda L: L.q1s32_f32_gemm(X, X, X, X, 1, 8, 64, 3, N), 3),
+    (lambda L: L.q1s32_f32_gemm(X, N, X, X, 1, 8, 64, 0, N), 2),
+    (lambda L: L.q1s32_f32_gemm(X, X, ctypes.c_void_p(0x1008), X, 1, 8, 64, 2, N), 2),
+    (lambda L: L.q1s32_f32_gemm(X, X, X, ctypes.c_void_p(0x1002), 1, 8, 64, 4, N), 2),
     (lambda L: L.gq_q1_0_pack(X, 8, 100, X, N), 1),
     (lambda L: L.gq_q1_0_pack(X, 8, 128, ctypes.c_void_p(0x1004), N), 2),
 ])

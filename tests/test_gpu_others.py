@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 import workloads as wl
+import gemm_q1_q8_gb300 as gqmod
 from tests.gpu_util import assert_same_bits, need_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -160,47 +161,95 @@ def test_prefill_mma_full_size_sampled(gq):
     assert gq.device_error() == 0
 
 
-# ----------------------------------------------------------------------------- Bonsai W1A32 decode
+# ----------------------------------------------------------------------------- Bonsai W1A32
 
-def _w1a32_bound(ws, x):
-    """The kernel's order (32-term block sums, fma per block, 5-level lane butterfly) has depth
-    < 64, so |got - exact| <= 64 * 2^-24 * sum |terms| (gamma_n bound); the f64 oracle is far tighter."""
+def _w1a32_terms(ws, x):
+    """sum_b |ws[n, b]| * sum_t |x[m, 32 b + t]| for every (m, n)."""
     M, K = x.shape
     N, nbk = ws.shape
     ax = np.abs(x.astype(np.float64)).reshape(M, nbk, 32).sum(axis=2)       # [M, nbk]
-    terms = ax @ np.abs(ws.astype(np.float64)).T                             # [M, N]
-    return 64 * 2.0 ** -24 * terms
+    return ax @ np.abs(ws.astype(np.float64)).T                              # [M, N]
 
 
-def test_w1a32_exact_special_case(gq):
+def _w1a32_depth(path, M, nbk):
+    """Roundings any one term passes through in the kernel's order (the gamma_n forward bound
+    |got - exact| <= c * 2^-24 * sum |terms| holds with this c, plus slack):
+    FMA: 31 adds of the block sum, one fma per block of the lane, a 5-level lane butterfly.
+    LUT4 decode (M <= 4, K % 128 == 0): two adds in a table entry, seven between the eight
+    lookups, one fma per block of the warp's share (16 per 32-block stage of its K slice, K cut in
+    up to eight slices), one add of the two halves, up to seven adds across the slices.
+    LUT4 otherwise: two adds in a table entry, seven between lookups, one fma per block."""
+    if path == gqmod.PATH_FMA:
+        return 40 + -(-nbk // 32)
+    if M <= 4 and nbk % 4 == 0:
+        return 32 + -(-nbk // 8)
+    return 12 + nbk
+
+
+def _w1a32_check(y, want, ws, x, path, M):
+    terms = _w1a32_terms(ws, x)
+    err = np.abs(y.astype(np.float64) - want)
+    bound = _w1a32_depth(path, M, ws.shape[1]) * 2.0 ** -24 * terms
+    assert np.all(err <= bound), f"max err/bound {np.max(err / bound)}"
+    # the pages' 1e-4 relative / 1e-6 absolute tolerance wherever the result is not a cancellation
+    big = np.abs(want) > 1e-2 * terms
+    assert np.all(err[big] <= 1e-4 * np.abs(want[big]) + 1e-6)
+
+
+W1A32_PATHS = [gqmod.PATH_LUT4, gqmod.PATH_FMA]
+
+
+@pytest.mark.parametrize("path", W1A32_PATHS)
+@pytest.mark.parametrize("M", [1, 2, 3, 7, 40])
+def test_w1a32_exact_special_case(gq, path, M):
     """Integer activations and power-of-two scales: every partial sum is exact in f32, so the GPU
     result equals the exact value bit for bit, whatever the order."""
-    M, N, K = 2, 77, 1024
-    rng = wl.Rng(33)
+    N, K = 77, 1024
+    rng = wl.Rng(33 + M)
     signs = rng.u32(N * K // 32).reshape(N, K // 32)
     ws = (2.0 ** -(2 + (rng.u32(N * K // 32) % 5).astype(np.int64))).astype(np.float32).reshape(N, K // 32)
     x = ((rng.u32(M * K) % 17).astype(np.int64) - 8).astype(np.float32).reshape(M, K)
-    y = gq.q1s32_f32_gemv(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x)).cpu().numpy()
+    y = gq.q1s32_f32_gemm(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x), path=path).cpu().numpy()
     want = oracle.q1s32_f32_gemv(signs, ws, x, M, N, K)
     assert np.array_equal(y.astype(np.float64), want)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1, 32), (1, 33, 96), (3, 130, 1024), (1, 300, 8224), (2, 64, 4096)])
-def test_w1a32_within_bound(gq, M, N, K):
+@pytest.mark.parametrize("path", W1A32_PATHS)
+@pytest.mark.parametrize("M,N,K", [(1, 1, 32), (1, 33, 96), (2, 130, 1024), (3, 300, 8224), (4, 64, 4096),
+                                   (1, 200, 16384), (3, 129, 2560), (1, 14336, 4096),
+                                   (5, 257, 160), (16, 513, 1056), (33, 300, 4128), (70, 1000, 512)])
+def test_w1a32_within_bound(gq, path, M, N, K):
     signs, ws, x = wl.prefill_inputs(wl.Rng(M + N + K), M, K, N)
-    y = gq.q1s32_f32_gemv(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x)).cpu().numpy()
-    want = oracle.q1s32_f32_gemv(signs, ws, x, M, N, K)
-    err = np.abs(y.astype(np.float64) - want)
-    assert np.all(err <= _w1a32_bound(ws, x)), f"max err {err.max()}"
-    # and the pages' tolerance where the result is not a cancellation
-    big = np.abs(want) > 1e-2 * _w1a32_bound(ws, x) / (64 * 2.0 ** -24)
-    assert np.all(err[big] <= 1e-4 * np.abs(want[big]) + 1e-6)
+    y = gq.q1s32_f32_gemm(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x), path=path).cpu().numpy()
+    _w1a32_check(y, oracle.q1s32_f32_gemv(signs, ws, x, M, N, K), ws, x, path, M)
 
 
-def test_w1a32_full_size(gq):
+@pytest.mark.parametrize("path", W1A32_PATHS)
+def test_w1a32_deterministic(gq, path):
+    M, N, K = 9, 700, 2048
+    signs, ws, x = wl.prefill_inputs(wl.Rng(77), M, K, N)
+    args = (to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x))
+    a = gq.q1s32_f32_gemm(*args, path=path).cpu().numpy()
+    b = gq.q1s32_f32_gemm(*args, path=path).cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("path", W1A32_PATHS)
+def test_w1a32_decode_full_size(gq, path):
     """The 14336 x 4096 Bonsai projection at one token, every row against the f64 oracle."""
     M, N, K = 1, 14336, 4096
     signs, ws, x = wl.prefill_inputs(wl.Rng(5), M, K, N)
-    y = gq.q1s32_f32_gemv(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x)).cpu().numpy()
-    want = oracle.q1s32_f32_gemv(signs, ws, x, M, N, K)
-    assert np.all(np.abs(y.astype(np.float64) - want) <= _w1a32_bound(ws, x))
+    y = gq.q1s32_f32_gemm(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x), path=path).cpu().numpy()
+    _w1a32_check(y, oracle.q1s32_f32_gemv(signs, ws, x, M, N, K), ws, x, path, M)
+
+
+def test_w1a32_prefill_full_size_sampled(gq):
+    """M = 512 tokens x 14336 rows x K = 4096 through the LUT4 prefill kernel, in the launch the
+    bench times; sampled rows and tokens (spanning every thread-block tile edge) against the oracle."""
+    M, N, K = 512, 14336, 4096
+    signs, ws, x = wl.prefill_inputs(wl.Rng(4), M, K, N)
+    y = gq.q1s32_f32_gemm(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x), path=gqmod.PATH_LUT4).cpu().numpy()
+    ns = np.unique(np.concatenate([np.arange(0, N, 997), [255, 256, N - 1]]))
+    ms = np.unique(np.concatenate([np.arange(0, M, 37), [31, 32, M - 1]]))
+    want = oracle.q1s32_f32_gemv(signs[ns], ws[ns], x[ms], ms.size, ns.size, K)
+    _w1a32_check(y[np.ix_(ms, ns)], want, ws[ns], x[ms], gqmod.PATH_LUT4, M)
