@@ -55,6 +55,8 @@ def lib():
                 ("gqo_quantize_q8_0", [P, I, I, P, P]),
                 ("gqo_prefill_q1s32", [P, P, P, P, P, I, I, I]),
                 ("gqo_q1s32_f32_gemv_f64", [P, P, P, P, I, I, I]),
+                ("gqo_w8a32_f64", [P, P, P, P, I, I, I]),
+                ("gqo_w4a32g128_f64", [P, P, P, P, I, I, I]),
                 ("gqo_f16_to_f32_array", [P, P, S]),
                 ("gqo_f32_to_f16_array", [P, P, S]),
                 ("gqo_fma_emulated_array", [P, P, P, P, S]),
@@ -185,3 +187,28 @@ def q1s32_f32_gemv(signs, ws, x, M: int, N: int, K: int) -> np.ndarray:
     y = np.empty(M * N, dtype=np.float64)
     lib().gqo_q1s32_f32_gemv_f64(_p(signs), _p(ws), _p(x), _p(y), M, N, K)
     return y.reshape(M, N)
+
+
+def w8a32(w, scale, x, T: int, N: int, K: int) -> np.ndarray:
+    """W8A32 matvec/matmul ([P4] matvecQ8 / matmulQ8): w [N, ceil(K/4)] u32 (int8 codes, LSB
+    first), scale [N] f32, x [T, K] f32 -> float64 [T, N]."""
+    w = np.ascontiguousarray(w, dtype=np.uint32)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert w.size == N * ((K + 3) // 4) and scale.size == N and x.size == T * K
+    y = np.empty((T, N), dtype=np.float64)
+    lib().gqo_w8a32_f64(_p(w), _p(scale), _p(x), _p(y), T, N, K)
+    return y
+
+
+def w4a32g128(w, scale, x, T: int, N: int, K: int) -> np.ndarray:
+    """W4A32 group-128 matvec/matmul ([P4] matvecQ4G128 / matmulQ4G128): w [N, ceil(K/8)] u32
+    (4-bit two's complement codes, LSB first), scale [N, ceil(K/128)] f32, x [T, K] f32 ->
+    float64 [T, N]."""
+    w = np.ascontiguousarray(w, dtype=np.uint32)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert w.size == N * ((K + 7) // 8) and scale.size == N * ((K + 127) // 128) and x.size == T * K
+    y = np.empty((T, N), dtype=np.float64)
+    lib().gqo_w4a32g128_f64(_p(w), _p(scale), _p(x), _p(y), T, N, K)
+    return y

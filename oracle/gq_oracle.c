@@ -17,6 +17,8 @@
  *       fn quant_at / fn main.
  *  [P3] "BonsaiのWebGPUカーネルを読み解く", the ternary P/N bitplane identity and the
  *       decode/prefill kernel figure (q1_bits, q1_scales).
+ *  [P4] web-xpu-ops README, the op table (matvecQ8, matvecQ4G128, matmulQ8, matmulQ4G128) and
+ *       "The q4 format (W4A32, group-128)".
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - Q8_0 activation quantizer (not on the pages): amax over 32, d = amax/127 (RN), stored as
@@ -28,6 +30,10 @@
  *  - block_q8_matmul_nt: products and sums are separate RN operations, as written in the WGSL.
  *  - Bonsai decode GEMV over f32 activations: the page leaves the float order open, so the
  *    oracle is the f64 definition and the GPU result is checked within a stated bound.
+ *  - W8A32 / W4A32 group-128 matvec and matmul: the page states the packing and where the scale
+ *    applies (per row after the dot product; per 128-column group) but no float order, so the
+ *    oracle is the f64 definition.  The matmul's weight is the right-hand operand with the
+ *    matvec's [rows, K] layout: out[t][n] = the matvec of weight row n with activation row t.
  *
  * Parity status: every function here is pinned by tests against closed forms, brute force or
  * library routines (see tests/test_oracle_*.py).  Bit-level agreement with bankML's own
@@ -332,6 +338,47 @@ void gqo_q1s32_f32_gemv_f64(const uint32_t* signs, const float* ws, const float*
                 acc += (double)ws[(size_t)n * nbk + b] * d;
             }
             y[(size_t)m * N + n] = acc;
+        }
+}
+
+/* W8A32 ([P4] matvecQ8 / matmulQ8): code k of weight row n is byte (k % 4) of word
+ * w[n * ceil(K/4) + k / 4], least-significant byte first, read as a signed (two's complement)
+ * byte; scale[n] multiplies the row's dot product once:
+ *   y[t * N + n] = scale[n] * sum_k q(n, k) * x[t * K + k]   (binary64, k ascending). */
+void gqo_w8a32_f64(const uint32_t* w, const float* scale, const float* x, double* y, int T, int N, int K) {
+    size_t wpr = ((size_t)K + 3) / 4;
+    for (int t = 0; t < T; t++)
+        for (int n = 0; n < N; n++) {
+            double dot = 0.0;
+            for (int k = 0; k < K; k++) {
+                uint32_t word = w[(size_t)n * wpr + (size_t)k / 4];
+                int8_t q = (int8_t)(uint8_t)(word >> (8 * (k % 4)));
+                dot += (double)q * (double)x[(size_t)t * K + k];
+            }
+            y[(size_t)t * N + n] = (double)scale[n] * dot;
+        }
+}
+
+/* W4A32 group-128 ([P4] matvecQ4G128 / matmulQ4G128, "The q4 format"): code k of weight row n
+ * is nibble (k % 8) of word w[n * ceil(K/8) + k / 8], least-significant nibble first, read as a
+ * 4-bit two's complement value (the quantizer emits [-7, 7]); scale[n * ceil(K/128) + g]
+ * multiplies the dot product of the row's columns 128 g .. 128 g + 127:
+ *   y[t * N + n] = sum_g scale[n, g] * sum_{k in g} q(n, k) * x[t * K + k]   (binary64). */
+void gqo_w4a32g128_f64(const uint32_t* w, const float* scale, const float* x, double* y, int T, int N, int K) {
+    size_t wpr = ((size_t)K + 7) / 8, gpr = ((size_t)K + 127) / 128;
+    for (int t = 0; t < T; t++)
+        for (int n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (size_t g = 0; g < gpr; g++) {
+                double dot = 0.0;
+                for (int k = (int)(128 * g); k < K && k < (int)(128 * g + 128); k++) {
+                    uint32_t nib = (w[(size_t)n * wpr + (size_t)k / 8] >> (4 * (k % 8))) & 0xFu;
+                    int q = (int)(nib ^ 8u) - 8;
+                    dot += (double)q * (double)x[(size_t)t * K + k];
+                }
+                acc += (double)scale[(size_t)n * gpr + g] * dot;
+            }
+            y[(size_t)t * N + n] = acc;
         }
 }
 

@@ -184,6 +184,36 @@ def prefill_inputs(rng: Rng, M: int, K: int, N: int, scale_lo=1e-3, scale_hi=5e-
     return signs, ws, x
 
 
+def wq_inputs(rng: Rng, T: int, K: int, N: int, bits: int, scale_lo=1e-3, scale_hi=2e-2, p_m8: float = 0.0):
+    """Block-quantized weights of the web-xpu-ops formats with f32 activations x [T, K] N(0,1).
+    bits = 8: codes uniform in [-127, 127], four per u32 least-significant byte first,
+      w [N, ceil(K/4)], one f32 scale per row [N].
+    bits = 4: codes uniform in [-7, 7] (with probability p_m8 the raw nibble 0x8 = -8, which the
+      quantizer never emits), eight per u32 least-significant nibble first, w [N, ceil(K/8)],
+      one f32 scale per 128 columns [N, ceil(K/128)].
+    Codes past K (the last word's padding) are zero."""
+    per = 32 // bits
+    words = (K + per - 1) // per
+    if bits == 8:
+        codes = (rng.u32(N * K) % 255).astype(np.int64) - 127
+    else:
+        codes = (rng.u32(N * K) % 15).astype(np.int64) - 7
+        if p_m8 > 0:
+            codes[rng.uniform(N * K) < p_m8] = -8
+    codes = codes.reshape(N, K)
+    padded = np.zeros((N, words * per), dtype=np.int64)
+    padded[:, :K] = codes
+    field = (padded & ((1 << bits) - 1)).astype(np.uint64).reshape(N, words, per)
+    shifts = (np.arange(per, dtype=np.uint64) * np.uint64(bits))
+    w = (field << shifts).sum(axis=2).astype(np.uint32)
+    groups = N if bits == 8 else N * ((K + 127) // 128)
+    scale = f32_uniform(rng, groups, scale_lo, scale_hi)
+    if bits == 4:
+        scale = scale.reshape(N, (K + 127) // 128)
+    x = f32_normal(rng, T * K).reshape(T, K)
+    return w, scale, x
+
+
 # ----------------------------------------------------------------------------- named workloads
 
 # BitNet-2B layer shapes for one decode token: four 2560x2560 attention projections, two
@@ -197,6 +227,7 @@ CONFIGS = {
     "block_q8_49152x960": dict(n=49152, k=960, ms=(1, 4, 16), seed=2),
     "ternary_14336x4096": dict(rows=14336, k=4096, batches=(1, 4, 16), seed=3),
     "prefill_512x4096x14336": dict(M=512, K=4096, N=14336, seed=4),
+    "wq_14336x4096": dict(N=14336, K=4096, tokens=(1, 512), seed=6),
 }
 
 
