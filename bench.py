@@ -259,6 +259,42 @@ def bench_w1a32(gq, torch, dev, hbm_peak, steps=40, warmup=5):
     return {"w1a32_decode_14336x4096": dec, "w1a32_prefill_512x4096x14336": pre}
 
 
+def bench_wq(gq, torch, dev, hbm_peak, steps=40, warmup=5):
+    """W8A32 (per-row scale) and W4A32 group-128 at 14336 x 4096: the matvec with rotating weight
+    copies (more bytes than L2), device time from CUDA-graph replay; the matmul at 512 tokens."""
+    N, K = 14336, 4096
+    out = {}
+    stream = torch.cuda.current_stream()
+    for bits, mv, mm in ((8, gq.matvec_q8, gq.matmul_q8), (4, gq.matvec_q4g128, gq.matmul_q4g128)):
+        wbytes = N * K * bits // 8 + (N * 4 if bits == 8 else N * (K // 128) * 4)
+        ncopies = max(2, -(-300_000_000 // wbytes))
+        copies = []
+        for c in range(ncopies):
+            w, sc, _ = wl.wq_inputs(wl.Rng(90 + c), 1, K, N, bits)
+            copies.append((torch.from_numpy(w.view(np.int32)).to(dev), torch.from_numpy(sc).to(dev)))
+        x = torch.from_numpy(wl.f32_normal(wl.Rng(91), K).reshape(1, K)).to(dev)
+        y = torch.empty((1, N), dtype=torch.float32, device=dev)
+        it = [0]
+
+        def f():
+            i = it[0] % len(copies)
+            it[0] += 1
+            mv(copies[i][0], copies[i][1], x, out=y)
+        t = time_graph(f, steps, warmup)
+        name = "q8" if bits == 8 else "q4g128"
+        res = {"matvec_us": round(t * 1e6, 2), "matvec_weight_GBps": round(wbytes / t / 1e9, 1),
+               "matvec_hbm_frac": round(wbytes / t / 1e9 / hbm_peak, 4)}
+        T = 512
+        xp = torch.from_numpy(wl.f32_normal(wl.Rng(92), T * K).reshape(T, K)).to(dev)
+        yp = torch.empty((T, N), dtype=torch.float32, device=dev)
+        tm = time_steps(lambda: mm(copies[0][0], copies[0][1], xp, out=yp), 5, 2, stream) / 5
+        res["matmul512_us"] = round(tm * 1e6, 1)
+        res["matmul512_TFLOPs"] = round(2.0 * T * N * K / tm / 1e12, 2)
+        out[f"w{bits}a32_{name}_14336x4096"] = res
+        del copies
+    return out
+
+
 def bench_prefill(gq, torch, dev, bf16_peak, steps=5, warmup=2, paths=("lut4", "mma")):
     """Prefill M=512, K=4096, N=14336: quantize, then the GEMM on each path."""
     stream = torch.cuda.current_stream()
@@ -312,10 +348,12 @@ def bench_gemv_shapes(gq, torch, dev, hbm_peak, items, wbytes):
 def extras(gq, torch, dev, hbm_peak, bf16_peak):
     """Secondary kernels, each timed alone (not part of the headline step): block_q8 and ternary
     by CUDA-graph replay of rotating calls (device time), prefill by CUDA events around calls."""
-    out = {"timing": "block_q8, ternary, w1a32: CUDA-graph replay (device time per call); prefill: CUDA events per call"}
+    out = {"timing": "block_q8, ternary, w1a32 decode, wq matvec: CUDA-graph replay (device time per call); "
+                     "prefill and matmuls: CUDA events per call"}
     out.update(bench_block_q8(gq, torch, dev, hbm_peak))
     out.update(bench_ternary(gq, torch, dev, hbm_peak))
     out.update(bench_w1a32(gq, torch, dev, hbm_peak))
+    out.update(bench_wq(gq, torch, dev, hbm_peak))
     out.update(bench_prefill(gq, torch, dev, bf16_peak))
     return out
 
@@ -332,6 +370,8 @@ def run_only(args):
         res = bench_ternary(gq, torch, dev, hbm_peak, steps=args.steps, warmup=args.warmup)
     elif args.only == "w1a32":
         res = bench_w1a32(gq, torch, dev, hbm_peak, steps=args.steps, warmup=args.warmup)
+    elif args.only == "wq":
+        res = bench_wq(gq, torch, dev, hbm_peak, steps=args.steps, warmup=args.warmup)
     elif args.only == "prefill_mma":
         res = bench_prefill(gq, torch, dev, bf16_peak, steps=args.steps, warmup=args.warmup, paths=("mma",))
     else:
@@ -486,7 +526,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
-    ap.add_argument("--only", choices=["block_q8", "ternary", "w1a32", "prefill_lut4", "prefill_mma"], default=None,
+    ap.add_argument("--only", choices=["block_q8", "ternary", "w1a32", "wq", "prefill_lut4", "prefill_mma"], default=None,
                     help="time one secondary kernel on its workload and print only that")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

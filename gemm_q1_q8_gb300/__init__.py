@@ -17,7 +17,8 @@ from . import build as _build
 __all__ = [
     "lib", "GQError", "PATH_AUTO", "PATH_DP4A", "PATH_LUT4", "PATH_MMA", "PATH_FMA",
     "q1_0_packed_bytes", "q1_0_pack", "q1_q8_gemv", "q1_q8_gemv_noalloc", "GroupedGemv", "q1_q8_gemm",
-    "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm",
+    "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm", "q1s32_f32_gemm",
+    "matvec_q8", "matmul_q8", "matvec_q4g128", "matmul_q4g128",
     "device_error", "version",
 ]
 
@@ -56,6 +57,10 @@ def lib():
             "q1_q8_gemv_noalloc": (I, [P, P, P, I, I, P]),
             "gq_gemv_group_plan": (I, [P, I, P]),
             "q1s32_f32_gemm": (I, [P, P, P, P, I, I, I, I, P]),
+            "matvec_q8": (I, [P, P, P, P, I, I, P]),
+            "matmul_q8": (I, [P, P, P, P, I, I, I, P]),
+            "matvec_q4g128": (I, [P, P, P, P, I, I, P]),
+            "matmul_q4g128": (I, [P, P, P, P, I, I, I, P]),
             "q1_q8_gemv_grouped": (I, [P, I, I, P, P]),
             "q1_q8_gemm": (I, [P, P, P, I, I, I, I, P]),
             "block_q8_matmul_nt": (I, [P, P, P, P, I, I, I, P]),
@@ -203,6 +208,45 @@ def q1s32_f32_gemm(signs: torch.Tensor, wscale: torch.Tensor, x: torch.Tensor, p
     _check(lib().q1s32_f32_gemm(_ptr(signs), _ptr(wscale), _ptr(x), _ptr(y), M, N, K, path, _stream()),
            "q1s32_f32_gemm")
     return y
+
+
+def _wq(bits: int, w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out, name: str):
+    N = w.shape[0]
+    T, K = x.shape
+    _need(w, torch.int32, N * K * bits // 32, "w")
+    _need(scale, torch.float32, N if bits == 8 else N * ((K + 127) // 128), "scale")
+    _need(x, torch.float32, T * K, "x")
+    y = torch.empty((T, N), dtype=torch.float32, device=x.device) if out is None else out
+    _need(y, torch.float32, T * N, "out")
+    fn = getattr(lib(), name)
+    if name.startswith("matvec"):
+        if T != 1:
+            raise GQError(f"{name}: x must hold one token")
+        _check(fn(_ptr(w), _ptr(scale), _ptr(x), _ptr(y), N, K, _stream()), name)
+    else:
+        _check(fn(_ptr(w), _ptr(scale), _ptr(x), _ptr(y), T, N, K, _stream()), name)
+    return y
+
+
+def matvec_q8(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None):
+    """W8A32 GEMV: w [N, K/4] int32 (int8 codes, LSB first), scale [N] f32, x [1, K] f32 -> y [1, N]."""
+    return _wq(8, w, scale, x, out, "matvec_q8")
+
+
+def matmul_q8(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None):
+    """W8A32 GEMM: w [N, K/4] int32, scale [N] f32, x [T, K] f32 -> y [T, N] f32."""
+    return _wq(8, w, scale, x, out, "matmul_q8")
+
+
+def matvec_q4g128(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None):
+    """W4A32 group-128 GEMV: w [N, K/8] int32 (4-bit codes, LSB first), scale [N, ceil(K/128)] f32,
+    x [1, K] f32 -> y [1, N]."""
+    return _wq(4, w, scale, x, out, "matvec_q4g128")
+
+
+def matmul_q4g128(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None):
+    """W4A32 group-128 GEMM: w [N, K/8] int32, scale [N, ceil(K/128)] f32, x [T, K] f32 -> y [T, N]."""
+    return _wq(4, w, scale, x, out, "matmul_q4g128")
 
 
 def q1_q8_gemm(packed: torch.Tensor, act: torch.Tensor, rows: int, n: int, cols: int, path: int = PATH_AUTO,

@@ -140,6 +140,29 @@ int q1s32_f32_gemm(const uint32_t* signs, const float* wscale, const float* x, f
         gq::launch_q1s32_f32(signs, wscale, x, y, M, N, K, path, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static int wq_call(int bits, const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+                   gq_stream_t stream) {
+    if (N < 1 || T < 1 || T > 65535 * 128 || K < 32 || K % 32 != 0 || K > kMaxK) return GQ_EINVAL_SHAPE;
+    if (!w || !scale || !x || !y) return GQ_EINVAL_PTR;
+    if (!aligned(w, 16) || !aligned(scale, 4) || !aligned(x, 16) || !aligned(y, 4)) return GQ_EINVAL_PTR;
+    return cuda_status(gq::launch_wq(bits, w, scale, x, y, T, N, K, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int matvec_q8(const uint32_t* w, const float* scale, const float* x, float* y, int N, int K, gq_stream_t stream) {
+    return wq_call(8, w, scale, x, y, 1, N, K, stream);
+}
+int matmul_q8(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+              gq_stream_t stream) {
+    return wq_call(8, w, scale, x, y, T, N, K, stream);
+}
+int matvec_q4g128(const uint32_t* w, const float* scale, const float* x, float* y, int N, int K, gq_stream_t stream) {
+    return wq_call(4, w, scale, x, y, 1, N, K, stream);
+}
+int matmul_q4g128(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+                  gq_stream_t stream) {
+    return wq_call(4, w, scale, x, y, T, N, K, stream);
+}
+
 int ternary_bitplane_gemv(const uint32_t* P, const uint32_t* N, const uint32_t* X, int32_t* y, int rows, int k,
                           int batch, gq_stream_t stream) {
     if (rows < 1 || k < 1024 || batch < 1 || k % 1024 != 0 || k > kMaxK || batch > 64) return GQ_EINVAL_SHAPE;

@@ -169,6 +169,8 @@ cudaError_t launch_quantize(const float* x, int m, int k, uint16_t* d, int8_t* q
                             cudaStream_t s);
 cudaError_t launch_prefill_lut4(const uint32_t* signs, const float* ws, const uint16_t* xd,
                                 const int8_t* xq, float* y, int M, int N, int K, cudaStream_t s);
+cudaError_t launch_wq(int bits, const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+                      cudaStream_t s);   // bits 8: per-row scale; bits 4: per-128-column-group scale
 cudaError_t launch_prefill_mma(const uint32_t* signs, const float* ws, const uint16_t* xd,
                                const uint16_t* xq_op, float* y, int M, int N, int K, cudaStream_t s);
 

@@ -1,0 +1,280 @@
+// Block-quantized weights times f32 activations on sm_103a (web-xpu-ops README: the op table rows
+// matvecQ8 / matmulQ8 and matvecQ4G128 / matmulQ4G128, and "The q4 format").
+//   8 bits: code k of row n is byte k % 4 of word n * K/4 + k/4 (least-significant first, signed);
+//           y[t, n] = scale[n] * sum_k q(n, k) * x[t, k] -- the row scale applied once at the end.
+//   4 bits: code k of row n is nibble k % 8 of word n * K/8 + k/8 (least-significant first, 4-bit
+//           two's complement); y[t, n] = sum_g scale[n, g] * sum_{k in g} q(n, k) * x[t, k] over
+//           groups of 128 columns.
+// The page fixes no float order, so results are checked against the exact value within an error
+// bound of each kernel's own order.
+//
+// Codes become floats exactly: a biased code (byte ^ 0x80, or nibble ^ 8) is placed in the low bits
+// of 2^23's bit pattern by a byte permute, and one subtraction removes 2^23 plus the bias.
+//
+// GEMV (T <= 4 tokens): a thread block covers 32/T rows; its eight warps take the 512-column chunks
+// of K in turn (chunk c to warp c % 8), each lane 16 consecutive columns of a chunk, so a warp's
+// load of one row is 512 (8-bit) or 256 (4-bit) contiguous bytes.  The lane keeps one partial sum
+// per (row, token) -- 32 in all -- and a butterfly over the lanes leaves lane l with the total of
+// value l; the eight warps' totals are then added in a fixed tree.
+//
+// GEMM (T > 4): a thread block computes 128 rows x 128 tokens, K staged 32 columns at a time.  The
+// codes are turned into floats (times the group scale for 4 bits) into shared memory once per
+// stage, and each thread accumulates an 8 x 8 block of outputs from outer products.
+#include "gq_internal.cuh"
+
+namespace gq {
+namespace {
+
+// Exact float of a signed byte / 4-bit code, from the biased field in the low byte.
+__device__ __forceinline__ float biased_byte_to_f32(uint32_t biased_word, int j) {
+    return __fsub_rn(__uint_as_float(__byte_perm(biased_word, 0x4B000000u, 0x7440 + j)), 8388736.0f);   // 2^23 + 128
+}
+__device__ __forceinline__ float biased_nibble_to_f32(uint32_t biased_bytes, int j) {
+    return __fsub_rn(__uint_as_float(__byte_perm(biased_bytes, 0x4B000000u, 0x7440 + j)), 8388616.0f);   // 2^23 + 8
+}
+
+// The 16 codes of one lane's slice, in column order.
+template <int BITS>
+__device__ __forceinline__ void decode16(const uint32_t (&wd)[BITS == 8 ? 4 : 2], float (&cf)[16]) {
+    if constexpr (BITS == 8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t b = wd[i] ^ 0x80808080u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cf[4 * i + j] = biased_byte_to_f32(b, j);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t ev = (wd[i] & 0x0F0F0F0Fu) ^ 0x08080808u;          // nibbles 0, 2, 4, 6
+            const uint32_t od = ((wd[i] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;   // nibbles 1, 3, 5, 7
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                cf[8 * i + 2 * j] = biased_nibble_to_f32(ev, j);
+                cf[8 * i + 2 * j + 1] = biased_nibble_to_f32(od, j);
+            }
+        }
+    }
+}
+
+constexpr int kGvWarps = 8;
+constexpr int kChunk = 512;                       // columns per warp step (16 per lane)
+
+template <int BITS, int T>
+__global__ void __launch_bounds__(kGvWarps * 32, 2)
+wq_gemv_kernel(const uint32_t* __restrict__ w, const float* __restrict__ scale, const float* __restrict__ x,
+               float* __restrict__ y, int N, int K, int Tn) {
+    constexpr int R = 32 / T;                     // rows per thread block
+    constexpr int WPL = BITS == 8 ? 4 : 2;        // words per lane per chunk
+    __shared__ float part[kGvWarps][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * R;
+    const size_t wpr = static_cast<size_t>(K) * BITS / 32;   // words per row
+    const int G = (K + 127) / 128;
+    const int nchunks = (K + kChunk - 1) / kChunk;
+    float acc[R][T];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int u = 0; u < T; ++u) acc[r][u] = 0.0f;
+
+    for (int c = warp; c < nchunks; c += kGvWarps) {
+        const int k0 = c * kChunk + 16 * lane;
+        if (k0 < K) {                             // K % 32 == 0: a live lane has all 16 columns
+            float xv[T][16];
+#pragma unroll
+            for (int u = 0; u < T; ++u) {
+                // tokens past Tn (a 3-token call through the 4-token kernel) repeat the last one
+                const float4* xp = reinterpret_cast<const float4*>(x + static_cast<size_t>(min(u, Tn - 1)) * K + k0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 a = __ldg(xp + q);
+                    xv[u][4 * q] = a.x; xv[u][4 * q + 1] = a.y; xv[u][4 * q + 2] = a.z; xv[u][4 * q + 3] = a.w;
+                }
+            }
+#pragma unroll
+            for (int rb = 0; rb < R; rb += 8) {
+                uint32_t wd[8][WPL];
+                float sc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int n = min(n0 + rb + i, N - 1);        // past-the-end rows: computed, not stored
+                    if constexpr (BITS == 4) sc[i] = __ldg(scale + static_cast<size_t>(n) * G + k0 / 128);
+                    const uint32_t* p = w + static_cast<size_t>(n) * wpr + static_cast<size_t>(k0) * BITS / 32;
+                    if constexpr (BITS == 8) {
+                        const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+                        wd[i][0] = a.x; wd[i][1] = a.y; wd[i][2] = a.z; wd[i][3] = a.w;
+                    } else {
+                        const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
+                        wd[i][0] = a.x; wd[i][1] = a.y;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float cf[16];
+                    decode16<BITS>(wd[i], cf);
+                    if constexpr (BITS == 8) {
+#pragma unroll
+                        for (int u = 0; u < T; ++u)
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[rb + i][u] = __fmaf_rn(cf[j], xv[u][j], acc[rb + i][u]);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < T; ++u) {
+                            float p = __fmul_rn(cf[0], xv[u][0]);
+#pragma unroll
+                            for (int j = 1; j < 16; ++j) p = __fmaf_rn(cf[j], xv[u][j], p);
+                            acc[rb + i][u] = __fmaf_rn(sc[i], p, acc[rb + i][u]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    // lanes -> lane l holds the warp's total of value l = (row l / T, token l % T)
+    float v[32];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int u = 0; u < T; ++u) v[r * T + u] = acc[r][u];
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool hi = (lane & s) != 0;
+#pragma unroll
+        for (int j = 0; j < s; ++j) {
+            const float send = hi ? v[j] : v[j + s];
+            const float keep = hi ? v[j + s] : v[j];
+            v[j] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, s));
+        }
+    }
+    part[warp][lane] = v[0];
+    __syncthreads();
+    if (warp == 0) {
+        const float tot = __fadd_rn(__fadd_rn(__fadd_rn(part[0][lane], part[1][lane]), __fadd_rn(part[2][lane], part[3][lane])),
+                                    __fadd_rn(__fadd_rn(part[4][lane], part[5][lane]), __fadd_rn(part[6][lane], part[7][lane])));
+        const int n = n0 + lane / T, u = lane % T;
+        if (n < N && u < Tn) {
+            const float out = (BITS == 8) ? __fmul_rn(__ldg(scale + n), tot) : tot;
+            y[static_cast<size_t>(u) * N + n] = out;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------- GEMM
+
+constexpr int kGmN = 128, kGmT = 128, kGmK = 32;  // tile: rows x tokens x columns per stage
+constexpr int kGmPad = 4;                         // row padding of the [k][n] / [k][t] stage arrays
+
+template <int BITS>
+__global__ void __launch_bounds__(256)
+wq_gemm_kernel(const uint32_t* __restrict__ w, const float* __restrict__ scale, const float* __restrict__ x,
+               float* __restrict__ y, int T, int N, int K) {
+    __shared__ __align__(16) float Ws[kGmK][kGmN + kGmPad];
+    __shared__ __align__(16) float Xs[kGmK][kGmT + kGmPad];
+    const int tid = threadIdx.x;
+    // 16 x 16 threads; thread (tx, ty) owns rows 4tx..4tx+3 and 64+4tx..+3, tokens 4ty.. and 64+4ty..
+    // (a quarter-warp's 16-byte reads then cover 128 contiguous bytes)
+    const int tx = tid & 15, ty = tid >> 4;
+    const int n0 = blockIdx.x * kGmN, t0 = blockIdx.y * kGmT;
+    const size_t wpr = static_cast<size_t>(K) * BITS / 32;
+    const int G = (K + 127) / 128;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+    for (int k0 = 0; k0 < K; k0 += kGmK) {
+        __syncthreads();                          // the previous stage is consumed
+        // weights: 128 rows x 32 codes; 8 bits: thread -> (row tid/2, 16 codes); 4 bits: (row tid/2, 16 codes)
+        {
+            const int r = tid >> 1, half = tid & 1;
+            const int n = min(n0 + r, N - 1);
+            const uint32_t* p = w + static_cast<size_t>(n) * wpr + static_cast<size_t>(k0 + 16 * half) * BITS / 32;
+            uint32_t wd[BITS == 8 ? 4 : 2];
+            if constexpr (BITS == 8) {
+                const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+                wd[0] = a.x; wd[1] = a.y; wd[2] = a.z; wd[3] = a.w;
+            } else {
+                const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
+                wd[0] = a.x; wd[1] = a.y;
+            }
+            float cf[16];
+            decode16<BITS>(wd, cf);
+            if constexpr (BITS == 4) {
+                const float sc = __ldg(scale + static_cast<size_t>(n) * G + k0 / 128);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) cf[j] = __fmul_rn(cf[j], sc);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) Ws[16 * half + j][r] = cf[j];
+        }
+        // activations: 128 tokens x 32 columns; thread -> (token tid/2, 16 columns)
+        {
+            const int tt = tid >> 1, half = tid & 1;
+            const int t = min(t0 + tt, T - 1);
+            const float4* xp = reinterpret_cast<const float4*>(x + static_cast<size_t>(t) * K + k0 + 16 * half);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 a = __ldg(xp + q);
+                Xs[16 * half + 4 * q][tt] = a.x;
+                Xs[16 * half + 4 * q + 1][tt] = a.y;
+                Xs[16 * half + 4 * q + 2][tt] = a.z;
+                Xs[16 * half + 4 * q + 3][tt] = a.w;
+            }
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int kk = 0; kk < kGmK; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&Ws[kk][4 * tx]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&Ws[kk][64 + 4 * tx]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Xs[kk][4 * ty]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Xs[kk][64 + 4 * ty]);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int n = n0 + (i < 4 ? 4 * tx + i : 64 + 4 * tx + i - 4);
+        if (n >= N) continue;
+        const float sc = (BITS == 8) ? __ldg(scale + n) : 1.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int t = t0 + (j < 4 ? 4 * ty + j : 64 + 4 * ty + j - 4);
+            if (t < T) y[static_cast<size_t>(t) * N + n] = (BITS == 8) ? __fmul_rn(sc, acc[i][j]) : acc[i][j];
+        }
+    }
+}
+
+template <int BITS, int T>
+cudaError_t launch_gemv(const uint32_t* w, const float* scale, const float* x, float* y, int N, int K, int Tn,
+                        cudaStream_t s) {
+    constexpr int R = 32 / T;
+    wq_gemv_kernel<BITS, T><<<(N + R - 1) / R, kGvWarps * 32, 0, s>>>(w, scale, x, y, N, K, Tn);
+    return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t launch_bits(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+                        cudaStream_t s) {
+    if (T == 1) return launch_gemv<BITS, 1>(w, scale, x, y, N, K, T, s);
+    if (T == 2) return launch_gemv<BITS, 2>(w, scale, x, y, N, K, T, s);
+    if (T <= 4) return launch_gemv<BITS, 4>(w, scale, x, y, N, K, T, s);
+    const dim3 grid((N + kGmN - 1) / kGmN, (T + kGmT - 1) / kGmT);
+    wq_gemm_kernel<BITS><<<grid, 256, 0, s>>>(w, scale, x, y, T, N, K);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_wq(int bits, const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+                      cudaStream_t s) {
+    return bits == 8 ? launch_bits<8>(w, scale, x, y, T, N, K, s) : launch_bits<4>(w, scale, x, y, T, N, K, s);
+}
+
+}  // namespace gq

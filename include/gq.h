@@ -189,6 +189,33 @@ int q1_q8_gemv_grouped(const gq_gemv_desc* descs_device, int count, int total_ti
 int q1s32_f32_gemm(const uint32_t* signs_device, const float* wscale_device, const float* x_device,
                    float* y_device, int M, int N, int K, int path, gq_stream_t stream);
 
+/* Block-quantized weights times f32 activations (web-xpu-ops README: the op table rows
+ * matvecQ8 / matmulQ8 and matvecQ4G128 / matmulQ4G128, and "The q4 format"):
+ *   matvec_q8 / matmul_q8 (W8A32, per-row scale):
+ *     code k of row n = byte (k % 4) of w[n * K/4 + k/4], least-significant byte first, signed;
+ *     y[t * N + n] = scale[n] * sum_k code(n, k) * x[t * K + k].
+ *   matvec_q4g128 / matmul_q4g128 (W4A32, one scale per 128 columns):
+ *     code k of row n = nibble (k % 8) of w[n * K/8 + k/8], least-significant nibble first,
+ *     4-bit two's complement (the page's quantizer emits [-7, 7]; a raw 0x8 reads as -8);
+ *     y[t * N + n] = sum_g scale[n * ceil(K/128) + g] * sum_{k in g} code(n, k) * x[t * K + k].
+ * The matvec is the matmul with T = 1.  The page fixes no float order, so the results are not
+ * defined bit for bit; each lies within c * 2^-24 * sum |scale * code * x| of the exact value
+ * (T <= 4: c = 16 * ceil(K/4096) + 10 for 8 bits, c = 28 + ceil(K/512) for 4 bits; T > 4:
+ * c = K + 2), and the same inputs give the same bits on every call.
+ *   w_device: N * K/4 (8 bits) or N * K/8 (4 bits) u32, 16-byte aligned; scale_device: N (8 bits)
+ *   or N * ceil(K/128) (4 bits) f32; x_device: T * K f32, 16-byte aligned; y_device: T * N f32.
+ *   One launch on `stream`; no workspace.
+ * Errors: GQ_EINVAL_SHAPE unless N >= 1, 1 <= T <= 65535 * 128, 32 <= K <= 65536 and
+ *         K % 32 == 0; GQ_EINVAL_PTR for a NULL or misaligned pointer; GQ_ECUDA. */
+int matvec_q8(const uint32_t* w_device, const float* scale_device, const float* x_device, float* y_device,
+              int N, int K, gq_stream_t stream);
+int matmul_q8(const uint32_t* w_device, const float* scale_device, const float* x_device, float* y_device,
+              int T, int N, int K, gq_stream_t stream);
+int matvec_q4g128(const uint32_t* w_device, const float* scale_device, const float* x_device, float* y_device,
+                  int N, int K, gq_stream_t stream);
+int matmul_q4g128(const uint32_t* w_device, const float* scale_device, const float* x_device, float* y_device,
+                  int T, int N, int K, gq_stream_t stream);
+
 /* Prefill GEMM over `cols` Q8_0 activation vectors ([P1] Q1_MM_WGSL / Q1_MM4_WGSL): every
  * (row, column) is the GEMV chain above, stored at y[c * rows + r].
  *   act_device: cols * (n/32) Q8_0 blocks, column after column (2-byte aligned).

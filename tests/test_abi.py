@@ -74,6 +74,13 @@ X = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
     (lambda L: L.q1s32_q8_gemm(X, X, X, X, N, X, 8, 8, 96, 2, N), 1),
     (lambda L: L.q1s32_q8_gemm(X, X, X, X, N, X, 8, 8, 128, 1, N), 3),
     (lambda L: L.q1s32_q8_gemm(X, X, X, X, N, X, 8, 8, 128, 3, N), 2),
+    (lambda L: L.matvec_q8(X, X, X, X, 8, 48, N), 1),
+    (lambda L: L.matmul_q8(X, X, X, X, 0, 8, 64, N), 1),
+    (lambda L: L.matvec_q4g128(X, X, X, X, 0, 64, N), 1),
+    (lambda L: L.matmul_q4g128(X, X, X, X, 2, 8, 65568, N), 1),
+    (lambda L: L.matvec_q8(ctypes.c_void_p(0x1008), X, X, X, 8, 64, N), 2),
+    (lambda L: L.matmul_q4g128(X, X, ctypes.c_void_p(0x1004), X, 3, 8, 64, N), 2),
+    (lambda L: L.matvec_q4g128(X, N, X, X, 8, 64, N), 2),
     (lambda L: L.q1s32_f32_gemm(X, X, X, X, 1, 8, 48, 0, N), 1),
     (lambda L: L.q1s32_f32_gemm(X, X, X, X, 0, 8, 64, 0, N), 1),
     (lambda L: L.q1s32_f32_gemm(X, X, X, X, 1, 0, 64, 0, N), 1),

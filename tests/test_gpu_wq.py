@@ -1,0 +1,116 @@
+"""GPU parity for the W8A32 (per-row scale) and W4A32 group-128 matvec/matmul (web-xpu-ops README:
+matvecQ8 / matmulQ8 / matvecQ4G128 / matmulQ4G128) against the f64 oracle.  The page fixes no
+float order, so each result must lie within the forward error bound of the kernel's own order,
+and within 1e-4 relative / 1e-6 absolute wherever it is not a cancellation."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from tests.gpu_util import need_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gq():
+    need_gpu()
+    import gemm_q1_q8_gb300 as m
+    return m
+
+
+def _terms(bits, w, scale, x, N, K):
+    """sum_k |scale| * |code| * |x| per (t, n), from an unpack written here with numpy."""
+    if bits == 8:
+        codes = w.view("<u4").view(np.int8).reshape(N, -1)[:, :K].astype(np.float64)
+        return (np.abs(x.astype(np.float64)) @ np.abs(codes).T) * np.abs(scale.astype(np.float64))[None, :]
+    nib = ((w[:, :, None] >> (4 * np.arange(8, dtype=np.uint32))[None, None, :]) & 0xF).reshape(N, -1)[:, :K]
+    codes = nib.astype(np.float64) - 16.0 * (nib >= 8)
+    sc = np.repeat(np.abs(scale.astype(np.float64)), 128, axis=1)[:, :K]
+    return np.abs(x.astype(np.float64)) @ (np.abs(codes) * sc).T
+
+
+def _depth(bits, T, K):
+    """Roundings a term passes through in the kernel's order.
+    T <= 4 (GEMV): 8 bits -- an fma chain over the lane's 16 columns of each of its warp's 512-column
+    chunks, a 5-level lane butterfly, a 3-level warp tree, the row-scale multiply; 4 bits -- a
+    16-term chain per chunk, one fma with the group scale per chunk, the butterfly and tree.
+    T > 4 (GEMM): one fma per column, plus the scale multiply (8 bits) or the dequantizing product
+    code * scale (4 bits)."""
+    if T <= 4:
+        return 16 * -(-K // 4096) + 10 if bits == 8 else 28 + -(-K // 512)
+    return K + 2
+
+
+def _check(bits, y, want, w, scale, x, T, N, K):
+    terms = _terms(bits, w, scale, x, N, K)
+    err = np.abs(y.astype(np.float64) - want)
+    bound = _depth(bits, T, K) * 2.0 ** -24 * terms
+    assert np.all(err <= bound), f"max err/bound {np.max(err / np.maximum(bound, 1e-300))}"
+    big = np.abs(want) > 1e-2 * terms
+    assert np.all(err[big] <= 1e-4 * np.abs(want[big]) + 1e-6)
+
+
+def _run(gq, bits, w, scale, x):
+    T = x.shape[0]
+    args = (to_dev(w.view(np.int32)), to_dev(scale), to_dev(x))
+    if bits == 8:
+        y = gq.matvec_q8(*args) if T == 1 else gq.matmul_q8(*args)
+    else:
+        y = gq.matvec_q4g128(*args) if T == 1 else gq.matmul_q4g128(*args)
+    return y.cpu().numpy()
+
+
+def _oracle(bits, w, scale, x, T, N, K):
+    return oracle.w8a32(w, scale, x, T, N, K) if bits == 8 else oracle.w4a32g128(w, scale, x, T, N, K)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("T,N,K", [(1, 1, 32), (1, 77, 96), (1, 1000, 544), (2, 129, 4128), (3, 40, 1024),
+                                   (4, 300, 2560), (5, 257, 160), (33, 130, 1056), (130, 300, 512),
+                                   (1, 3000, 16384)])
+def test_within_bound(gq, bits, T, N, K):
+    w, scale, x = wl.wq_inputs(wl.Rng(1000 * bits + T + N + K), T, K, N, bits, p_m8=0.02)
+    _check(bits, _run(gq, bits, w, scale, x), _oracle(bits, w, scale, x, T, N, K), w, scale, x, T, N, K)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("T", [1, 3, 9])
+def test_exact_special_case(gq, bits, T):
+    """Integer x in [-8, 8] and power-of-two scales: every partial sum is exact in f32 at this size,
+    so the GPU equals the oracle bit for bit, whatever the order."""
+    N, K = 200, 1024
+    rng = wl.Rng(60 + bits + T)
+    w, scale, _ = wl.wq_inputs(rng, T, K, N, bits, p_m8=0.05)
+    scale = (2.0 ** -(1 + (rng.u32(scale.size) % 6).astype(np.int64))).astype(np.float32).reshape(scale.shape)
+    x = ((rng.u32(T * K) % 17).astype(np.int64) - 8).astype(np.float32).reshape(T, K)
+    assert np.array_equal(_run(gq, bits, w, scale, x).astype(np.float64), _oracle(bits, w, scale, x, T, N, K))
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("T", [1, 2, 64])
+def test_deterministic(gq, bits, T):
+    N, K = 700, 2048
+    w, scale, x = wl.wq_inputs(wl.Rng(5 + T), T, K, N, bits)
+    a, b = _run(gq, bits, w, scale, x), _run(gq, bits, w, scale, x)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_matvec_full_size(gq, bits):
+    """14336 x 4096 at one token, every row against the oracle."""
+    T, N, K = 1, 14336, 4096
+    w, scale, x = wl.wq_inputs(wl.Rng(6), T, K, N, bits)
+    _check(bits, _run(gq, bits, w, scale, x), _oracle(bits, w, scale, x, T, N, K), w, scale, x, T, N, K)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_matmul_full_size_sampled(gq, bits):
+    """512 tokens x 14336 rows x 4096: sampled rows and tokens (across tile edges) against the oracle."""
+    T, N, K = 512, 14336, 4096
+    w, scale, x = wl.wq_inputs(wl.Rng(6), T, K, N, bits)
+    y = _run(gq, bits, w, scale, x)
+    ns = np.unique(np.concatenate([np.arange(0, N, 911), [127, 128, N - 1]]))
+    ts = np.unique(np.concatenate([np.arange(0, T, 41), [63, 64, 127, 128, T - 1]]))
+    want = _oracle(bits, w[ns], scale[ns], x[ts], ts.size, ns.size, K)
+    _check(bits, y[np.ix_(ts, ns)], want, w[ns], scale[ns], x[ts], T, ns.size, K)
