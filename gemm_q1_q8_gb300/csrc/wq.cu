@@ -11,11 +11,11 @@
 // Codes become floats exactly: a biased code (byte ^ 0x80, or nibble ^ 8) is placed in the low bits
 // of 2^23's bit pattern by a byte permute, and one subtraction removes 2^23 plus the bias.
 //
-// GEMV (T <= 4 tokens): a thread block covers 32/T rows; its eight warps take the 512-column chunks
-// of K in turn (chunk c to warp c % 8), each lane 16 consecutive columns of a chunk, so a warp's
-// load of one row is 512 (8-bit) or 256 (4-bit) contiguous bytes.  The lane keeps one partial sum
-// per (row, token) -- 32 in all -- and a butterfly over the lanes leaves lane l with the total of
-// value l; the eight warps' totals are then added in a fixed tree.
+// GEMV (T <= 4 tokens): a thread block covers 32/T rows, 8 at a time; its eight warps take the
+// 512-column chunks of K in turn (chunk c to warp c % 8), each lane 16 consecutive columns of a
+// chunk, so a warp's load of one row is 512 (8-bit) or 256 (4-bit) contiguous bytes.  Per (row,
+// token) a lane keeps the even- and odd-column sums as one f32 pair; after the chunks the lanes
+// are reduced by halving exchanges and the eight warps' totals are added in a fixed tree.
 //
 // GEMM (T > 4): a thread block computes 128 rows x 128 tokens, K staged 32 columns at a time.  The
 // codes are turned into floats (times the group scale for 4 bits) into shared memory once per
@@ -60,46 +60,70 @@ __device__ __forceinline__ void decode16(const uint32_t (&wd)[BITS == 8 ? 4 : 2]
 constexpr int kGvWarps = 8;
 constexpr int kChunk = 512;                       // columns per warp step (16 per lane)
 
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+    return fadd2(a, make_float2(-b.x, -b.y));     // negation is exact
+}
+
+// The 16 codes of one lane's slice as 8 float pairs (codes 2i, 2i+1), exact.
+template <int BITS>
+__device__ __forceinline__ void decode16x2(const uint32_t (&wd)[BITS == 8 ? 4 : 2], float2 (&cf)[8]) {
+    if constexpr (BITS == 8) {
+        const float2 bias = make_float2(8388736.0f, 8388736.0f);             // 2^23 + 128
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t b = wd[i] ^ 0x80808080u;
+            cf[2 * i] = fsub2(make_float2(__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7440)),
+                                          __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7441))), bias);
+            cf[2 * i + 1] = fsub2(make_float2(__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7442)),
+                                              __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7443))), bias);
+        }
+    } else {
+        const float2 bias = make_float2(8388616.0f, 8388616.0f);             // 2^23 + 8
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t ev = (wd[i] & 0x0F0F0F0Fu) ^ 0x08080808u;          // nibbles 0, 2, 4, 6
+            const uint32_t od = ((wd[i] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;   // nibbles 1, 3, 5, 7
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                cf[4 * i + j] = fsub2(make_float2(__uint_as_float(__byte_perm(ev, 0x4B000000u, 0x7440 + j)),
+                                                  __uint_as_float(__byte_perm(od, 0x4B000000u, 0x7440 + j))), bias);
+        }
+    }
+}
+
+// GEMV: 32/T rows per thread block, taken 8 rows at a time; warp w takes the 512-column chunks
+// w, w + 8, ... of K.  A lane keeps two partial sums per (row, token) -- even and odd columns of
+// its 16 -- as one f32 pair (fma.f32x2), adds them at the end of its chunks, and the lanes are
+// then reduced by halving exchanges (lane l ends with value (l >> (5 - log2 V)) of the V = 8T).
 template <int BITS, int T>
-__global__ void __launch_bounds__(kGvWarps * 32, 2)
+__global__ void __launch_bounds__(kGvWarps * 32, T == 1 ? 3 : 1)   // one token: 3 blocks per SM, one wave
 wq_gemv_kernel(const uint32_t* __restrict__ w, const float* __restrict__ scale, const float* __restrict__ x,
                float* __restrict__ y, int N, int K, int Tn) {
     constexpr int R = 32 / T;                     // rows per thread block
+    constexpr int V = 8 * T;                      // values per lane per row batch
     constexpr int WPL = BITS == 8 ? 4 : 2;        // words per lane per chunk
-    __shared__ float part[kGvWarps][32];
+    __shared__ float part[kGvWarps][R * T];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * R;
     const size_t wpr = static_cast<size_t>(K) * BITS / 32;   // words per row
     const int G = (K + 127) / 128;
     const int nchunks = (K + kChunk - 1) / kChunk;
-    float acc[R][T];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int u = 0; u < T; ++u) acc[r][u] = 0.0f;
 
-    for (int c = warp; c < nchunks; c += kGvWarps) {
-        const int k0 = c * kChunk + 16 * lane;
-        if (k0 < K) {                             // K % 32 == 0: a live lane has all 16 columns
-            float xv[T][16];
 #pragma unroll
-            for (int u = 0; u < T; ++u) {
-                // tokens past Tn (a 3-token call through the 4-token kernel) repeat the last one
-                const float4* xp = reinterpret_cast<const float4*>(x + static_cast<size_t>(min(u, Tn - 1)) * K + k0);
+    for (int rb = 0; rb < R; rb += 8) {
+        float2 acc[8][T];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 a = __ldg(xp + q);
-                    xv[u][4 * q] = a.x; xv[u][4 * q + 1] = a.y; xv[u][4 * q + 2] = a.z; xv[u][4 * q + 3] = a.w;
-                }
-            }
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int rb = 0; rb < R; rb += 8) {
+            for (int u = 0; u < T; ++u) acc[i][u] = make_float2(0.0f, 0.0f);
+        for (int c = warp; c < nchunks; c += kGvWarps) {
+            const int k0 = c * kChunk + 16 * lane;
+            if (k0 < K) {                         // K % 32 == 0: a live lane has all 16 columns
                 uint32_t wd[8][WPL];
                 float sc[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int n = min(n0 + rb + i, N - 1);        // past-the-end rows: computed, not stored
-                    if constexpr (BITS == 4) sc[i] = __ldg(scale + static_cast<size_t>(n) * G + k0 / 128);
                     const uint32_t* p = w + static_cast<size_t>(n) * wpr + static_cast<size_t>(k0) * BITS / 32;
                     if constexpr (BITS == 8) {
                         const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
@@ -107,52 +131,67 @@ wq_gemv_kernel(const uint32_t* __restrict__ w, const float* __restrict__ scale, 
                     } else {
                         const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
                         wd[i][0] = a.x; wd[i][1] = a.y;
+                        sc[i] = __ldg(scale + static_cast<size_t>(n) * G + k0 / 128);
+                    }
+                }
+                float2 xv[T][8];
+#pragma unroll
+                for (int u = 0; u < T; ++u) {
+                    // tokens past Tn (a 3-token call through the 4-token kernel) repeat the last one
+                    const float4* xp = reinterpret_cast<const float4*>(x + static_cast<size_t>(min(u, Tn - 1)) * K + k0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 a = __ldg(xp + q);
+                        xv[u][2 * q] = make_float2(a.x, a.y);
+                        xv[u][2 * q + 1] = make_float2(a.z, a.w);
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    float cf[16];
-                    decode16<BITS>(wd[i], cf);
-                    if constexpr (BITS == 8) {
+                    float2 cf[8];
+                    decode16x2<BITS>(wd[i], cf);
 #pragma unroll
-                        for (int u = 0; u < T; ++u)
+                    for (int u = 0; u < T; ++u) {
+                        if constexpr (BITS == 8) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) acc[rb + i][u] = __fmaf_rn(cf[j], xv[u][j], acc[rb + i][u]);
-                    } else {
+                            for (int j = 0; j < 8; ++j) acc[i][u] = ffma2(cf[j], xv[u][j], acc[i][u]);
+                        } else {
+                            float2 p = fmul2(cf[0], xv[u][0]);
 #pragma unroll
-                        for (int u = 0; u < T; ++u) {
-                            float p = __fmul_rn(cf[0], xv[u][0]);
-#pragma unroll
-                            for (int j = 1; j < 16; ++j) p = __fmaf_rn(cf[j], xv[u][j], p);
-                            acc[rb + i][u] = __fmaf_rn(sc[i], p, acc[rb + i][u]);
+                            for (int j = 1; j < 8; ++j) p = ffma2(cf[j], xv[u][j], p);
+                            // one sum per (row, token) for 4 bits: the even/odd pair is added first
+                            acc[i][u].x = __fmaf_rn(sc[i], __fadd_rn(p.x, p.y), acc[i][u].x);
                         }
                     }
                 }
             }
         }
-    }
-    // lanes -> lane l holds the warp's total of value l = (row l / T, token l % T)
-    float v[32];
+        float v[V];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int u = 0; u < T; ++u) v[r * T + u] = acc[r][u];
+            for (int u = 0; u < T; ++u) v[i * T + u] = __fadd_rn(acc[i][u].x, acc[i][u].y);
+        // halving exchanges over lane bits 4, 3, ... until one value is left, then plain butterflies
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        const bool hi = (lane & s) != 0;
+        for (int h = V / 2, m = 16; h >= 1; h >>= 1, m >>= 1) {
+            const bool hi = (lane & m) != 0;
 #pragma unroll
-        for (int j = 0; j < s; ++j) {
-            const float send = hi ? v[j] : v[j + s];
-            const float keep = hi ? v[j + s] : v[j];
-            v[j] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, s));
+            for (int j = 0; j < h; ++j) {
+                const float send = hi ? v[j] : v[j + h];
+                const float keep = hi ? v[j + h] : v[j];
+                v[j] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, m));
+            }
         }
+#pragma unroll
+        for (int m = 16 / V; m >= 1; m >>= 1) v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], m));
+        const int idx = lane / (32 / V);          // (row i, token u) = (idx / T, idx % T)
+        if (lane % (32 / V) == 0) part[warp][rb * T + idx] = v[0];
     }
-    part[warp][lane] = v[0];
     __syncthreads();
-    if (warp == 0) {
-        const float tot = __fadd_rn(__fadd_rn(__fadd_rn(part[0][lane], part[1][lane]), __fadd_rn(part[2][lane], part[3][lane])),
-                                    __fadd_rn(__fadd_rn(part[4][lane], part[5][lane]), __fadd_rn(part[6][lane], part[7][lane])));
-        const int n = n0 + lane / T, u = lane % T;
+    for (int e = threadIdx.x; e < R * T; e += blockDim.x) {
+        const float tot = __fadd_rn(__fadd_rn(__fadd_rn(part[0][e], part[1][e]), __fadd_rn(part[2][e], part[3][e])),
+                                    __fadd_rn(__fadd_rn(part[4][e], part[5][e]), __fadd_rn(part[6][e], part[7][e])));
+        const int n = n0 + e / T, u = e % T;
         if (n < N && u < Tn) {
             const float out = (BITS == 8) ? __fmul_rn(__ldg(scale + n), tot) : tot;
             y[static_cast<size_t>(u) * N + n] = out;
