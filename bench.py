@@ -342,6 +342,13 @@ def bench_gemv_shapes(gq, torch, dev, hbm_peak, items, wbytes):
     launches = sum(1 if (r + 127) // 128 < sms else 2 for _, _, _, r, _ in items)
     out["sweep_per_matrix_graph"] = {"us_per_token": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
                                      "hbm_frac": round(wbytes / t / 1e9 / hbm_peak, 4), "launches_per_token": launches}
+    # the grouped sweep over f32 activations, quantized to Q8_0 inside the constants launch
+    xs = [torch.from_numpy(wl.f32_normal(wl.Rng(500 + i), nn)).to(dev) for i, (_, _, _, _, nn) in enumerate(items)]
+    g32 = gq.GroupedGemv([(pk, x, yy, r, nn) for (pk, _, yy, r, nn), x in zip(items, xs)], device=dev)
+    t = time_graph(g32, 1, 2, reps=20)
+    out["sweep_grouped_f32_acts"] = {"us_per_token": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
+                                     "hbm_frac": round(wbytes / t / 1e9 / hbm_peak, 4),
+                                     "act_f32_bytes": 4 * sum(nn for _, _, _, _, nn in items)}
     return out
 
 

@@ -16,7 +16,8 @@ from . import build as _build
 
 __all__ = [
     "lib", "GQError", "PATH_AUTO", "PATH_DP4A", "PATH_LUT4", "PATH_MMA", "PATH_FMA",
-    "q1_0_packed_bytes", "q1_0_pack", "q1_q8_gemv", "q1_q8_gemv_noalloc", "GroupedGemv", "q1_q8_gemm",
+    "q1_0_packed_bytes", "q1_0_pack", "q1_q8_gemv", "q1_q8_gemv_f32", "q1_q8_gemv_noalloc", "GroupedGemv",
+    "q1_q8_gemm", "ACT_Q8_0", "ACT_F32",
     "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm", "q1s32_f32_gemm",
     "matvec_q8", "matmul_q8", "matvec_q4g128", "matmul_q4g128",
     "device_error", "version",
@@ -33,7 +34,10 @@ class GQError(RuntimeError):
 class _Desc(ctypes.Structure):
     _fields_ = [("packed_w", ctypes.c_void_p), ("act", ctypes.c_void_p), ("y", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("rows", ctypes.c_int), ("n", ctypes.c_int),
-                ("tile_begin", ctypes.c_int), ("reserved", ctypes.c_int)]
+                ("tile_begin", ctypes.c_int), ("act_format", ctypes.c_int)]
+
+
+ACT_Q8_0, ACT_F32 = 0, 1
 
 
 def lib():
@@ -55,6 +59,7 @@ def lib():
             "gq_q1_q8_workspace_bytes": (S, [I]),
             "q1_q8_gemv": (I, [P, P, P, I, I, P, P]),
             "q1_q8_gemv_noalloc": (I, [P, P, P, I, I, P]),
+            "q1_q8_gemv_f32": (I, [P, P, P, I, I, P, P]),
             "gq_gemv_group_plan": (I, [P, I, P]),
             "q1s32_f32_gemm": (I, [P, P, P, P, I, I, I, I, P]),
             "matvec_q8": (I, [P, P, P, P, I, I, P]),
@@ -146,6 +151,20 @@ def q1_q8_gemv(packed: torch.Tensor, act: torch.Tensor, rows: int, n: int, out: 
     return y
 
 
+def q1_q8_gemv_f32(packed: torch.Tensor, x: torch.Tensor, rows: int, n: int, out: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None):
+    """y[r] for a packed rows x n Q1_0 matrix and one f32 activation vector (n values), quantized to
+    Q8_0 inside the call: bit-identical to quantize_q8_0 followed by q1_q8_gemv."""
+    _need(x, torch.float32, n, "x")
+    _need(packed, torch.uint8, q1_0_packed_bytes(rows, n), "packed")
+    y = torch.empty(rows, dtype=torch.float32, device=x.device) if out is None else out
+    _need(y, torch.float32, rows, "out")
+    ws = torch.empty(workspace_bytes(n), dtype=torch.uint8, device=x.device) if workspace is None else workspace
+    _need(ws, torch.uint8, workspace_bytes(n), "workspace")
+    _check(lib().q1_q8_gemv_f32(_ptr(packed), _ptr(x), _ptr(y), rows, n, _ptr(ws), _stream()), "q1_q8_gemv_f32")
+    return y
+
+
 def q1_q8_gemv_noalloc(packed: torch.Tensor, act: torch.Tensor, rows: int, n: int,
                        out: torch.Tensor | None = None):
     """q1_q8_gemv without a caller workspace: the library's built-in scratch block is used (for
@@ -163,7 +182,8 @@ class GroupedGemv:
     """A planned grouped GEMV: one launch over many (packed weights, activation, output) triples."""
 
     def __init__(self, items, device="cuda"):
-        """items: sequence of (packed, act, y, rows, n) with CUDA tensors (kept alive here)."""
+        """items: sequence of (packed, act, y, rows, n) with CUDA tensors (kept alive here); an act
+        of dtype uint8 holds n/32 Q8_0 blocks, one of dtype float32 n values quantized in the call."""
         self._keep = []
         host = (_Desc * len(items))()
         offs, total = [], 0
@@ -174,10 +194,14 @@ class GroupedGemv:
         self.counter = self.workspace[total:total + 16].view(torch.int32)
         base = self.workspace.data_ptr()
         for i, (packed, act, y, rows, n) in enumerate(items):
-            _need(act, torch.uint8, (n // 32) * 34, f"act[{i}]")
+            fmt = ACT_F32 if act.dtype == torch.float32 else ACT_Q8_0
+            if fmt == ACT_F32:
+                _need(act, torch.float32, n, f"act[{i}]")
+            else:
+                _need(act, torch.uint8, (n // 32) * 34, f"act[{i}]")
             _need(packed, torch.uint8, q1_0_packed_bytes(rows, n), f"packed[{i}]")
             _need(y, torch.float32, rows, f"y[{i}]")
-            host[i] = _Desc(packed.data_ptr(), act.data_ptr(), y.data_ptr(), base + offs[i], rows, n, 0, 0)
+            host[i] = _Desc(packed.data_ptr(), act.data_ptr(), y.data_ptr(), base + offs[i], rows, n, 0, fmt)
             self._keep += [packed, act, y]
         tiles = ctypes.c_int(0)
         _check(lib().gq_gemv_group_plan(ctypes.cast(host, ctypes.c_void_p), len(items), ctypes.byref(tiles)),

@@ -78,8 +78,17 @@ int q1_q8_gemv(const void* packed_w, const void* act, float* y, int rows, int n,
     const int st = check_q1(packed_w, act, y, rows, n);
     if (st != GQ_OK) return st;
     if (!workspace || !aligned(workspace, 16)) return GQ_EINVAL_PTR;
-    return cuda_status(
-        gq::launch_q1_gemv(packed_w, act, y, rows, n, workspace, reinterpret_cast<cudaStream_t>(stream)));
+    return cuda_status(gq::launch_q1_gemv(packed_w, act, y, rows, n, workspace, GQ_ACT_Q8_0,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int q1_q8_gemv_f32(const void* packed_w, const float* x, float* y, int rows, int n, void* workspace,
+                   gq_stream_t stream) {
+    const int st = check_q1(packed_w, x, y, rows, n);
+    if (st != GQ_OK) return st;
+    if (!aligned(x, 16) || !workspace || !aligned(workspace, 16)) return GQ_EINVAL_PTR;
+    return cuda_status(gq::launch_q1_gemv(packed_w, x, y, rows, n, workspace, GQ_ACT_F32,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int gq_gemv_group_plan(gq_gemv_desc* descs, int count, int* total_tiles) {
@@ -88,6 +97,8 @@ int gq_gemv_group_plan(gq_gemv_desc* descs, int count, int* total_tiles) {
     for (int i = 0; i < count; ++i) {
         const int st = check_q1(descs[i].packed_w, descs[i].act, descs[i].y, descs[i].rows, descs[i].n);
         if (st != GQ_OK) return st;
+        if (descs[i].act_format != GQ_ACT_Q8_0 && descs[i].act_format != GQ_ACT_F32) return GQ_EINVAL_SHAPE;
+        if (descs[i].act_format == GQ_ACT_F32 && !aligned(descs[i].act, 16)) return GQ_EINVAL_PTR;
         if (!descs[i].workspace || !aligned(descs[i].workspace, 16)) return GQ_EINVAL_PTR;
     }
     // Largest n first (stable): the kernel hands tiles to warps in snake order over this list.
@@ -96,7 +107,6 @@ int gq_gemv_group_plan(gq_gemv_desc* descs, int count, int* total_tiles) {
     long long tiles = 0;
     for (int i = 0; i < count; ++i) {
         descs[i].tile_begin = static_cast<int>(tiles);
-        descs[i].reserved = 0;
         tiles += gq::gemv_tiles_for(descs[i].rows);
         if (tiles > 0x7fffffffLL) return GQ_EINVAL_SHAPE;
     }

@@ -142,6 +142,18 @@ __device__ __forceinline__ float f16_to_f32(uint32_t bits16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
 }
 
+// Q8_0 activation quantization of one value (the stated reading: amax over the 32-block,
+// d = amax / 127 rounded to nearest, stored as f16 rounded to nearest even; q = round half up of
+// x / d with the f32 d, clamped to [-127, 127]; amax = 0 gives q = 0).
+__device__ __forceinline__ float q8_0_scale(float amax) { return __fdiv_rn(amax, 127.0f); }
+__device__ __forceinline__ int q8_0_quant(float v, float amax, float dd) {
+    if (amax == 0.0f) return 0;
+    const float vv = __fdiv_rn(v, dd);
+    const float fl = floorf(vv);
+    const int qi = static_cast<int>(fl) + (__fsub_rn(vv, fl) >= 0.5f ? 1 : 0);
+    return max(-127, min(127, qi));
+}
+
 // --------------------------------------------------------------------------------------------
 // Launch bodies (defined in the per-operation .cu files; arguments already validated).
 // --------------------------------------------------------------------------------------------
@@ -151,7 +163,7 @@ constexpr int kMaxN = 1 << 20;                   // reduction length limit of th
 
 cudaError_t launch_q1_pack(const void* raw, int rows, int n, void* packed, cudaStream_t s);
 cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int rows, int n, void* workspace,
-                           cudaStream_t s);
+                           int act_format, cudaStream_t s);   // act_format: GQ_ACT_Q8_0 or GQ_ACT_F32
 size_t gemv_workspace_bytes(int n);
 cudaError_t launch_q1s32_f32(const uint32_t* signs, const float* ws, const float* x, float* y, int M, int N, int K,
                              int path, cudaStream_t s);   // path: GQ_PATH_FMA or GQ_PATH_LUT4

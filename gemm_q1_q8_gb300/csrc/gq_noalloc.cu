@@ -59,7 +59,8 @@ extern "C" int q1_q8_gemv_noalloc(const void* packed_w, const void* act, float* 
         return GQ_ECUDA;
     }
     // The launch writes the constants for this n and zeroes the counter before the GEMV reads them.
-    const cudaError_t e = gq::launch_q1_gemv(packed_w, act, y, rows, n, scratch, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t e = gq::launch_q1_gemv(packed_w, act, y, rows, n, scratch, GQ_ACT_Q8_0,
+                                                 reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         gq::record_cuda_error(static_cast<int>(e));
         return GQ_ECUDA;

@@ -27,14 +27,8 @@ quantize_kernel(const float* __restrict__ x, int m, int k, uint16_t* __restrict_
     float amax = fabsf(v);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float dd = __fdiv_rn(amax, 127.0f);
-    int qi = 0;
-    if (amax != 0.0f) {
-        const float vv = __fdiv_rn(v, dd);
-        const float fl = floorf(vv);
-        qi = static_cast<int>(fl) + (__fsub_rn(vv, fl) >= 0.5f ? 1 : 0);
-        qi = max(-127, min(127, qi));
-    }
+    const float dd = q8_0_scale(amax);
+    const int qi = q8_0_quant(v, amax, dd);
     q[base + lane] = static_cast<int8_t>(qi);
     if (lane == 0) d[gw] = __half_as_ushort(__float2half_rn(dd));
     if (op) {

@@ -97,6 +97,23 @@ __device__ __forceinline__ void act_lane_consts(const uint16_t* blk, int l, uint
                 qt, seed, d1s);
 }
 
+// The same from f32 activations, quantized to Q8_0 on the way (the values gq_quantize_q8_0 would
+// store): lane l of sub-block kg quantizes x[32 kg + 4 l .. + 3]; the sub-block's eight lanes are
+// eight consecutive, 8-aligned lanes of the warp, which exchange their amax.  x is 16-aligned.
+__device__ __forceinline__ void act_lane_consts_f32(const float* x, int kg, int l, uint32_t& qt, uint32_t& seed,
+                                                    float& d1s) {
+    const float4 v = *reinterpret_cast<const float4*>(x + static_cast<size_t>(kg) * 32 + 4 * l);
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float dd = q8_0_scale(amax);
+    const uint32_t qw = (static_cast<uint32_t>(q8_0_quant(v.x, amax, dd)) & 0xFFu) |
+                        ((static_cast<uint32_t>(q8_0_quant(v.y, amax, dd)) & 0xFFu) << 8) |
+                        ((static_cast<uint32_t>(q8_0_quant(v.z, amax, dd)) & 0xFFu) << 16) |
+                        (static_cast<uint32_t>(q8_0_quant(v.w, amax, dd)) << 24);
+    lane_consts(__half_as_ushort(__float2half_rn(dd)), qw, l, qt, seed, d1s);
+}
+
 // The eight lane values t_l = (sigma_l/2) * s_l of one 32-weight sub-block word (transposed
 // layout), as four f32 pairs (lanes 0-1, 2-3, 4-5, 6-7).
 __device__ __forceinline__ void lane_values(uint32_t w, const uint4& q0, const uint4& q1, const uint4& s0,
@@ -217,14 +234,17 @@ act_prep_kernel(gq_gemv_desc single, const gq_gemv_desc* __restrict__ descs, int
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const gq_gemv_desc d = (count == 0) ? single : descs[blockIdx.y];
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *counter = 0;
-    const int items = (d.n / 32) * 8;
+    const int items = (d.n / 32) * 8;     // a multiple of 32: whole warps take part in every step
     const uint8_t* act = static_cast<const uint8_t*>(d.act);
     uint32_t* ws = static_cast<uint32_t*>(d.workspace);
     for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < items; it += gridDim.x * blockDim.x) {
         const int kg = it >> 3, l = it & 7;
         uint32_t qt, seed;
         float d1s;
-        act_lane_consts(reinterpret_cast<const uint16_t*>(act + static_cast<size_t>(kg) * 34), l, qt, seed, d1s);
+        if (d.act_format == GQ_ACT_F32)
+            act_lane_consts_f32(static_cast<const float*>(d.act), kg, l, qt, seed, d1s);
+        else
+            act_lane_consts(reinterpret_cast<const uint16_t*>(act + static_cast<size_t>(kg) * 34), l, qt, seed, d1s);
         ws[kg * kConstWords + l] = qt;
         ws[kg * kConstWords + 8 + l] = seed;
         ws[kg * kConstWords + 16 + l] = __float_as_uint(d1s);
@@ -404,7 +424,7 @@ constexpr int kSmallPass = 32;            // blocks per pass through shared memo
 
 __global__ void __launch_bounds__(kSmallWarps * 32)
 q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ act, float* __restrict__ y,
-                     int rows, int nb) {
+                     int rows, int nb, int act_format) {
     __shared__ __align__(16) float4 s_ab[kSmallPass][2][32];            // ab of (block, row): two float4
     __shared__ float s_d0[kSmallPass][32];
     __shared__ __align__(16) uint32_t s_cst[kSmallWarps][4 * kConstWords];  // a warp's current block
@@ -429,8 +449,11 @@ q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restri
                 const int k = lane >> 3, l = lane & 7;
                 uint32_t qt, seed;
                 float d1s;
-                act_lane_consts(reinterpret_cast<const uint16_t*>(act + static_cast<size_t>(4 * b + k) * 34), l, qt,
-                                seed, d1s);
+                if (act_format == GQ_ACT_F32)
+                    act_lane_consts_f32(reinterpret_cast<const float*>(act), 4 * b + k, l, qt, seed, d1s);
+                else
+                    act_lane_consts(reinterpret_cast<const uint16_t*>(act + static_cast<size_t>(4 * b + k) * 34), l,
+                                    qt, seed, d1s);
                 s_cst[warp][k * kConstWords + l] = qt;
                 s_cst[warp][k * kConstWords + 8 + l] = seed;
                 s_cst[warp][k * kConstWords + 16 + l] = __float_as_uint(d1s);
@@ -706,7 +729,7 @@ static cudaError_t launch_gemv_dependent(int grid, cudaStream_t s, const GemvArg
 size_t gemv_workspace_bytes(int n) { return static_cast<size_t>(n / 32) * kConstWords * 4 + 16; }
 
 cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int rows, int n, void* workspace,
-                           cudaStream_t s) {
+                           int act_format, cudaStream_t s) {
     const int tiles = gemv_tiles_for(rows);
     static int sm_cached[64] = {0};
     int dev = 0;
@@ -720,14 +743,14 @@ cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int ro
     if (tiles < sm_cached[dev]) {
         // fewer tiles than SMs: the block-parallel kernel (one launch, no workspace)
         q1_gemv_small_kernel<<<(rows + 31) / 32, kSmallWarps * 32, 0, s>>>(
-            static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(act), y, rows, n / 128);
+            static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(act), y, rows, n / 128, act_format);
         return cudaGetLastError();
     }
     int grid = 0, active = 0;
     cudaError_t e = gemv_grid(tiles, &grid, &active);
     if (e != cudaSuccess) return e;
     int* counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + gemv_workspace_bytes(n) - 16);
-    gq_gemv_desc d{packed, act, y, workspace, rows, n, 0, 0};
+    gq_gemv_desc d{packed, act, y, workspace, rows, n, 0, act_format};
     act_prep_kernel<<<dim3(8, 1), 256, 0, s>>>(d, nullptr, 0, counter);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -114,6 +114,23 @@ size_t gq_q1_q8_workspace_bytes(int n);
 int q1_q8_gemv(const void* packed_w_device, const void* act_device, float* y_device,
                int rows, int n, void* workspace_device, gq_stream_t stream);
 
+/* Activation formats of the decode GEMV (gq_gemv_desc.act_format). */
+enum gq_act_format {
+    GQ_ACT_Q8_0 = 0,       /* n/32 Q8_0 blocks of 34 bytes (f16 d, 32 int8), 2-byte aligned       */
+    GQ_ACT_F32 = 1         /* n f32 values, 16-byte aligned, quantized to Q8_0 inside the call     */
+};
+
+/* The decode GEMV over f32 activations, with the Q8_0 quantization of the activations fused into
+ * the GEMV's activation-constant step (no separate quantize launch, no Q8_0 round trip through
+ * memory).  The result is bit-identical to gq_quantize_q8_0 on x followed by q1_q8_gemv: each
+ * 32-block is quantized as that call states (d = f16(amax / 127), q = round half up of x / d
+ * with the f32 d, clamped to [-127, 127]; an all-zero block gives d = 0, q = 0).  The pages do
+ * not describe a decode-side quantizer; this is the reading of the prefill one.
+ *   x_device: n f32, 16-byte aligned; other arguments and launches as q1_q8_gemv.
+ * Errors: as q1_q8_gemv, with GQ_EINVAL_PTR if x_device is NULL or not 16-aligned. */
+int q1_q8_gemv_f32(const void* packed_w_device, const float* x_device, float* y_device, int rows, int n,
+                   void* workspace_device, gq_stream_t stream);
+
 /* Largest n that q1_q8_gemv_noalloc accepts. */
 #define GQ_NOALLOC_MAX_N 16384
 
@@ -136,13 +153,13 @@ int q1_q8_gemv_noalloc(const void* packed_w_device, const void* act_device, floa
 /* One matrix of a grouped GEMV sweep (all fields filled by the caller except tile_begin). */
 typedef struct gq_gemv_desc {
     const void* packed_w;    /* device, from gq_q1_0_pack(rows, n)                      */
-    const void* act;         /* device, n/32 Q8_0 blocks                                */
+    const void* act;         /* device, n/32 Q8_0 blocks, or n f32 (act_format)         */
     float* y;                /* device, rows f32                                        */
     void* workspace;         /* device, gq_q1_q8_workspace_bytes(n), 16-aligned, its own */
     int rows;
     int n;
     int tile_begin;          /* filled by gq_gemv_group_plan                            */
-    int reserved;
+    int act_format;          /* GQ_ACT_Q8_0 (0) or GQ_ACT_F32 (quantized in the call)   */
 } gq_gemv_desc;
 
 /* Host-side planning for q1_q8_gemv_grouped: validates every descriptor (host array), sorts the

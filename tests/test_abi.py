@@ -74,6 +74,9 @@ X = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
     (lambda L: L.q1s32_q8_gemm(X, X, X, X, N, X, 8, 8, 96, 2, N), 1),
     (lambda L: L.q1s32_q8_gemm(X, X, X, X, N, X, 8, 8, 128, 1, N), 3),
     (lambda L: L.q1s32_q8_gemm(X, X, X, X, N, X, 8, 8, 128, 3, N), 2),
+    (lambda L: L.q1_q8_gemv_f32(X, X, X, 16, 1000, X, N), 1),
+    (lambda L: L.q1_q8_gemv_f32(X, ctypes.c_void_p(0x1008), X, 16, 1024, X, N), 2),
+    (lambda L: L.q1_q8_gemv_f32(X, X, X, 16, 1024, N, N), 2),
     (lambda L: L.matvec_q8(X, X, X, X, 8, 48, N), 1),
     (lambda L: L.matmul_q8(X, X, X, X, 0, 8, 64, N), 1),
     (lambda L: L.matvec_q4g128(X, X, X, X, 0, 64, N), 1),
@@ -121,3 +124,15 @@ def test_group_plan_host_only(L):
     assert tiles.value == 11
     descs[1].n = 2500
     assert L.gq_gemv_group_plan(ctypes.cast(descs, ctypes.c_void_p), 3, ctypes.byref(tiles)) == 1
+
+
+def test_group_plan_act_format(L):
+    """act_format must be Q8_0 (0) or F32 (1); an f32 activation must be 16-byte aligned."""
+    import gemm_q1_q8_gb300 as gq
+    tiles = ctypes.c_int(0)
+    for fmt, act, want in [(gq.ACT_F32, 0x2000, 0), (gq.ACT_F32, 0x2008, 2), (2, 0x2000, 1), (gq.ACT_Q8_0, 0x2002, 0)]:
+        descs = (gq._Desc * 1)()
+        descs[0] = gq._Desc(0x1000, act, 0x3000, 0x4000, 256, 1024, -1, fmt)
+        assert L.gq_gemv_group_plan(ctypes.cast(descs, ctypes.c_void_p), 1, ctypes.byref(tiles)) == want
+        if want == 0:
+            assert descs[0].act_format == fmt

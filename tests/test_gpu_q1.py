@@ -173,3 +173,62 @@ def test_bitnet_sweep_full_size_sampled(gq):
             want, _ = oracle.q1_q8_row(w[r * rb:(r + 1) * rb], a, n)
             assert_same_bits(got[r:r + 1], np.array([want]), f"row {r} of {rows}x{n}")
     assert gq.device_error() == 0
+
+
+# ----------------------------------------------------------------------------- fused quantization
+
+def _q8_0_blocks(x, n):
+    """The Q8_0 bytes (f16 d little-endian, then 32 int8) of the oracle's quantization of x."""
+    d, q = oracle.quantize_q8_0(x, 1, n)
+    blocks = np.zeros((n // 32, 34), dtype=np.uint8)
+    blocks[:, 0:2] = d.reshape(-1, 1).view(np.uint8).reshape(-1, 2)
+    blocks[:, 2:] = q.reshape(-1, 32).view(np.uint8)
+    return blocks.reshape(-1)
+
+
+def _act_f32(rng, n, kind):
+    x = wl.f32_normal(rng, n)
+    if kind == "zeros":                    # every third block all zero: d = 0, q = 0
+        x.reshape(-1, 32)[::3] = 0.0
+    elif kind == "ties":                   # x = (k + 1/2) * d for the block's own d: round half up
+        xb = x.reshape(-1, 32)
+        xb[:, 0] = 127.0
+        xb[:, 1:] = (np.round(xb[:, 1:] * 20) + 0.5).astype(np.float32)
+    elif kind == "range":                  # magnitudes spread over many binades
+        x = (x * np.exp2(rng.uniform(n) * 40 - 20)).astype(np.float32)
+    return x
+
+
+@pytest.mark.parametrize("rows,n,kind", [(256, 1024, "normal"), (256, 1024, "zeros"), (130, 2560, "ties"),
+                                         (2560, 2560, "range"), (19500, 256, "normal")])
+def test_gemv_f32_fused_quantize(gq, rows, n, kind):
+    """q1_q8_gemv_f32 == the oracle's Q8_0 quantization followed by the oracle GEMV, bit for bit."""
+    rng = wl.Rng(4242 + rows + n)
+    w = wl.q1_0_weights(rng, rows, n)
+    x = _act_f32(rng, n, kind)
+    packed = gq.q1_0_pack(to_dev(w), rows, n)
+    y = gq.q1_q8_gemv_f32(packed, to_dev(x), rows, n).cpu().numpy()
+    assert_same_bits(y, oracle.q1_q8_gemv(w, _q8_0_blocks(x, n), rows, n), f"gemv_f32 {rows}x{n} {kind}")
+
+
+def test_grouped_mixed_activation_formats(gq):
+    """A grouped sweep mixing Q8_0 and f32 activations: each output equals its own oracle GEMV."""
+    import torch
+    rng = wl.Rng(5151)
+    items, want = [], []
+    for i, (rows, n) in enumerate([(2560, 2560), (6912, 2560), (2560, 6912), (300, 1024)]):
+        w = wl.q1_0_weights(rng, rows, n)
+        packed = gq.q1_0_pack(to_dev(w), rows, n)
+        y = torch.empty(rows, dtype=torch.float32, device="cuda")
+        if i % 2 == 0:
+            x = _act_f32(rng, n, "normal")
+            items.append((packed, to_dev(x), y, rows, n))
+            want.append(oracle.q1_q8_gemv(w, _q8_0_blocks(x, n), rows, n))
+        else:
+            a = wl.q8_0_acts(rng, 1, n)
+            items.append((packed, to_dev(a), y, rows, n))
+            want.append(oracle.q1_q8_gemv(w, a, rows, n))
+    g = gq.GroupedGemv(items)
+    g()
+    for (_, _, y, rows, n), wv in zip(items, want):
+        assert_same_bits(y.cpu().numpy(), wv, f"grouped mixed {rows}x{n}")
