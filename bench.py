@@ -386,6 +386,33 @@ def run_only(args):
     print(json.dumps({"only": args.only, "kernels": res}), flush=True)
 
 
+PROBES = ("lut4_decode", "lut4_prefill", "wq8_gemv", "wq4_gemv", "wq8_gemm", "wq4_gemm")
+
+
+def run_probe(name):
+    """Three untimed calls of one kernel on its workload (14336 x 4096; one token or 512), for a
+    profiler to capture; prints a checksum."""
+    import torch
+    import gemm_q1_q8_gb300 as gq
+    N, K = 14336, 4096
+    if name.startswith("lut4"):
+        M = 1 if name == "lut4_decode" else 512
+        s, w, x = wl.prefill_inputs(wl.Rng(70), M, K, N)
+        s, w, x = (torch.from_numpy(a).cuda() for a in (s.view(np.int32), w, x))
+        f = lambda: gq.q1s32_f32_gemm(s, w, x, path=gq.PATH_LUT4)
+    else:
+        bits = 8 if name.startswith("wq8") else 4
+        T = 1 if name.endswith("gemv") else 512
+        w, sc, x = wl.wq_inputs(wl.Rng(90), T, K, N, bits)
+        w, sc, x = (torch.from_numpy(a).cuda() for a in (w.view(np.int32), sc, x))
+        fn = {(8, 1): gq.matvec_q8, (8, 512): gq.matmul_q8, (4, 1): gq.matvec_q4g128, (4, 512): gq.matmul_q4g128}
+        f = lambda: fn[(bits, T)](w, sc, x)
+    for _ in range(3):
+        y = f()
+    torch.cuda.synchronize()
+    print(json.dumps({"probe": name, "checksum": float(y.abs().sum())}), flush=True)
+
+
 def run_ours(args, rank, world, dist):
     import torch
     import gemm_q1_q8_gb300 as gq
@@ -533,10 +560,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--probe", choices=PROBES, default=None,
+                    help="run one kernel three times untimed on its workload (for ncu) and exit")
     ap.add_argument("--only", choices=["block_q8", "ternary", "w1a32", "wq", "prefill_lut4", "prefill_mma"], default=None,
                     help="time one secondary kernel on its workload and print only that")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.probe:
+        run_probe(args.probe)
+        return
     if args.only:
         run_only(args)
         return

@@ -422,9 +422,10 @@ constexpr size_t kGemvSmem = sizeof(WarpSmem) * kGemvWarps + kCachedDescs * size
 constexpr int kSmallWarps = 16;
 constexpr int kSmallPass = 32;            // blocks per pass through shared memory (42 KB static)
 
+template <int ACT>   // GQ_ACT_Q8_0 or GQ_ACT_F32
 __global__ void __launch_bounds__(kSmallWarps * 32)
 q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ act, float* __restrict__ y,
-                     int rows, int nb, int act_format) {
+                     int rows, int nb) {
     __shared__ __align__(16) float4 s_ab[kSmallPass][2][32];            // ab of (block, row): two float4
     __shared__ float s_d0[kSmallPass][32];
     __shared__ __align__(16) uint32_t s_cst[kSmallWarps][4 * kConstWords];  // a warp's current block
@@ -449,7 +450,7 @@ q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restri
                 const int k = lane >> 3, l = lane & 7;
                 uint32_t qt, seed;
                 float d1s;
-                if (act_format == GQ_ACT_F32)
+                if constexpr (ACT == GQ_ACT_F32)
                     act_lane_consts_f32(reinterpret_cast<const float*>(act), 4 * b + k, l, qt, seed, d1s);
                 else
                     act_lane_consts(reinterpret_cast<const uint16_t*>(act + static_cast<size_t>(4 * b + k) * 34), l,
@@ -742,8 +743,12 @@ cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int ro
     }
     if (tiles < sm_cached[dev]) {
         // fewer tiles than SMs: the block-parallel kernel (one launch, no workspace)
-        q1_gemv_small_kernel<<<(rows + 31) / 32, kSmallWarps * 32, 0, s>>>(
-            static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(act), y, rows, n / 128, act_format);
+        if (act_format == GQ_ACT_F32)
+            q1_gemv_small_kernel<GQ_ACT_F32><<<(rows + 31) / 32, kSmallWarps * 32, 0, s>>>(
+                static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(act), y, rows, n / 128);
+        else
+            q1_gemv_small_kernel<GQ_ACT_Q8_0><<<(rows + 31) / 32, kSmallWarps * 32, 0, s>>>(
+                static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(act), y, rows, n / 128);
         return cudaGetLastError();
     }
     int grid = 0, active = 0;
