@@ -18,11 +18,15 @@
 //   warps 4-19  : epilogue -- per 32-block, one tcgen05.ld of the 128x128 f32 block sums (each
 //                 warp its 32 TMEM lanes x 32 columns), p = dx*S, acc = fma(w_s, p, acc) in
 //                 registers; four epilogue warps per SMSP overlap their TMEM load latencies
-// Four smem stages (A 16 KB + B 16 KB each) and four TMEM accumulators of 128 columns.  The weight
-// producers also bring each stage's row scales (2 x 128 f32) into an 8-slot ring, so the epilogue
-// reads them from shared memory.  Slot k % 8 is written again for stage k + 8 only after the MMAs
-// of stage k + 4 completed, which needs every epilogue warp past stage k + 2: the slot's barrier
-// cannot run a phase ahead of an epilogue warp that still has to wait on it.  Every
+// Four smem stages (A 16 KB + B 16 KB each) and four TMEM accumulators of 128 columns, one per
+// 32-block (block b uses accumulator b % 4): each accumulator has its own "sums ready" and
+// "drained" barriers, so the MMAs of block b + 4 start as soon as the epilogue has drained block
+// b, and the epilogue of a block overlaps the MMAs of the next three.  The weight producers also
+// bring each stage's row scales (2 x 128 f32) into an 8-slot ring, so the epilogue reads them from
+// shared memory.  Slot k % 8 is written again for stage k + 8 only after the MMAs of stage k + 4
+// completed, which needs every epilogue warp past stage k + 2 (block 2k + 8 reuses the accumulator
+// of block 2k + 4): the slot's barrier cannot run a phase ahead of an epilogue warp that still has
+// to wait on it.  Every
 // wait is bounded (~1 s); a role that gives up raises an abort flag the others honour, and the
 // block drains its copies and MMAs and frees TMEM before it exits.
 #include "gq_internal.cuh"
@@ -36,7 +40,7 @@ constexpr int BM = 128;          // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;          // tokens per tile (MMA N)
 constexpr int BK = 64;           // K per stage (two 32-blocks)
 constexpr int kStagesM = 4;
-constexpr int kPairs = 2;        // TMEM: two pairs of 128-column accumulators (one pair per stage)
+constexpr int kAccs = 4;         // TMEM: four 128-column accumulators, one per 32-block in flight
 constexpr int kTmemCols = 512;
 constexpr int kTileA = BM * BK * 2;    // 16 KB
 constexpr int kTileB = BN * BK * 2;    // 16 KB
@@ -53,8 +57,9 @@ constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0
 
 struct Bars {
     uint64_t fullA[kStagesM], fullB[kStagesM];
-    uint64_t done[kStagesM];          // a stage's MMAs complete: smem stage free, block sums ready
-    uint64_t tempty[2];               // a TMEM pair drained by the epilogue
+    uint64_t done[kStagesM];          // a stage's MMAs complete: its smem stage is free
+    uint64_t bdone[kAccs];            // a block's MMAs complete: its sums are in its accumulator
+    uint64_t tempty[kAccs];           // an accumulator drained by the epilogue
     uint64_t wfull[2 * kStagesM];     // a row-scale slot written by the producers
     uint64_t final_;
     uint32_t tmem_base;
@@ -145,7 +150,10 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
             mbar_init(&bars->fullB[s], 1);
             mbar_init(&bars->done[s], 1);
         }
-        for (int p = 0; p < kPairs; ++p) mbar_init(&bars->tempty[p], kNumEWarps);
+        for (int p = 0; p < kAccs; ++p) {
+            mbar_init(&bars->bdone[p], 1);
+            mbar_init(&bars->tempty[p], kNumEWarps);
+        }
         for (int w = 0; w < kWSlots; ++w) mbar_init(&bars->wfull[w], kNumAWarps);
         mbar_init(&bars->final_, 1);
         bars->abort = 0;
@@ -179,27 +187,32 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
             }
         }
     } else if (warp == kWarpMma) {
-        // ---------------- MMA issue (one thread): one commit per stage
+        // ---------------- MMA issue (one thread): a commit per block, then one per stage
         if (lane == 0) {
-            for (int k = 0; k < stages && !*abort; ++k) {
+            bool live = true;
+            for (int k = 0; k < stages && live && !*abort; ++k) {
                 const int s = k % kStagesM;
-                const int pair = k % kPairs;
                 const uint32_t ph = static_cast<uint32_t>(k / kStagesM) & 1u;
                 if (!wait_or_abort(&bars->fullA[s], ph, abort) || !wait_or_abort(&bars->fullB[s], ph, abort)) break;
-                if (k >= kPairs &&
-                    !wait_or_abort(&bars->tempty[pair], static_cast<uint32_t>(k / kPairs - 1) & 1u, abort))
-                    break;
-                tc_fence_after();
 #pragma unroll
                 for (int bi = 0; bi < 2; ++bi) {
-                    const uint32_t d = tmem + static_cast<uint32_t>((pair * 2 + bi) * BN);
+                    const int b = 2 * k + bi;
+                    const int acc = b % kAccs;
+                    if (b >= kAccs &&
+                        !wait_or_abort(&bars->tempty[acc], static_cast<uint32_t>(b / kAccs - 1) & 1u, abort)) {
+                        live = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int koff = (bi * 32 + j * 16) * 2;     // bytes along the 128-byte row
                         tc_mma(d, smem_desc(sA + s * kTileA + koff), smem_desc(sB + s * kTileB + koff), j);
                     }
+                    tc_commit(&bars->bdone[acc]);
                 }
-                tc_commit(&bars->done[s]);
+                if (live) tc_commit(&bars->done[s]);
             }
             // all MMAs issued so far complete before TMEM may be freed
             tc_commit(&bars->final_);
@@ -315,23 +328,26 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
 #pragma unroll
         for (int j = 0; j < kECols; ++j) acc[j] = 0.0f;
         bool ok = true;
-        for (int k = 0; k < stages; ++k) {
-            const int s = k % kStagesM;
-            const int pair = k % kPairs;
-            // done[s]: the stage's block sums are in TMEM; wfull: its row scales are in the ring
-            if (!wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStagesM) & 1u, abort) ||
-                !wait_or_abort(&bars->wfull[k % kWSlots], static_cast<uint32_t>(k / kWSlots) & 1u, abort)) {
+        for (int k = 0; k < stages && ok; ++k) {
+            // wfull: the stage's row scales are in the ring
+            if (!wait_or_abort(&bars->wfull[k % kWSlots], static_cast<uint32_t>(k / kWSlots) & 1u, abort)) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
             const float* wslot = sws + (k % kWSlots) * 2 * BM;
             const float wb0 = wslot[r], wb1 = wslot[BM + r];
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi) {
                 const int b = 2 * k + bi;
+                const int accx = b % kAccs;
+                // bdone: the block's sums are in its accumulator
+                if (!wait_or_abort(&bars->bdone[accx], static_cast<uint32_t>(b / kAccs) & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>((pair * 2 + bi) * BN + h * kECols);
+                                       static_cast<uint32_t>(accx * BN + h * kECols);
                 const float4* dxr = reinterpret_cast<const float4*>(sdx + b * BN + h * kECols);
                 const float wsc = bi ? wb1 : wb0;
                 const float2 w2 = make_float2(wsc, wsc);
@@ -359,10 +375,10 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
                         acc[j + 3] = a23.y;
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->tempty[accx]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->tempty[pair]);
         }
         if (ok && n < N) {
 #pragma unroll
