@@ -396,7 +396,7 @@ def run_only(args):
     print(json.dumps({"only": args.only, "kernels": res}), flush=True)
 
 
-PROBES = ("lut4_decode", "lut4_prefill", "wq8_gemv", "wq4_gemv", "wq8_gemm", "wq4_gemm")
+PROBES = ("lut4_decode", "lut4_prefill", "wq8_gemv", "wq4_gemv", "wq8_gemm", "wq4_gemm", "bq8_m1", "bq8_m4")
 
 
 def run_probe(name):
@@ -405,7 +405,12 @@ def run_probe(name):
     import torch
     import gemm_q1_q8_gb300 as gq
     N, K = 14336, 4096
-    if name.startswith("lut4"):
+    if name.startswith("bq8"):
+        m = int(name[-1])
+        x, q, sc = wl.block_q8_inputs(wl.Rng(20), m, 960, 49152)
+        x, q, sc = (torch.from_numpy(a).cuda() for a in (x, q.view(np.int32), sc))
+        f = lambda: gq.block_q8_matmul_nt(x, q, sc)
+    elif name.startswith("lut4"):
         M = 1 if name == "lut4_decode" else 512
         s, w, x = wl.prefill_inputs(wl.Rng(70), M, K, N)
         s, w, x = (torch.from_numpy(a).cuda() for a in (s.view(np.int32), w, x))

@@ -193,6 +193,104 @@ block_q8_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants
     }
 }
 
+// One or two activation rows: a lane takes a whole 32-block of a weight row (its 32 codes are 32
+// contiguous bytes, so a warp's two 16-byte loads per row cover 1 KB of the row, coalesced), keeps
+// the block's activations in registers for every row, and runs the block sum in order; the warp's
+// rows are summed side by side (one independent chain per row).  The rounded products
+// scale*block_sum go through shared memory to lane r, which adds row r's blocks in order.  Blocks
+// beyond 32 per row are taken 32 at a time, the owner's acc carrying on across them.
+constexpr int kRwWarps = 8;
+
+// rows per warp: one independent block-sum chain each.  Seven for one token: 94 registers, two
+// thread blocks per SM, and for n = 49152 about 2.9 waves of warps (eight rows: 2.5 waves, whose
+// half-empty last wave cost ~8%)
+template <int MT>
+__host__ __device__ constexpr int rw_rows() { return MT == 1 ? 7 : 4; }
+
+template <int MT>
+__global__ void __launch_bounds__(kRwWarps * 32)
+block_q8_rowwarp_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants,
+                        const float* __restrict__ scales, float* __restrict__ y, int m, int k, int n) {
+    constexpr int R = rw_rows<MT>();
+    __shared__ float ps[kRwWarps][R][33];           // a warp's rounded block products, odd stride
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbk = k / 32;
+    const int row0 = (blockIdx.x * kRwWarps + warp) * R;
+    if (row0 >= n) return;                           // whole warps only: no block-wide barrier below
+    float accs[MT];                                  // lane r < R: row row0 + r
+#pragma unroll
+    for (int u = 0; u < MT; ++u) accs[u] = 0.0f;
+    for (int c0 = 0; c0 < nbk; c0 += 32) {
+        const int b = c0 + lane;
+        const bool live = b < nbk;
+        // the block's activations for the MT tokens
+        float xv[MT][32];
+#pragma unroll
+        for (int u = 0; u < MT; ++u) {
+            const float4* xp = reinterpret_cast<const float4*>(x + static_cast<size_t>(u < m ? u : m - 1) * k +
+                                                               static_cast<size_t>(live ? b : 0) * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 a = __ldg(xp + q4);
+                xv[u][4 * q4] = a.x; xv[u][4 * q4 + 1] = a.y; xv[u][4 * q4 + 2] = a.z; xv[u][4 * q4 + 3] = a.w;
+            }
+        }
+        uint32_t wq[R][8];
+        float sc[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int row = min(row0 + i, n - 1);    // past-the-end rows: computed, not stored
+            const uint4* qp = reinterpret_cast<const uint4*>(quants) + static_cast<size_t>(row) * (k / 16) +
+                              2 * static_cast<size_t>(live ? b : 0);
+            const uint4 w0 = __ldg(qp), w1 = __ldg(qp + 1);
+            wq[i][0] = w0.x ^ 0x80808080u; wq[i][1] = w0.y ^ 0x80808080u; wq[i][2] = w0.z ^ 0x80808080u;
+            wq[i][3] = w0.w ^ 0x80808080u; wq[i][4] = w1.x ^ 0x80808080u; wq[i][5] = w1.y ^ 0x80808080u;
+            wq[i][6] = w1.z ^ 0x80808080u; wq[i][7] = w1.w ^ 0x80808080u;
+            sc[i] = __ldg(scales + static_cast<size_t>(row) * nbk + (live ? b : 0));
+        }
+        float bs[R][MT];
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int u = 0; u < MT; ++u) bs[i][u] = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                // two codes at once: their biased floats, minus the bias in one packed (exact) subtraction
+                const uint32_t wv = wq[i][t >> 2];
+                const float2 q2 = fadd2(make_float2(__int_as_float(static_cast<int>(__byte_perm(wv, 0x4B000000u, 0x7540u | (t & 3)))),
+                                                    __int_as_float(static_cast<int>(__byte_perm(wv, 0x4B000000u, 0x7540u | ((t & 3) + 1))))),
+                                        make_float2(-kQBias, -kQBias));
+#pragma unroll
+                for (int u = 0; u < MT; ++u) {
+                    bs[i][u] = __fadd_rn(bs[i][u], __fmul_rn(xv[u][t], q2.x));
+                    bs[i][u] = __fadd_rn(bs[i][u], __fmul_rn(xv[u][t + 1], q2.y));
+                }
+            }
+        }
+        // per token: the rounded products to shared memory, lane r adds row r's in block order
+#pragma unroll
+        for (int u = 0; u < MT; ++u) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) ps[warp][i][lane] = __fmul_rn(sc[i], bs[i][u]);
+            __syncwarp();
+            if (lane < R) {
+                const int nb = min(32, nbk - c0);
+                float a = accs[u];
+                for (int j = 0; j < nb; ++j) a = __fadd_rn(a, ps[warp][lane][j]);
+                accs[u] = a;
+            }
+            __syncwarp();
+        }
+    }
+    if (lane < R && row0 + lane < n) {
+#pragma unroll
+        for (int u = 0; u < MT; ++u)
+            if (u < m) y[static_cast<size_t>(u) * n + row0 + lane] = accs[u];
+    }
+}
+
 // Many activation rows (m >= 8): each thread owns two weight columns and a tile of MT rows, the
 // two columns' chains side by side (two scalar rounded products, then one packed add), so each
 // broadcast activation load feeds two columns; the activation tile is staged transposed in passes
@@ -308,8 +406,20 @@ cudaError_t launch_mt(const float* x, const uint32_t* q, const float* s, float* 
 
 cudaError_t launch_block_q8(const float* x, const uint32_t* quants, const float* scales, float* y, int m, int k,
                             int n, cudaStream_t s) {
-    if (m <= 1) return launch_mt<1>(x, quants, scales, y, m, k, n, s);
-    if (m <= 2) return launch_mt<2>(x, quants, scales, y, m, k, n, s);
+    if (m <= 2) {
+        // x rows 16-byte aligned for the activations' vector loads (k % 32 == 0 and x 16-aligned)
+        if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+            if (m == 1) {
+                constexpr int rows = kRwWarps * rw_rows<1>();
+                block_q8_rowwarp_kernel<1><<<(n + rows - 1) / rows, kRwWarps * 32, 0, s>>>(x, quants, scales, y, m, k, n);
+            } else {
+                constexpr int rows = kRwWarps * rw_rows<2>();
+                block_q8_rowwarp_kernel<2><<<(n + rows - 1) / rows, kRwWarps * 32, 0, s>>>(x, quants, scales, y, m, k, n);
+            }
+            return cudaGetLastError();
+        }
+        return m <= 1 ? launch_mt<1>(x, quants, scales, y, m, k, n, s) : launch_mt<2>(x, quants, scales, y, m, k, n, s);
+    }
     if (m <= 4) return launch_mt<4>(x, quants, scales, y, m, k, n, s);
     if (m <= 8) return launch_mt<8>(x, quants, scales, y, m, k, n, s);
     return launch_mt<16>(x, quants, scales, y, m, k, n, s);

@@ -23,7 +23,8 @@ def gq():
 # ----------------------------------------------------------------------------- block_q8
 
 @pytest.mark.parametrize("m,k,n", [(1, 32, 1), (1, 960, 1001), (3, 96, 513), (4, 960, 257), (7, 64, 33),
-                                   (16, 960, 300), (17, 320, 129), (40, 128, 64)])
+                                   (16, 960, 300), (17, 320, 129), (40, 128, 64), (2, 2048, 700), (1, 2080, 100),
+                                   (4, 32, 33), (1, 960, 20000)])
 def test_block_q8_bit_exact(gq, m, k, n):
     rng = wl.Rng(m * 1000 + k + n)
     x, quants, scales = wl.block_q8_inputs(rng, m, k, n)
