@@ -339,6 +339,141 @@ lut4_decode_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constan
     // the other blocks leave: nothing reads their shared memory
 }
 
+// Decode of one token, persistent: one thread block per SM builds the tables of all of K once (the
+// activation is the same for every row), then takes 32-row tiles in turn.  A tile's sign words and
+// scales come by TMA (four 128-byte-wide boxes of 32 rows each, 128B swizzle) into a three-stage
+// ring, two tiles ahead of the one being summed.  The sixteen warps split a tile's blocks (warp w
+// the blocks w*nb/16 ...), each lane one row; the warps' partial sums are added in a fixed tree.
+constexpr int kPdWarps = 16;
+constexpr int kPdStages = 3;
+constexpr int kPdMaxBlocks = 160;                 // K <= 5120: the tables fit beside the ring
+constexpr int kPdBoxWords = 32;                   // words per TMA box row (128 bytes)
+
+struct PdLayout {
+    uint32_t ring, lut, part, bar, bytes;
+};
+__host__ __device__ inline PdLayout pd_layout(int nbk) {
+    PdLayout L{};
+    const uint32_t boxes = static_cast<uint32_t>((nbk + kPdBoxWords - 1) / kPdBoxWords);
+    const uint32_t stage = 2u * boxes * 32u * 128u;                      // signs then scales
+    L.ring = 0;
+    L.lut = kPdStages * stage;
+    L.part = L.lut + static_cast<uint32_t>(nbk) * 8u * kDecTab * 4u;
+    L.part = (L.part + 15u) & ~15u;
+    L.bar = L.part + kPdWarps * 32u * 4u;
+    L.bytes = L.bar + kPdStages * 8u;
+    return L;
+}
+
+__global__ void __launch_bounds__(kPdWarps * 32, 1)
+lut4_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmW,
+                              const float* __restrict__ x, float* __restrict__ y, int N, int K) {
+    extern __shared__ __align__(1024) uint8_t psm1[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(psm1) + 1023) & ~uintptr_t(1023));
+    const int nbk = K / 32;
+    const PdLayout L = pd_layout(nbk);
+    const int boxes = (nbk + kPdBoxWords - 1) / kPdBoxWords;
+    const uint32_t half = static_cast<uint32_t>(boxes) * 32u * 128u;    // bytes of one tensor in a stage
+    float* lut = reinterpret_cast<float*>(base + L.lut);                 // [block][group][kDecTab]
+    float* part = reinterpret_cast<float*>(base + L.part);               // [warp][lane]
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + L.bar);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles = (N + 31) / 32;
+
+    auto issue = [&](int t, int s) {              // thread 0: tile t into stage s
+        mbar_arrive_expect_tx(&full[s], 2u * half);
+        for (int bx = 0; bx < boxes; ++bx) {
+            tma_load_2d(base + L.ring + s * 2u * half + bx * 4096u, &tmS, bx * kPdBoxWords, t * 32, &full[s]);
+            tma_load_2d(base + L.ring + s * 2u * half + half + bx * 4096u, &tmW, bx * kPdBoxWords, t * 32, &full[s]);
+        }
+    };
+    int issued = 0;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmS);
+        prefetch_tmap(&tmW);
+        for (int s = 0; s < kPdStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+        for (int j = 0; j < kPdStages; ++j) {
+            const int t = blockIdx.x + j * gridDim.x;
+            if (t < tiles) {
+                issue(t, j);
+                ++issued;
+            }
+        }
+    }
+    // the tables of all K: one (block, group) per item
+    for (int it = threadIdx.x; it < nbk * 8; it += blockDim.x) {
+        const int j = it >> 3, g = it & 7;
+        const float4 a = ldg_x4(x, 0, K, j, g);
+        const float p0 = -(a.x + a.y), p1 = a.x - a.y;
+        const float q0 = -(a.z + a.w), q1 = a.z - a.w;
+        const float p[4] = {p0, p1, -p1, -p0};
+        const float qq[4] = {q0, q1, -q1, -q0};
+        float* dst = lut + static_cast<size_t>(it) * kDecTab;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = __fadd_rn(p[i & 3], qq[i >> 2]);
+    }
+    __syncthreads();
+
+    // whole 16-byte chunks (four blocks) per warp: nbk is a multiple of 4 (K % 128 == 0)
+    const int per = ((nbk + kPdWarps - 1) / kPdWarps + 3) & ~3;
+    const int jlo = warp * per, cnt = max(0, min(per, nbk - jlo));
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+        const int s = i % kPdStages;
+        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>(i / kPdStages) & 1u);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) report_error(kErrWaitTimeout);
+            break;
+        }
+        const uint8_t* sig = base + L.ring + s * 2u * half;
+        const uint8_t* scl = sig + half;
+        float acc = 0.0f;
+        for (int j4 = jlo; j4 < jlo + cnt; j4 += 4) {
+            // four blocks' words and scales: one 16-byte chunk of the lane's row in each (swizzled)
+            const uint32_t off = static_cast<uint32_t>(j4 / kPdBoxWords) * 4096u + static_cast<uint32_t>(lane) * 128u +
+                                 ((static_cast<uint32_t>((j4 % kPdBoxWords) >> 2) ^ static_cast<uint32_t>(lane & 7)) << 4);
+            const uint4 w4 = *reinterpret_cast<const uint4*>(sig + off);
+            const float4 s4 = *reinterpret_cast<const float4*>(scl + off);
+            const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const uint32_t w = wv[k4];
+                const float* tb = lut + static_cast<size_t>(j4 + k4) * 8 * kDecTab;
+                float S = tb[w & 15u];
+#pragma unroll
+                for (int g = 1; g < 8; ++g) S = __fadd_rn(S, tb[g * kDecTab + ((w >> (4 * g)) & 15u)]);
+                acc = __fmaf_rn(sv[k4], S, acc);
+            }
+        }
+        part[warp * 32 + lane] = acc;
+        __syncthreads();
+        if (warp == 0) {
+            float v[kPdWarps];
+#pragma unroll
+            for (int w2 = 0; w2 < kPdWarps; ++w2) v[w2] = part[w2 * 32 + lane];
+#pragma unroll
+            for (int h = kPdWarps / 2; h >= 1; h >>= 1)
+#pragma unroll
+                for (int w2 = 0; w2 < h; ++w2) v[w2] = __fadd_rn(v[w2], v[w2 + h]);
+            const int n = t * 32 + lane;
+            if (n < N) y[n] = v[0];
+        }
+        __syncthreads();                          // stage s and the partial sums are free
+        if (threadIdx.x == 0 && t + kPdStages * static_cast<int>(gridDim.x) < tiles) {
+            issue(t + kPdStages * gridDim.x, s);
+            ++issued;
+        }
+    }
+    if (threadIdx.x == 0) {
+        // after an early exit, copies still in flight land before shared memory is released
+        for (int j = i; j < issued; ++j)
+            if (!mbar_wait(&full[j % kPdStages], static_cast<uint32_t>(j / kPdStages) & 1u))
+                report_error(kErrDrainTimeout);
+    }
+}
+
 constexpr int kPreWarps = 8;
 constexpr int kPreRows = kPreWarps * 32;          // one row per lane
 constexpr int kPreStage = 4;                      // blocks per stage
@@ -523,6 +658,27 @@ cudaError_t launch_decode(const uint32_t* signs, const float* ws, const float* x
     return cudaLaunchKernelEx(&cfg, lut4_decode_kernel<T>, tmS, tmW, x, y, N, K, M, ks);
 }
 
+cudaError_t launch_decode_persistent(const uint32_t* signs, const float* ws, const float* x, float* y, int N, int K,
+                                     cudaStream_t s) {
+    static int configured = -1;
+    const int nbk = K / 32;
+    const size_t smem = pd_layout(nbk).bytes + 1024;
+    cudaError_t e = set_smem_once(lut4_decode_persistent_kernel, pd_layout(kPdMaxBlocks).bytes + 1024, configured);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    CUtensorMap tmS, tmW;
+    if (!make_tmap_2d(&tmS, signs, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, nbk, N, static_cast<uint64_t>(nbk) * 4,
+                      kPdBoxWords, 32, true) ||
+        !make_tmap_2d(&tmW, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, nbk, N, static_cast<uint64_t>(nbk) * 4,
+                      kPdBoxWords, 32, true))
+        return cudaErrorInvalidValue;
+    const int tiles = (N + 31) / 32;
+    lut4_decode_persistent_kernel<<<min(tiles, sms), kPdWarps * 32, smem, s>>>(tmS, tmW, x, y, N, K);
+    return cudaGetLastError();
+}
+
 template <int MQ>
 cudaError_t launch_prefill(const uint32_t* signs, const float* ws, const float* x, float* y, int N, int K, int M,
                            cudaStream_t s) {
@@ -543,6 +699,7 @@ cudaError_t launch_q1s32_f32(const uint32_t* signs, const float* ws, const float
         // decode through TMA needs rows of 16-byte multiples (K % 128 == 0) on 16-byte boundaries
         const bool tma_ok = K % 128 == 0 && (reinterpret_cast<uintptr_t>(signs) & 15) == 0 &&
                             (reinterpret_cast<uintptr_t>(ws) & 15) == 0;
+        if (M == 1 && tma_ok && K / 32 <= kPdMaxBlocks) return launch_decode_persistent(signs, ws, x, y, N, K, s);
         if (M == 1 && tma_ok) return launch_decode<1>(signs, ws, x, y, N, K, M, s);
         if (M == 2 && tma_ok) return launch_decode<2>(signs, ws, x, y, N, K, M, s);
         if (M <= 4 && tma_ok) return launch_decode<4>(signs, ws, x, y, N, K, M, s);
