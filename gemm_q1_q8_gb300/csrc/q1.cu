@@ -151,9 +151,11 @@ __device__ __forceinline__ float final_reduce(const float2 acc[4]) {
 //     lane: each activation word is loaded once for four rows); units are handed out through the
 //     counter, largest matrix first, so the greedy hand-out balances the warps.  Each warp streams
 //     its units' (unit, block) chunks -- the tile's sign bits and d0 of the block plus the
-//     block's 384 bytes of constants -- through a private ring of kStages stages: lane 0 refills
-//     the stage it has just consumed with the chunk kStages ahead, so the copies run ahead across
-//     unit boundaries.  Lane 0 claims the next unit when it requests the last block of the
+//     block's 384 bytes of constants -- through a private ring of kStages stages of two blocks
+//     each (two consecutive blocks' chunks are contiguous, and so are their constants, so a stage
+//     is still two bulk copies): lane 0 refills the stage it has just consumed with the blocks
+//     kStages stages ahead, so the copies run ahead across unit boundaries, and the waits and
+//     refills come once per two blocks.  Lane 0 claims the next unit when it requests the last block of the
 //     current one, so the counter's round trip overlaps a block of work.  The unit of each chunk
 //     run travels through a small per-warp queue; the end of the work is a full-barrier phase
 //     completed without data.  Every wait is bounded, and a warp that gives up first lets its
@@ -166,11 +168,12 @@ __device__ __forceinline__ float final_reduce(const float2 acc[4]) {
 // their accumulators on (for an even finish) costs as much as the uneven finish it removes.
 constexpr int kGemvR = 4;                                   // rows per lane: a warp covers a tile
 constexpr int kGemvWarps = 16;                              // 4 per SMSP (124 registers each)
-constexpr int kStages = 4;
+constexpr int kStages = 2;
+constexpr int kStageBlocks = 2;                             // blocks per ring stage
 constexpr int kCstBytes = 4 * kConstWords * 4;              // 384: constants of one block
 constexpr int kTileBits = kTileRows * 16;                   // sign bits of one (tile, block)
 constexpr int kTileD0 = kTileRows * 2;                      // d0 of one (tile, block)
-constexpr int kStageBytes = kTileBits + kTileD0 + kCstBytes;
+constexpr int kStageBytes = kStageBlocks * (kTileBits + kTileD0 + kCstBytes);
 constexpr int kCachedDescs = 2048;                          // tile_begin cached in smem up to this
 constexpr int kUnitQueue = 16;                              // > kStages + 1: units requested ahead
 static_assert(kUnitQueue > kStages + 1, "unit queue too short");
@@ -285,11 +288,15 @@ __device__ __forceinline__ void fetch_next(WarpSmem& ws, int& next_unit, int s, 
         F.blk = 0;
         F.blk_end = t.nb;
     }
+    // up to kStageBlocks consecutive blocks of the unit: their chunks are contiguous, and so are
+    // their constants
+    const int nblk = min(kStageBlocks, F.blk_end - F.blk);
     const uint8_t* ch = F.base + static_cast<size_t>(F.blk) * kChunkBytes;
-    mbar_arrive_expect_tx(&ws.full[s], kStageBytes);
-    bulk_g2s(ws.ring[s], ch, kTileBits + kTileD0, &ws.full[s]);
-    bulk_g2s(ws.ring[s] + kTileBits + kTileD0, F.cst + static_cast<size_t>(F.blk) * kCstBytes, kCstBytes, &ws.full[s]);
-    ++F.blk;
+    mbar_arrive_expect_tx(&ws.full[s], static_cast<uint32_t>(nblk) * (kTileBits + kTileD0 + kCstBytes));
+    bulk_g2s(ws.ring[s], ch, nblk * (kTileBits + kTileD0), &ws.full[s]);
+    bulk_g2s(ws.ring[s] + kStageBlocks * (kTileBits + kTileD0), F.cst + static_cast<size_t>(F.blk) * kCstBytes,
+             nblk * kCstBytes, &ws.full[s]);
+    F.blk += nblk;
     ++F.issued;
     if (F.blk == F.blk_end) next_unit = atomicAdd(a.counter, 1);     // consumed one block later
 }
@@ -346,10 +353,12 @@ q1_gemv_kernel(GemvArgs a) {
 #pragma unroll
             for (int p = 0; p < 4; ++p) acc[j][p] = make_float2(0.0f, 0.0f);
 
-        for (int blk = 0; blk < t.nb; ++blk, ++chunk) {
+        for (int blk0 = 0; blk0 < t.nb; blk0 += kStageBlocks, ++chunk) {
             const int s = chunk % kStages;
-            if (blk > 0 && !wait_chunk(ws, chunk, lane)) return;
-            const uint8_t* stage = ws.ring[s];
+            if (blk0 > 0 && !wait_chunk(ws, chunk, lane)) return;
+            const int nblk = min(kStageBlocks, t.nb - blk0);
+          for (int bb = 0; bb < nblk; ++bb) {   // the stage's blocks, in order
+            const uint8_t* stage = ws.ring[s] + bb * (kTileBits + kTileD0);
             uint4 wb[kGemvR];
             float d0[kGemvR];
 #pragma unroll
@@ -357,7 +366,8 @@ q1_gemv_kernel(GemvArgs a) {
                 wb[j] = reinterpret_cast<const uint4*>(stage)[lane + 32 * j];
                 d0[j] = f16_to_f32(reinterpret_cast<const uint16_t*>(stage + kTileBits)[lane + 32 * j]);
             }
-            const uint4* cst = reinterpret_cast<const uint4*>(stage + kTileBits + kTileD0);
+            const uint4* cst = reinterpret_cast<const uint4*>(ws.ring[s] + kStageBlocks * (kTileBits + kTileD0) +
+                                                              bb * kCstBytes);
 
             float2 ab[kGemvR][4];
 #pragma unroll
@@ -387,10 +397,12 @@ q1_gemv_kernel(GemvArgs a) {
                     }
                 }
             }
-            __syncwarp();                         // every lane has read the stage
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                fetch_next(ws, next_unit, s, a, s_tb);
+            if (bb == nblk - 1) {
+                __syncwarp();                     // every lane has read the stage
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    fetch_next(ws, next_unit, s, a, s_tb);
+                }
             }
 #pragma unroll
             for (int j = 0; j < kGemvR; ++j) {
@@ -398,6 +410,7 @@ q1_gemv_kernel(GemvArgs a) {
 #pragma unroll
                 for (int p = 0; p < 4; ++p) acc[j][p] = ffma2(dd, ab[j][p], acc[j][p]);
             }
+          }
         }
 #pragma unroll
         for (int j = 0; j < kGemvR; ++j) {
