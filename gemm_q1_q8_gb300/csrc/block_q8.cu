@@ -199,6 +199,8 @@ block_q8_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants
 // rows are summed side by side (one independent chain per row).  The rounded products
 // scale*block_sum go through shared memory to lane r, which adds row r's blocks in order.  Blocks
 // beyond 32 per row are taken 32 at a time, the owner's acc carrying on across them.
+// Launched as a programmatic dependent: the first weight rows are requested before the wait for
+// the preceding grids, the activations read and the outputs written after it.
 constexpr int kRwWarps = 8;
 
 // rows per warp: one independent block-sum chain each.  Seven for one token: 94 registers, two
@@ -216,6 +218,7 @@ block_q8_rowwarp_kernel(const float* __restrict__ x, const uint32_t* __restrict_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbk = k / 32;
     const int row0 = (blockIdx.x * kRwWarps + warp) * R;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (row0 >= n) return;                           // whole warps only: no block-wide barrier below
     float accs[MT];                                  // lane r < R: row row0 + r
 #pragma unroll
@@ -223,18 +226,6 @@ block_q8_rowwarp_kernel(const float* __restrict__ x, const uint32_t* __restrict_
     for (int c0 = 0; c0 < nbk; c0 += 32) {
         const int b = c0 + lane;
         const bool live = b < nbk;
-        // the block's activations for the MT tokens
-        float xv[MT][32];
-#pragma unroll
-        for (int u = 0; u < MT; ++u) {
-            const float4* xp = reinterpret_cast<const float4*>(x + static_cast<size_t>(u < m ? u : m - 1) * k +
-                                                               static_cast<size_t>(live ? b : 0) * 32);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 a = __ldg(xp + q4);
-                xv[u][4 * q4] = a.x; xv[u][4 * q4 + 1] = a.y; xv[u][4 * q4 + 2] = a.z; xv[u][4 * q4 + 3] = a.w;
-            }
-        }
         uint32_t wq[R][8];
         float sc[R];
 #pragma unroll
@@ -247,6 +238,19 @@ block_q8_rowwarp_kernel(const float* __restrict__ x, const uint32_t* __restrict_
             wq[i][3] = w0.w ^ 0x80808080u; wq[i][4] = w1.x ^ 0x80808080u; wq[i][5] = w1.y ^ 0x80808080u;
             wq[i][6] = w1.z ^ 0x80808080u; wq[i][7] = w1.w ^ 0x80808080u;
             sc[i] = __ldg(scales + static_cast<size_t>(row) * nbk + (live ? b : 0));
+        }
+        if (c0 == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // the preceding grids are done
+        // the block's activations for the MT tokens
+        float xv[MT][32];
+#pragma unroll
+        for (int u = 0; u < MT; ++u) {
+            const float4* xp = reinterpret_cast<const float4*>(x + static_cast<size_t>(u < m ? u : m - 1) * k +
+                                                               static_cast<size_t>(live ? b : 0) * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 a = __ldg(xp + q4);
+                xv[u][4 * q4] = a.x; xv[u][4 * q4 + 1] = a.y; xv[u][4 * q4 + 2] = a.z; xv[u][4 * q4 + 3] = a.w;
+            }
         }
         float bs[R][MT];
 #pragma unroll
@@ -409,14 +413,22 @@ cudaError_t launch_block_q8(const float* x, const uint32_t* quants, const float*
     if (m <= 2) {
         // x rows 16-byte aligned for the activations' vector loads (k % 32 == 0 and x 16-aligned)
         if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.blockDim = dim3(kRwWarps * 32);
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
             if (m == 1) {
                 constexpr int rows = kRwWarps * rw_rows<1>();
-                block_q8_rowwarp_kernel<1><<<(n + rows - 1) / rows, kRwWarps * 32, 0, s>>>(x, quants, scales, y, m, k, n);
-            } else {
-                constexpr int rows = kRwWarps * rw_rows<2>();
-                block_q8_rowwarp_kernel<2><<<(n + rows - 1) / rows, kRwWarps * 32, 0, s>>>(x, quants, scales, y, m, k, n);
+                cfg.gridDim = dim3((n + rows - 1) / rows);
+                return cudaLaunchKernelEx(&cfg, block_q8_rowwarp_kernel<1>, x, quants, scales, y, m, k, n);
             }
-            return cudaGetLastError();
+            constexpr int rows = kRwWarps * rw_rows<2>();
+            cfg.gridDim = dim3((n + rows - 1) / rows);
+            return cudaLaunchKernelEx(&cfg, block_q8_rowwarp_kernel<2>, x, quants, scales, y, m, k, n);
         }
         return m <= 1 ? launch_mt<1>(x, quants, scales, y, m, k, n, s) : launch_mt<2>(x, quants, scales, y, m, k, n, s);
     }

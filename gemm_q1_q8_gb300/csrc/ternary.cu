@@ -13,6 +13,12 @@
 // one thread per row -- count their chunk and add into shared-memory totals.  K beyond four
 // chunks goes to more thread blocks of the same rows, which add their totals into y (zeroed on
 // the stream first); with K <= 4096 y is written once.
+//
+// The kernel is launched as a programmatic dependent of the work before it on the stream: it lets
+// its own dependents start at once, requests the weight planes P and N (which nothing before it
+// writes), and only then waits for the preceding grids before it requests the activation plane X
+// and, later, writes y.  In a stream of GEMVs the weights of the next one stream in while the
+// current one finishes.
 #include "gq_internal.cuh"
 
 namespace gq {
@@ -60,6 +66,7 @@ ternary_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ 
     const int nch = min(kChunksPerCta, chunks - c0);
     const uint32_t chunk_bytes = 2u * rt * kChunkRowBytes + static_cast<uint32_t>(batch) * kChunkRowBytes;
 
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmP);
         prefetch_tmap(&tmN);
@@ -71,9 +78,12 @@ ternary_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ 
             mbar_arrive_expect_tx(&bars[c], chunk_bytes);
             tma_load_2d(base + L.p_off + po, &tmP, (c0 + c) * kWords, row0, &bars[c]);
             tma_load_2d(base + L.n_off + po, &tmN, (c0 + c) * kWords, row0, &bars[c]);
+        }
+        // the activations (and, below, the outputs) only after the preceding grids are done
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        for (int c = 0; c < nch; ++c)
             tma_load_2d(base + L.x_off + static_cast<uint32_t>(c) * batch * kChunkRowBytes, &tmX, (c0 + c) * kWords, 0,
                         &bars[c]);
-        }
     }
     for (int i = threadIdx.x; i < batch * rt; i += blockDim.x) red[i] = 0;
     for (int i = threadIdx.x; i < rt; i += blockDim.x) pnr[i] = 0;
@@ -179,9 +189,17 @@ cudaError_t launch_ternary(const uint32_t* P, const uint32_t* N, const uint32_t*
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    const dim3 grid((rows + rt - 1) / rt, slices);
-    ternary_kernel<<<grid, kChunksPerCta * rt, smem, s>>>(tmP, tmN, tmX, y, rows, k, batch, rt, slices > 1);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((rows + rt - 1) / rt, slices);
+    cfg.blockDim = dim3(kChunksPerCta * rt);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ternary_kernel, tmP, tmN, tmX, y, rows, k, batch, rt, slices > 1 ? 1 : 0);
 }
 
 }  // namespace gq

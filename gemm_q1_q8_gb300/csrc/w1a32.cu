@@ -344,6 +344,8 @@ lut4_decode_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constan
 // scales come by TMA (four 128-byte-wide boxes of 32 rows each, 128B swizzle) into a three-stage
 // ring, two tiles ahead of the one being summed.  The sixteen warps split a tile's blocks (warp w
 // the blocks w*nb/16 ...), each lane one row; the warps' partial sums are added in a fixed tree.
+// Launched as a programmatic dependent: the first tiles' copies are requested before the wait for
+// the preceding grids, the activations (tables) read and the outputs written after it.
 constexpr int kPdWarps = 16;
 constexpr int kPdStages = 3;
 constexpr int kPdMaxBlocks = 160;                 // K <= 5120: the tables fit beside the ring
@@ -388,6 +390,7 @@ lut4_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmS, const __g
         }
     };
     int issued = 0;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmS);
         prefetch_tmap(&tmW);
@@ -401,6 +404,7 @@ lut4_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmS, const __g
             }
         }
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");       // the preceding grids are done
     // the tables of all K: one (block, group) per item
     for (int it = threadIdx.x; it < nbk * 8; it += blockDim.x) {
         const int j = it >> 3, g = it & 7;
@@ -675,8 +679,17 @@ cudaError_t launch_decode_persistent(const uint32_t* signs, const float* ws, con
                       kPdBoxWords, 32, true))
         return cudaErrorInvalidValue;
     const int tiles = (N + 31) / 32;
-    lut4_decode_persistent_kernel<<<min(tiles, sms), kPdWarps * 32, smem, s>>>(tmS, tmW, x, y, N, K);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(min(tiles, sms));
+    cfg.blockDim = dim3(kPdWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lut4_decode_persistent_kernel, tmS, tmW, x, y, N, K);
 }
 
 template <int MQ>

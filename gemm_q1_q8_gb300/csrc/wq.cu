@@ -91,6 +91,8 @@ __device__ __forceinline__ void decode16x2(const uint32_t (&wd)[BITS == 8 ? 4 : 
     }
 }
 
+// Launched as a programmatic dependent: a warp's first weight loads are issued before the wait for
+// the preceding grids; the activations are read and the outputs written after it.
 // GEMV: 32/T rows per thread block, taken 8 rows at a time; warp w takes the 512-column chunks
 // w, w + 8, ... of K.  A lane keeps two partial sums per (row, token) -- even and odd columns of
 // its 16 -- as one f32 pair (fma.f32x2), adds them at the end of its chunks, and the lanes are
@@ -108,6 +110,8 @@ wq_gemv_kernel(const uint32_t* __restrict__ w, const float* __restrict__ scale, 
     const size_t wpr = static_cast<size_t>(K) * BITS / 32;   // words per row
     const int G = (K + 127) / 128;
     const int nchunks = (K + kChunk - 1) / kChunk;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    bool waited = false;
 
 #pragma unroll
     for (int rb = 0; rb < R; rb += 8) {
@@ -133,6 +137,10 @@ wq_gemv_kernel(const uint32_t* __restrict__ w, const float* __restrict__ scale, 
                         wd[i][0] = a.x; wd[i][1] = a.y;
                         sc[i] = __ldg(scale + static_cast<size_t>(n) * G + k0 / 128);
                     }
+                }
+                if (!waited) {
+                    asm volatile("griddepcontrol.wait;" ::: "memory");   // the preceding grids are done
+                    waited = true;
                 }
                 float2 xv[T][8];
 #pragma unroll
@@ -187,6 +195,7 @@ wq_gemv_kernel(const uint32_t* __restrict__ w, const float* __restrict__ scale, 
         const int idx = lane / (32 / V);          // (row i, token u) = (idx / T, idx % T)
         if (lane % (32 / V) == 0) part[warp][rb * T + idx] = v[0];
     }
+    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");   // warps with no chunk
     __syncthreads();
     for (int e = threadIdx.x; e < R * T; e += blockDim.x) {
         const float tot = __fadd_rn(__fadd_rn(__fadd_rn(part[0][e], part[1][e]), __fadd_rn(part[2][e], part[3][e])),
@@ -294,8 +303,16 @@ template <int BITS, int T>
 cudaError_t launch_gemv(const uint32_t* w, const float* scale, const float* x, float* y, int N, int K, int Tn,
                         cudaStream_t s) {
     constexpr int R = 32 / T;
-    wq_gemv_kernel<BITS, T><<<(N + R - 1) / R, kGvWarps * 32, 0, s>>>(w, scale, x, y, N, K, Tn);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + R - 1) / R);
+    cfg.blockDim = dim3(kGvWarps * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, wq_gemv_kernel<BITS, T>, w, scale, x, y, N, K, Tn);
 }
 
 template <int BITS>
