@@ -15,9 +15,10 @@
 //   warps 2-3   : weight producers -- expand sign bits to +-1 f16 in the same swizzled K-major
 //                 layout (pairs (u, u+16) of a 32-block in one 32-bit word, the order the
 //                 quantizer's MMA operand uses), two rows per thread
-//   warps 4-19  : epilogue -- per 32-block, one tcgen05.ld of the 128x128 f32 block sums (each
-//                 warp its 32 TMEM lanes x 32 columns), p = dx*S, acc = fma(w_s, p, acc) in
-//                 registers; four epilogue warps per SMSP overlap their TMEM load latencies
+//   warps 4-19  : epilogue -- per 32-block, two 16x256b tcgen05.ld of the f32 block sums (each
+//                 warp its 32 TMEM lanes x 32 columns; a thread holds 4 rows x 8 columns, so it
+//                 reads 8 token scales, not 32), p = dx*S, acc = fma(w_s, p, acc) in registers;
+//                 four epilogue warps per SMSP overlap their TMEM load latencies
 // Four smem stages (A 16 KB + B 16 KB each) and four TMEM accumulators of 128 columns, one per
 // 32-block (block b uses accumulator b % 4): each accumulator has its own "sums ready" and
 // "drained" barriers, so the MMAs of block b + 4 start as soon as the epilogue has drained block
@@ -96,11 +97,13 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// 32 lanes x 16 columns of f32 from TMEM into registers (this warp's lane quadrant).
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
+// 16 lanes x 32 columns of f32 from TMEM (16x256b shape, four 8-column repetitions): thread t gets,
+// per repetition r, rows (t / 4) and (t / 4) + 8 of the 16 at columns 8 r + 2 (t % 4) and + 1, as
+// v[4 r .. 4 r + 3] = (row, c), (row, c + 1), (row + 8, c), (row + 8, c + 1).
+__device__ __forceinline__ void tc_ld16x256_x4(uint32_t taddr, float* v) {
     uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
@@ -322,11 +325,19 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
         asm volatile("bar.sync 1, %0;" ::"r"(kNumEWarps * 32) : "memory");
         const int q = warp & 3;                        // TMEM lane quadrant of this warp
         const int h = (warp - kWarpE0) >> 2;           // column quarter
-        const int r = q * 32 + lane;                   // row of the tile = TMEM lane
-        const int n = n0 + r;
-        float acc[kECols];
+        // 16x256b TMEM loads: per 16-lane half and 8-column repetition, thread t holds rows
+        // (t / 4) and (t / 4) + 8 of the half at columns 2 (t % 4) and 2 (t % 4) + 1.  So a
+        // thread's block sums cover 4 rows x 8 columns, it needs only 8 token scales per block
+        // (four 8-byte loads shared by the 8 threads of equal t % 4), and 4 row scales.
+        const int rsub = lane >> 2, csub = 2 * (lane & 3);
+        int rloc[4];                                   // the thread's rows in the tile
 #pragma unroll
-        for (int j = 0; j < kECols; ++j) acc[j] = 0.0f;
+        for (int kk = 0; kk < 4; ++kk) rloc[kk] = q * 32 + 16 * (kk >> 1) + 8 * (kk & 1) + rsub;
+        float2 acc[4][4];                              // [row][repetition]: columns 8 r + csub, + 1
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) acc[kk][rr] = make_float2(0.0f, 0.0f);
         bool ok = true;
         for (int k = 0; k < stages && ok; ++k) {
             // wfull: the stage's row scales are in the ring
@@ -335,44 +346,38 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
                 break;
             }
             const float* wslot = sws + (k % kWSlots) * 2 * BM;
-            const float wb0 = wslot[r], wb1 = wslot[BM + r];
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi) {
                 const int b = 2 * k + bi;
                 const int accx = b % kAccs;
+                float wsr[4];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) wsr[kk] = wslot[bi * BM + rloc[kk]];
+                float2 dxp[4];
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr)
+                    dxp[rr] = *reinterpret_cast<const float2*>(sdx + b * BN + h * kECols + 8 * rr + csub);
                 // bdone: the block's sums are in its accumulator
                 if (!wait_or_abort(&bars->bdone[accx], static_cast<uint32_t>(b / kAccs) & 1u, abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(accx * BN + h * kECols);
-                const float4* dxr = reinterpret_cast<const float4*>(sdx + b * BN + h * kECols);
-                const float wsc = bi ? wb1 : wb0;
-                const float2 w2 = make_float2(wsc, wsc);
-                // two halves of 16 columns: the half's token scales (shared memory) and block sums
-                // (TMEM) are requested together, so their latencies overlap
 #pragma unroll
-                for (int hf = 0; hf < kECols / 16; ++hf) {
-                    float4 dd[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dd[i] = dxr[hf * 4 + i];
+                for (int hf = 0; hf < 2; ++hf) {
+                    const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32 + 16 * hf) << 16) +
+                                           static_cast<uint32_t>(accx * BN + h * kECols);
                     float S[16];
-                    tc_ld16(taddr + 16 * hf, S);
+                    tc_ld16x256_x4(taddr, S);
                     tc_wait_ld();
 #pragma unroll
-                    for (int j4 = 0; j4 < 4; ++j4) {
-                        const int j = hf * 16 + 4 * j4;
+                    for (int rr = 0; rr < 4; ++rr) {
                         // p = dx * S (exact), then acc = fma(w_s, p, acc): two separate IEEE steps per column
-                        const float2 p01 = fmul2(make_float2(dd[j4].x, dd[j4].y), make_float2(S[4 * j4], S[4 * j4 + 1]));
-                        const float2 p23 = fmul2(make_float2(dd[j4].z, dd[j4].w), make_float2(S[4 * j4 + 2], S[4 * j4 + 3]));
-                        const float2 a01 = ffma2(w2, p01, make_float2(acc[j], acc[j + 1]));
-                        const float2 a23 = ffma2(w2, p23, make_float2(acc[j + 2], acc[j + 3]));
-                        acc[j] = a01.x;
-                        acc[j + 1] = a01.y;
-                        acc[j + 2] = a23.x;
-                        acc[j + 3] = a23.y;
+                        const int ka = 2 * hf, kb = 2 * hf + 1;
+                        const float2 pa = fmul2(dxp[rr], make_float2(S[4 * rr], S[4 * rr + 1]));
+                        const float2 pb = fmul2(dxp[rr], make_float2(S[4 * rr + 2], S[4 * rr + 3]));
+                        acc[ka][rr] = ffma2(make_float2(wsr[ka], wsr[ka]), pa, acc[ka][rr]);
+                        acc[kb][rr] = ffma2(make_float2(wsr[kb], wsr[kb]), pb, acc[kb][rr]);
                     }
                 }
                 tc_fence_before();
@@ -380,11 +385,17 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
                 if (lane == 0) mbar_arrive(&bars->tempty[accx]);
             }
         }
-        if (ok && n < N) {
+        if (ok) {
 #pragma unroll
-            for (int j = 0; j < kECols; ++j) {
-                const int m = m0 + h * kECols + j;
-                if (m < M) y[static_cast<size_t>(m) * N + n] = acc[j];
+            for (int kk = 0; kk < 4; ++kk) {
+                const int n = n0 + rloc[kk];
+                if (n >= N) continue;
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int m = m0 + h * kECols + 8 * rr + csub;
+                    if (m < M) y[static_cast<size_t>(m) * N + n] = acc[kk][rr].x;
+                    if (m + 1 < M) y[static_cast<size_t>(m + 1) * N + n] = acc[kk][rr].y;
+                }
             }
         }
     }
