@@ -119,6 +119,21 @@ def recorded_traffic(profile: str, khash: str):
     return rec.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's value (the slowest rank's time); the value itself on one rank."""
+    if not dist:
+        return value
+    import torch
+    tt = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_rate(world: int, bytes_per_step: int, steps: int, seconds: float) -> float:
+    """Weak scaling: every rank moves bytes_per_step per step; the job's rate uses the slowest rank."""
+    return world * bytes_per_step * steps / seconds / 1e9
+
+
 def time_steps(fn, steps, warmup, stream):
     import torch
     for _ in range(warmup):
@@ -453,12 +468,9 @@ def run_ours(args, rank, world, dist):
     clocks.start()
     t = time_steps(group, args.steps, 0, stream)
     clk = clocks.stop()
-    if dist:
-        tt = torch.tensor([t], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(t, dist, dev)
     per_launch = t / args.steps
-    value = world * wbytes * args.steps / t / 1e9
+    value = whole_job_rate(world, wbytes, args.steps, t)
     achieved = (wbytes + abytes + ybytes) / per_launch / 1e9
 
     # --- end to end through the public API with host buffers: activations H2D from pinned memory,
@@ -480,11 +492,8 @@ def run_ours(args, rank, world, dist):
     for _ in range(e2e_steps):
         e2e_step()
     te = time.perf_counter() - t0
-    if dist:
-        tt = torch.tensor([te], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        te = float(tt.item())
-    e2e_value = world * wbytes * e2e_steps / te / 1e9
+    te = max_over_ranks(te, dist, dev)
+    e2e_value = whole_job_rate(world, wbytes, e2e_steps, te)
 
     khash = kernel_hash("q1.cu", "gq_internal.cuh")
     line = {
