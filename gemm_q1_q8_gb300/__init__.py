@@ -19,7 +19,7 @@ __all__ = [
     "q1_0_packed_bytes", "q1_0_pack", "q1_q8_gemv", "q1_q8_gemv_f32", "q1_q8_gemv_noalloc", "GroupedGemv",
     "q1_q8_gemm", "ACT_Q8_0", "ACT_F32",
     "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm", "q1s32_f32_gemm",
-    "matvec_q8", "matmul_q8", "matvec_q4g128", "matmul_q4g128",
+    "matvec_q8", "matmul_q8", "matmul_q8_mma", "wq_mma_workspace_bytes", "matvec_q4g128", "matmul_q4g128",
     "device_error", "version",
 ]
 
@@ -64,6 +64,8 @@ def lib():
             "q1s32_f32_gemm": (I, [P, P, P, P, I, I, I, I, P]),
             "matvec_q8": (I, [P, P, P, P, I, I, P]),
             "matmul_q8": (I, [P, P, P, P, I, I, I, P]),
+            "gq_wq_mma_workspace_bytes": (S, [I, I]),
+            "matmul_q8_mma": (I, [P, P, P, P, I, I, I, P, P]),
             "matvec_q4g128": (I, [P, P, P, P, I, I, P]),
             "matmul_q4g128": (I, [P, P, P, P, I, I, I, P]),
             "q1_q8_gemv_grouped": (I, [P, I, I, P, P]),
@@ -260,6 +262,36 @@ def matvec_q8(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.
 def matmul_q8(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None):
     """W8A32 GEMM: w [N, K/4] int32, scale [N] f32, x [T, K] f32 -> y [T, N] f32."""
     return _wq(8, w, scale, x, out, "matmul_q8")
+
+
+def wq_mma_workspace_bytes(T: int, K: int) -> int:
+    """Bytes of the workspace matmul_q8_mma needs for T tokens of K columns (3 * T * K bf16)."""
+    return lib().gq_wq_mma_workspace_bytes(T, K)
+
+
+def matmul_q8_mma(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None):
+    """matmul_q8 on the tensor cores (x split exactly into three bf16 planes): w [N, K/4] int32,
+    scale [N] f32, x [T, K] f32 -> y [T, N] f32.  workspace: a uint8 CUDA tensor of at least
+    wq_mma_workspace_bytes(T, K) bytes (allocated here when None)."""
+    N = w.shape[0]
+    T, K = x.shape
+    _need(w, torch.int32, N * K // 4, "w")
+    _need(scale, torch.float32, N, "scale")
+    _need(x, torch.float32, T * K, "x")
+    y = torch.empty((T, N), dtype=torch.float32, device=x.device) if out is None else out
+    _need(y, torch.float32, T * N, "out")
+    need = wq_mma_workspace_bytes(T, K)
+    if need == 0:
+        raise GQError("matmul_q8_mma: invalid shape")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _need(workspace, torch.uint8, workspace.numel(), "workspace")
+    if workspace.numel() < need:
+        raise GQError(f"matmul_q8_mma: workspace holds {workspace.numel()} bytes, needs {need}")
+    _check(lib().matmul_q8_mma(_ptr(w), _ptr(scale), _ptr(x), _ptr(y), T, N, K, _ptr(workspace), _stream()),
+           "matmul_q8_mma")
+    return y
 
 
 def matvec_q4g128(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None):

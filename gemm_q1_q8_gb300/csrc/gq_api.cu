@@ -4,6 +4,7 @@
 #include <cstdint>
 
 #include "gq_internal.cuh"
+#include "wq_mma.cuh"
 
 namespace {
 
@@ -52,7 +53,8 @@ int gq_last_cuda_error(void) { return t_last_cuda_error; }
 int gq_device_error(void) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_status(e) == GQ_OK ? 0 : -1;
-    const unsigned v = gq::error_read_clear_q1() | gq::error_read_clear_ternary() | gq::error_read_clear_prefill_mma();
+    const unsigned v = gq::error_read_clear_q1() | gq::error_read_clear_ternary() | gq::error_read_clear_prefill_mma() |
+                       gq::error_read_clear_wq_mma();
     return v == ~0u ? -1 : static_cast<int>(v);
 }
 
@@ -165,6 +167,21 @@ int matmul_q8(const uint32_t* w, const float* scale, const float* x, float* y, i
               gq_stream_t stream) {
     return wq_call(8, w, scale, x, y, T, N, K, stream);
 }
+size_t gq_wq_mma_workspace_bytes(int T, int K) {
+    if (T < 1 || T > 65535 * 128 || K < 64 || K % 32 != 0 || K > kMaxK) return 0;
+    return gq::wq_mma_workspace_bytes(T, K);
+}
+
+int matmul_q8_mma(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+                  void* workspace, gq_stream_t stream) {
+    if (N < 1 || T < 1 || T > 65535 * 128 || K < 64 || K % 32 != 0 || K > kMaxK) return GQ_EINVAL_SHAPE;
+    if (!w || !scale || !x || !y || !workspace) return GQ_EINVAL_PTR;
+    if (!aligned(w, 16) || !aligned(scale, 4) || !aligned(x, 16) || !aligned(y, 4) || !aligned(workspace, 16))
+        return GQ_EINVAL_PTR;
+    return cuda_status(
+        gq::launch_wq8_mma(w, scale, x, y, T, N, K, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int matvec_q4g128(const uint32_t* w, const float* scale, const float* x, float* y, int N, int K, gq_stream_t stream) {
     return wq_call(4, w, scale, x, y, 1, N, K, stream);
 }

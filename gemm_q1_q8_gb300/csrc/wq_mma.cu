@@ -1,0 +1,358 @@
+// W8A32 matmul on the 5th-generation tensor cores (web-xpu-ops README: matmulQ8 -- int8 weights
+// [N, K] with one f32 scale per row, f32 activations [T, K]):  y[t, n] = scale[n] * sum_k q[n, k] x[t, k].
+//
+// The activations are f32, the tensor cores take bf16: each x is split exactly into three bf16
+// parts, hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid) (round to nearest each time; the
+// two subtractions are exact), so hi + mid + lo = x for every normal x.  The int8 codes are exact in
+// bf16.  Every product code * part is exact in the tensor core.  The three parts of one 64-column
+// stage accumulate into a TMEM accumulator of their own (12 MMA steps); the epilogue adds the stage
+// partials in stage order in f32 with round to nearest, and multiplies by the row scale at the end.
+// (The tensor core's own f32 accumulation is not round-to-nearest: letting one accumulator run over
+// all of K gave a one-signed error that grew with K.)
+//
+// Thread block (one per SM): 128 weight rows x 128 tokens, K in stages of 64.
+//   warp 0      : TMA producer of the three bf16 planes of the activation tile (128B swizzle)
+//   warp 1      : TMEM allocator and MMA issuer (one elected thread): 3 planes x 4 K16 steps per
+//                 stage into accumulator (stage % 4)
+//   warps 2-5   : weight producers, one row per thread: the row's 64 codes of the stage become bf16
+//                 in the swizzled K-major layout the MMA reads
+//   warps 6-13  : epilogue: after every stage, tcgen05.ld of its accumulator (a warp holds 32 rows x
+//                 64 tokens) added into registers; at the end y = scale * sum
+// Three smem stages (A 16 KB + B 3 x 16 KB), four TMEM accumulators (512 columns).  Every wait is
+// bounded (~1 s); a role that gives up raises an abort flag the others honour, and the block drains
+// its copies and MMAs and frees TMEM before it exits.
+#include "gq_internal.cuh"
+#include "wq_mma.cuh"
+
+#include <cuda_bf16.h>
+
+namespace gq {
+GQ_ERROR_ACCESSOR(wq_mma)
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int kStages = 3;
+constexpr int kPlanes = 3;
+constexpr int kTileA = BM * BK * 2;               // 16 KB
+constexpr int kTileB = BN * BK * 2;               // 16 KB per plane
+constexpr int kAccs = 4;                          // TMEM accumulators of BN columns, stage k -> k % kAccs
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpP0 = 2, kNumPWarps = 4, kWarpE0 = 6, kNumEWarps = 8;
+constexpr int kThreads = (kWarpE0 + kNumEWarps) * 32;    // 448
+constexpr int kTmemCols = kAccs * BN;                    // 512
+
+// instruction descriptor: D f32, A/B bf16, both K-major, N = 128, M = 128
+constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                (static_cast<uint32_t>(BM >> 4) << 24);
+
+struct Bars {
+    uint64_t fullA[kStages], fullB[kStages], done[kStages];
+    uint64_t accfull[kAccs], accempty[kAccs];
+    uint64_t final_;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ uint64_t smem_desc(const void* p) {   // 128B swizzle, K-major, 8-row groups 1 KB apart
+    const uint64_t addr = smem_u32(p);
+    uint64_t d = 0;
+    d |= (addr >> 4) & 0x3FFFull;
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(kIdescBf16), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {    // 32 lanes x 32 columns
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > 1000000000ull) {
+            report_error(kErrMmaTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// Four int8 codes (a word) as two words of bf16 pairs (codes 0,1 and 2,3), exactly.
+__device__ __forceinline__ uint2 codes_to_bf16x4(uint32_t w) {
+    const uint32_t b = w ^ 0x80808080u;
+    const float2 bias = make_float2(8388736.0f, 8388736.0f);            // 2^23 + 128
+    const float2 lo = fadd2(make_float2(__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7440)),
+                                        __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7441))),
+                            make_float2(-bias.x, -bias.y));
+    const float2 hi = fadd2(make_float2(__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7442)),
+                                        __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7443))),
+                            make_float2(-bias.x, -bias.y));
+    // |code| <= 128 has at most 8 significant bits: the upper half of its f32 is its bf16
+    return make_uint2(__byte_perm(__float_as_uint(lo.x), __float_as_uint(lo.y), 0x7632),
+                      __byte_perm(__float_as_uint(hi.x), __float_as_uint(hi.y), 0x7632));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+wq8_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restrict__ w, const float* __restrict__ scale,
+               float* __restrict__ y, int T, int N, int K) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = base;                                      // [kStages][kTileA]
+    uint8_t* sB = base + kStages * kTileA;                   // [kStages][kPlanes][kTileB]
+    Bars* bars = reinterpret_cast<Bars*>(sB + kStages * kPlanes * kTileB);
+    volatile int* abort = &bars->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BM, t0 = blockIdx.y * BN;
+    const int stages = (K + BK - 1) / BK;     // the activation tile past K is zero-filled by the copy
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->fullA[s], kNumPWarps);
+            mbar_init(&bars->fullB[s], 1);
+            mbar_init(&bars->done[s], 1);
+        }
+        for (int a = 0; a < kAccs; ++a) {
+            mbar_init(&bars->accfull[a], 1);
+            mbar_init(&bars->accempty[a], kNumEWarps);
+        }
+        mbar_init(&bars->final_, 1);
+        bars->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars->tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    int tma_issued = 0;
+    if (warp == kWarpTma) {
+        if (lane == 0) {
+            prefetch_tmap(&tmB);
+            for (int k = 0; k < stages; ++k) {
+                const int s = k % kStages;
+                if (k >= kStages &&
+                    !wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStages - 1) & 1u, abort))
+                    break;
+                mbar_arrive_expect_tx(&bars->fullB[s], kPlanes * kTileB);
+                for (int p = 0; p < kPlanes; ++p)
+                    tma_load_2d(sB + (s * kPlanes + p) * kTileB, &tmB, k * BK, p * T + t0, &bars->fullB[s]);
+                ++tma_issued;
+            }
+        }
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            for (int k = 0; k < stages && !*abort; ++k) {
+                const int s = k % kStages;
+                const int a = k % kAccs;
+                const uint32_t ph = static_cast<uint32_t>(k / kStages) & 1u;
+                if (!wait_or_abort(&bars->fullA[s], ph, abort) || !wait_or_abort(&bars->fullB[s], ph, abort)) break;
+                if (k >= kAccs &&
+                    !wait_or_abort(&bars->accempty[a], static_cast<uint32_t>(k / kAccs - 1) & 1u, abort))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(a * BN);
+#pragma unroll
+                for (int p = 0; p < kPlanes; ++p)
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)
+                        tc_mma(d, smem_desc(sA + s * kTileA + j * 32), smem_desc(sB + (s * kPlanes + p) * kTileB + j * 32),
+                               (p > 0 || j > 0) ? 1u : 0u);
+                tc_commit(&bars->done[s]);
+                tc_commit(&bars->accfull[a]);
+            }
+            tc_commit(&bars->final_);
+        }
+    } else if (warp < kWarpE0) {
+        // ---------------- weight producers: row r's 64 codes of the stage as bf16, two stages ahead
+        const int r = threadIdx.x - kWarpP0 * 32;               // 0..127
+        const int n = min(n0 + r, N - 1);                       // past-the-end rows: produced, not stored
+        const int chunks = K / 16;                              // 16 codes per uint4; a K % 64 == 32 tail reads zeros
+        const uint4* row = reinterpret_cast<const uint4*>(w) + static_cast<size_t>(n) * chunks;
+        uint4 pf[2][4];
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pf[a][i] = (4 * a + i < chunks) ? __ldg(row + 4 * a + i) : make_uint4(0u, 0u, 0u, 0u);
+        uint8_t* trow = sA + (r >> 3) * 1024 + (r & 7) * 128;
+        bool live = true;
+        for (int k0 = 0; k0 < stages && live; k0 += 2) {
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                const int k = k0 + kk;
+                if (k >= stages) break;
+                const int s = k % kStages;
+                if (k >= kStages &&
+                    !wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStages - 1) & 1u, abort)) {
+                    live = false;
+                    break;
+                }
+                uint4 cw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    cw[i] = pf[kk][i];
+                    pf[kk][i] = (4 * (k + 2) + i < chunks) ? __ldg(row + 4 * (k + 2) + i) : make_uint4(0u, 0u, 0u, 0u);
+                }
+                uint8_t* tileA = trow + s * kTileA;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {          // 16 codes -> two 16-byte chunks of 8 bf16
+                    const uint2 a0 = codes_to_bf16x4(cw[i].x), a1 = codes_to_bf16x4(cw[i].y);
+                    const uint2 a2 = codes_to_bf16x4(cw[i].z), a3 = codes_to_bf16x4(cw[i].w);
+                    const int c0 = 2 * i, c1 = 2 * i + 1;
+                    *reinterpret_cast<uint4*>(tileA + ((c0 ^ (r & 7)) << 4)) = make_uint4(a0.x, a0.y, a1.x, a1.y);
+                    *reinterpret_cast<uint4*>(tileA + ((c1 ^ (r & 7)) << 4)) = make_uint4(a2.x, a2.y, a3.x, a3.y);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->fullA[s]);
+            }
+        }
+    } else {
+        // ---------------- epilogue: y = scale * (sum over stages of the stage partials)
+        const int q = warp & 3;                                  // TMEM lanes 32q..32q+31
+        const int h = (warp - kWarpE0) / 4;                      // tokens 64h..64h+63 of the tile
+        const int r = q * 32 + lane;
+        const int n = n0 + r;
+        float acc[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+        bool ok = true;
+        for (int k = 0; k < stages; ++k) {
+            const int a = k % kAccs;
+            if (!wait_or_abort(&bars->accfull[a], static_cast<uint32_t>(k / kAccs) & 1u, abort) || *abort) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v[32];
+                tc_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BN + h * 64 + c * 32), v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[c * 32 + i] = __fadd_rn(acc[c * 32 + i], v[i]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->accempty[a]);
+        }
+        if (ok && n < N) {
+            const float sc = __ldg(scale + n);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const int t = t0 + h * 64 + i;
+                if (t < T) y[static_cast<size_t>(t) * N + n] = __fmul_rn(sc, acc[i]);
+            }
+        }
+    }
+
+    // ---------------- teardown
+    __syncwarp();
+    if (warp == kWarpMma) {
+        // every MMA issued has completed before TMEM is freed
+        if (lane == 0 && !mbar_wait(&bars->final_, 0)) report_error(kErrMmaTimeout);
+        __syncwarp();
+    }
+    if (warp == kWarpTma && lane == 0) {
+        const int first = tma_issued > kStages ? tma_issued - kStages : 0;
+        for (int k = first; k < tma_issued; ++k)
+            if (!mbar_wait(&bars->fullB[k % kStages], static_cast<uint32_t>(k / kStages) & 1u))
+                report_error(kErrDrainTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// x [T, K] f32 -> planes [3][T][K] bf16: hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid).
+__global__ void split_planes_kernel(const float4* __restrict__ x, uint2* __restrict__ planes, size_t quads) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < quads;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const float4 v = x[i];
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+        uint32_t h[4], m[4], l[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat16 bh = __float2bfloat16_rn(vv[j]);
+            const float r1 = __fsub_rn(vv[j], __bfloat162float(bh));
+            const __nv_bfloat16 bm = __float2bfloat16_rn(r1);
+            const float r2 = __fsub_rn(r1, __bfloat162float(bm));
+            const __nv_bfloat16 bl = __float2bfloat16_rn(r2);
+            h[j] = __bfloat16_as_ushort(bh);
+            m[j] = __bfloat16_as_ushort(bm);
+            l[j] = __bfloat16_as_ushort(bl);
+        }
+        planes[i] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        planes[quads + i] = make_uint2(m[0] | (m[1] << 16), m[2] | (m[3] << 16));
+        planes[2 * quads + i] = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+    }
+}
+
+}  // namespace
+
+size_t wq_mma_workspace_bytes(int T, int K) { return static_cast<size_t>(kPlanes) * T * K * 2; }
+
+cudaError_t launch_wq8_mma(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+                           void* workspace, cudaStream_t s) {
+    const size_t quads = static_cast<size_t>(T) * K / 4;
+    split_planes_kernel<<<static_cast<unsigned>(std::min<size_t>((quads + 255) / 256, 4096)), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(x), static_cast<uint2*>(workspace), quads);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmB;
+    if (!make_tmap_2d(&tmB, workspace, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(K),
+                      static_cast<uint64_t>(kPlanes) * T, static_cast<uint64_t>(K) * 2, BK, BN, true))
+        return cudaErrorInvalidValue;
+    const size_t smem = 1024 + static_cast<size_t>(kStages) * (kTileA + kPlanes * kTileB) + sizeof(Bars);
+    static int configured_dev = -1;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (configured_dev != dev) {
+        e = cudaFuncSetAttribute(wq8_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    const dim3 grid((N + BM - 1) / BM, (T + BN - 1) / BN);
+    wq8_mma_kernel<<<grid, kThreads, smem, s>>>(tmB, w, scale, y, T, N, K);
+    return cudaGetLastError();
+}
+
+}  // namespace gq

@@ -30,30 +30,38 @@ def _terms(bits, w, scale, x, N, K):
     return np.abs(x.astype(np.float64)) @ (np.abs(codes) * sc).T
 
 
-def _depth(bits, T, K):
+def _depth(bits, T, K, mma=False):
     """Roundings a term passes through in the kernel's order.
     T <= 4 (GEMV): 8 bits -- an fma chain over the lane's 16 columns of each of its warp's 512-column
     chunks, a 5-level lane butterfly, a 3-level warp tree, the row-scale multiply; 4 bits -- a
     16-term chain per chunk, one fma with the group scale per chunk, the butterfly and tree.
     T > 4 (GEMM): one fma per column, plus the scale multiply (8 bits) or the dequantizing product
-    code * scale (4 bits)."""
+    code * scale (4 bits).
+    Tensor cores (matmul_q8_mma): per 64-column stage, 12 MMA steps (three planes x 4 K16 steps)
+    into a fresh accumulator -- the hardware's accumulation rounding is not published, so each step
+    is allowed two units -- then a round-to-nearest f32 add of each stage partial in stage order
+    (ceil(K/64)), the scale multiply, and 7 units of slack for the sums inside a step."""
+    if mma:
+        return -(-K // 64) + 2 * 12 + 8
     if T <= 4:
         return 16 * -(-K // 4096) + 10 if bits == 8 else 28 + -(-K // 512)
     return K + 2
 
 
-def _check(bits, y, want, w, scale, x, T, N, K):
+def _check(bits, y, want, w, scale, x, T, N, K, mma=False):
     terms = _terms(bits, w, scale, x, N, K)
     err = np.abs(y.astype(np.float64) - want)
-    bound = _depth(bits, T, K) * 2.0 ** -24 * terms
+    bound = _depth(bits, T, K, mma) * 2.0 ** -24 * terms
     assert np.all(err <= bound), f"max err/bound {np.max(err / np.maximum(bound, 1e-300))}"
     big = np.abs(want) > 1e-2 * terms
     assert np.all(err[big] <= 1e-4 * np.abs(want[big]) + 1e-6)
 
 
-def _run(gq, bits, w, scale, x):
+def _run(gq, bits, w, scale, x, mma=False):
     T = x.shape[0]
     args = (to_dev(w.view(np.int32)), to_dev(scale), to_dev(x))
+    if mma:
+        return gq.matmul_q8_mma(*args).cpu().numpy()
     if bits == 8:
         y = gq.matvec_q8(*args) if T == 1 else gq.matmul_q8(*args)
     else:
@@ -114,3 +122,62 @@ def test_matmul_full_size_sampled(gq, bits):
     ts = np.unique(np.concatenate([np.arange(0, T, 41), [63, 64, 127, 128, T - 1]]))
     want = _oracle(bits, w[ns], scale[ns], x[ts], ts.size, ns.size, K)
     _check(bits, y[np.ix_(ts, ns)], want, w[ns], scale[ns], x[ts], T, ns.size, K)
+
+
+# ---- the tensor-core W8A32 matmul -------------------------------------------------------------
+
+@pytest.mark.parametrize("T,N,K", [(1, 1, 64), (5, 257, 96), (33, 130, 1056), (128, 128, 64), (129, 129, 4128),
+                                   (130, 300, 512), (300, 1000, 2048), (7, 3000, 16384)])
+def test_mma_within_bound(gq, T, N, K):
+    """Ragged tokens and rows across the 128 x 128 tile, K % 64 == 32 tails, one to many K stages."""
+    w, scale, x = wl.wq_inputs(wl.Rng(7000 + T + N + K), T, K, N, 8, p_m8=0.02)
+    _check(8, _run(gq, 8, w, scale, x, mma=True), _oracle(8, w, scale, x, T, N, K), w, scale, x, T, N, K, mma=True)
+
+
+@pytest.mark.parametrize("T", [1, 9, 200])
+def test_mma_exact_special_case(gq, T):
+    """Integer x in [-8, 8] and power-of-two scales: the bf16 split is x itself and every partial
+    sum is exact, so the tensor cores give the oracle's value bit for bit."""
+    N, K = 300, 1024
+    rng = wl.Rng(80 + T)
+    w, scale, _ = wl.wq_inputs(rng, T, K, N, 8, p_m8=0.05)
+    scale = (2.0 ** -(1 + (rng.u32(scale.size) % 6).astype(np.int64))).astype(np.float32).reshape(scale.shape)
+    x = ((rng.u32(T * K) % 17).astype(np.int64) - 8).astype(np.float32).reshape(T, K)
+    assert np.array_equal(_run(gq, 8, w, scale, x, mma=True).astype(np.float64), _oracle(8, w, scale, x, T, N, K))
+
+
+def test_mma_split_is_exact(gq):
+    """One nonzero code per row selects single activations: y = scale * code * x exactly, so the
+    three bf16 planes must sum back to every x (normal range, all exponents of N(0,1) data)."""
+    T, N, K = 140, 256, 256
+    rng = wl.Rng(91)
+    x = rng.normal(T * K).astype(np.float32).reshape(T, K)
+    codes = np.zeros((N, K), np.int8)
+    codes[np.arange(N), np.arange(N) % K] = 1
+    w = codes.view(np.uint32).reshape(N, K // 4)
+    scale = np.ones(N, np.float32)
+    y = _run(gq, 8, w, scale, x, mma=True)
+    assert np.array_equal(y, x[:, np.arange(N) % K])
+
+
+def test_mma_deterministic_and_workspace(gq):
+    import torch
+    T, N, K = 260, 700, 2048
+    w, scale, x = wl.wq_inputs(wl.Rng(17), T, K, N, 8)
+    dw, ds, dx = to_dev(w.view(np.int32)), to_dev(scale), to_dev(x)
+    ws = torch.full((gq.wq_mma_workspace_bytes(T, K) + 64,), 0x7F, dtype=torch.uint8, device="cuda")
+    a = gq.matmul_q8_mma(dw, ds, dx, workspace=ws).cpu().numpy()
+    b = gq.matmul_q8_mma(dw, ds, dx).cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert gq.device_error() == 0
+
+
+def test_mma_full_size_sampled(gq):
+    """512 tokens x 14336 rows x 4096 on the tensor cores: sampled rows and tokens against the oracle."""
+    T, N, K = 512, 14336, 4096
+    w, scale, x = wl.wq_inputs(wl.Rng(6), T, K, N, 8)
+    y = _run(gq, 8, w, scale, x, mma=True)
+    ns = np.unique(np.concatenate([np.arange(0, N, 911), [127, 128, N - 1]]))
+    ts = np.unique(np.concatenate([np.arange(0, T, 41), [63, 64, 127, 128, T - 1]]))
+    want = _oracle(8, w[ns], scale[ns], x[ts], ts.size, ns.size, K)
+    _check(8, y[np.ix_(ts, ns)], want, w[ns], scale[ns], x[ts], T, ns.size, K, mma=True)
