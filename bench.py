@@ -315,13 +315,12 @@ def bench_wq(gq, torch, dev, hbm_peak, steps=40, warmup=5):
         tm = time_steps(lambda: mm(copies[0][0], copies[0][1], xp, out=yp), 5, 2, stream) / 5
         res["matmul512_us"] = round(tm * 1e6, 1)
         res["matmul512_TFLOPs"] = round(2.0 * T * N * K / tm / 1e12, 2)
-        if bits == 8:
-            ws = torch.empty(gq.wq_mma_workspace_bytes(T, K), dtype=torch.uint8, device=dev)
-            tmc = time_steps(lambda: gq.matmul_q8_mma(copies[0][0], copies[0][1], xp, out=yp, workspace=ws),
-                             10, 3, stream) / 10
-            res["matmul512_mma_us"] = round(tmc * 1e6, 1)
-            res["matmul512_mma_TFLOPs"] = round(2.0 * T * N * K / tmc / 1e12, 2)
-            res["matmul512_mma_bf16_TFLOPs"] = round(3 * 2.0 * T * N * K / tmc / 1e12, 2)
+        mmc = gq.matmul_q8_mma if bits == 8 else gq.matmul_q4g128_mma
+        ws = torch.empty(gq.wq_mma_workspace_bytes(T, K), dtype=torch.uint8, device=dev)
+        tmc = time_steps(lambda: mmc(copies[0][0], copies[0][1], xp, out=yp, workspace=ws), 10, 3, stream) / 10
+        res["matmul512_mma_us"] = round(tmc * 1e6, 1)
+        res["matmul512_mma_TFLOPs"] = round(2.0 * T * N * K / tmc / 1e12, 2)
+        res["matmul512_mma_bf16_TFLOPs"] = round(3 * 2.0 * T * N * K / tmc / 1e12, 2)
         out[f"w{bits}a32_{name}_14336x4096"] = res
         del copies
     return out
@@ -418,8 +417,8 @@ def run_only(args):
     print(json.dumps({"only": args.only, "kernels": res}), flush=True)
 
 
-PROBES = ("lut4_decode", "lut4_prefill", "wq8_gemv", "wq4_gemv", "wq8_gemm", "wq4_gemm", "wq8_mma", "bq8_m1",
-          "bq8_m4")
+PROBES = ("lut4_decode", "lut4_prefill", "wq8_gemv", "wq4_gemv", "wq8_gemm", "wq4_gemm", "wq8_mma", "wq4_mma",
+          "bq8_m1", "bq8_m4")
 
 
 def run_probe(name):
@@ -440,12 +439,12 @@ def run_probe(name):
         f = lambda: gq.q1s32_f32_gemm(s, w, x, path=gq.PATH_LUT4)
     else:
         bits = 8 if name.startswith("wq8") else 4
-        T = 1 if name.endswith("gemv") else 512     # wq8_mma: the tensor-core matmul at 512 tokens
+        T = 1 if name.endswith("gemv") else 512     # wq*_mma: the tensor-core matmuls at 512 tokens
         w, sc, x = wl.wq_inputs(wl.Rng(90), T, K, N, bits)
         w, sc, x = (torch.from_numpy(a).cuda() for a in (w.view(np.int32), sc, x))
         fn = {(8, 1): gq.matvec_q8, (8, 512): gq.matmul_q8, (4, 1): gq.matvec_q4g128, (4, 512): gq.matmul_q4g128}
-        if name == "wq8_mma":
-            f = lambda: gq.matmul_q8_mma(w, sc, x)
+        if name.endswith("_mma"):
+            f = lambda: (gq.matmul_q8_mma if bits == 8 else gq.matmul_q4g128_mma)(w, sc, x)
         else:
             f = lambda: fn[(bits, T)](w, sc, x)
     for _ in range(3):

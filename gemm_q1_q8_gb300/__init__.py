@@ -20,6 +20,7 @@ __all__ = [
     "q1_q8_gemm", "ACT_Q8_0", "ACT_F32",
     "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm", "q1s32_f32_gemm",
     "matvec_q8", "matmul_q8", "matmul_q8_mma", "wq_mma_workspace_bytes", "matvec_q4g128", "matmul_q4g128",
+    "matmul_q4g128_mma",
     "device_error", "version",
 ]
 
@@ -66,6 +67,7 @@ def lib():
             "matmul_q8": (I, [P, P, P, P, I, I, I, P]),
             "gq_wq_mma_workspace_bytes": (S, [I, I]),
             "matmul_q8_mma": (I, [P, P, P, P, I, I, I, P, P]),
+            "matmul_q4g128_mma": (I, [P, P, P, P, I, I, I, P, P]),
             "matvec_q4g128": (I, [P, P, P, P, I, I, P]),
             "matmul_q4g128": (I, [P, P, P, P, I, I, I, P]),
             "q1_q8_gemv_grouped": (I, [P, I, I, P, P]),
@@ -269,29 +271,39 @@ def wq_mma_workspace_bytes(T: int, K: int) -> int:
     return lib().gq_wq_mma_workspace_bytes(T, K)
 
 
-def matmul_q8_mma(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
-                  workspace: torch.Tensor | None = None):
-    """matmul_q8 on the tensor cores (x split exactly into three bf16 planes): w [N, K/4] int32,
-    scale [N] f32, x [T, K] f32 -> y [T, N] f32.  workspace: a uint8 CUDA tensor of at least
-    wq_mma_workspace_bytes(T, K) bytes (allocated here when None)."""
+def _wq_mma(bits: int, w, scale, x, out, workspace, name: str):
     N = w.shape[0]
     T, K = x.shape
-    _need(w, torch.int32, N * K // 4, "w")
-    _need(scale, torch.float32, N, "scale")
+    _need(w, torch.int32, N * K * bits // 32, "w")
+    _need(scale, torch.float32, N if bits == 8 else N * ((K + 127) // 128), "scale")
     _need(x, torch.float32, T * K, "x")
     y = torch.empty((T, N), dtype=torch.float32, device=x.device) if out is None else out
     _need(y, torch.float32, T * N, "out")
     need = wq_mma_workspace_bytes(T, K)
     if need == 0:
-        raise GQError("matmul_q8_mma: invalid shape")
+        raise GQError(f"{name}: invalid shape")
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     _need(workspace, torch.uint8, workspace.numel(), "workspace")
     if workspace.numel() < need:
-        raise GQError(f"matmul_q8_mma: workspace holds {workspace.numel()} bytes, needs {need}")
-    _check(lib().matmul_q8_mma(_ptr(w), _ptr(scale), _ptr(x), _ptr(y), T, N, K, _ptr(workspace), _stream()),
-           "matmul_q8_mma")
+        raise GQError(f"{name}: workspace holds {workspace.numel()} bytes, needs {need}")
+    _check(getattr(lib(), name)(_ptr(w), _ptr(scale), _ptr(x), _ptr(y), T, N, K, _ptr(workspace), _stream()), name)
     return y
+
+
+def matmul_q8_mma(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None):
+    """matmul_q8 on the tensor cores (x split exactly into three bf16 planes): w [N, K/4] int32,
+    scale [N] f32, x [T, K] f32 -> y [T, N] f32.  workspace: a uint8 CUDA tensor of at least
+    wq_mma_workspace_bytes(T, K) bytes (allocated here when None)."""
+    return _wq_mma(8, w, scale, x, out, workspace, "matmul_q8_mma")
+
+
+def matmul_q4g128_mma(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None):
+    """matmul_q4g128 on the tensor cores: w [N, K/8] int32, scale [N, ceil(K/128)] f32, x [T, K] f32
+    -> y [T, N] f32; workspace as matmul_q8_mma."""
+    return _wq_mma(4, w, scale, x, out, workspace, "matmul_q4g128_mma")
 
 
 def matvec_q4g128(w: torch.Tensor, scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None):

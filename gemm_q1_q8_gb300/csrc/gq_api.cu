@@ -172,14 +172,23 @@ size_t gq_wq_mma_workspace_bytes(int T, int K) {
     return gq::wq_mma_workspace_bytes(T, K);
 }
 
-int matmul_q8_mma(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
-                  void* workspace, gq_stream_t stream) {
+static int wq_mma_call(int bits, const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+                       void* workspace, gq_stream_t stream) {
     if (N < 1 || T < 1 || T > 65535 * 128 || K < 64 || K % 32 != 0 || K > kMaxK) return GQ_EINVAL_SHAPE;
     if (!w || !scale || !x || !y || !workspace) return GQ_EINVAL_PTR;
     if (!aligned(w, 16) || !aligned(scale, 4) || !aligned(x, 16) || !aligned(y, 4) || !aligned(workspace, 16))
         return GQ_EINVAL_PTR;
     return cuda_status(
-        gq::launch_wq8_mma(w, scale, x, y, T, N, K, workspace, reinterpret_cast<cudaStream_t>(stream)));
+        gq::launch_wq_mma(bits, w, scale, x, y, T, N, K, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int matmul_q8_mma(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+                  void* workspace, gq_stream_t stream) {
+    return wq_mma_call(8, w, scale, x, y, T, N, K, workspace, stream);
+}
+int matmul_q4g128_mma(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
+                      void* workspace, gq_stream_t stream) {
+    return wq_mma_call(4, w, scale, x, y, T, N, K, workspace, stream);
 }
 
 int matvec_q4g128(const uint32_t* w, const float* scale, const float* x, float* y, int N, int K, gq_stream_t stream) {

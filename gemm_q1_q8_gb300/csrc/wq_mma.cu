@@ -1,12 +1,17 @@
-// W8A32 matmul on the 5th-generation tensor cores (web-xpu-ops README: matmulQ8 -- int8 weights
-// [N, K] with one f32 scale per row, f32 activations [T, K]):  y[t, n] = scale[n] * sum_k q[n, k] x[t, k].
+// W8A32 and W4A32 group-128 matmuls on the 5th-generation tensor cores (web-xpu-ops README:
+// matmulQ8 -- int8 weights [N, K] with one f32 scale per row; matmulQ4G128 -- 4-bit weights with one
+// f32 scale per 128 columns; f32 activations [T, K]):
+//   8 bits: y[t, n] = scale[n] * sum_k q[n, k] x[t, k]
+//   4 bits: y[t, n] = sum_g scale[n, g] * sum_{k in g} q[n, k] x[t, k]
 //
 // The activations are f32, the tensor cores take bf16: each x is split exactly into three bf16
 // parts, hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid) (round to nearest each time; the
 // two subtractions are exact), so hi + mid + lo = x for every normal x.  The int8 codes are exact in
 // bf16.  Every product code * part is exact in the tensor core.  The three parts of one 64-column
 // stage accumulate into a TMEM accumulator of their own (12 MMA steps); the epilogue adds the stage
-// partials in stage order in f32 with round to nearest, and multiplies by the row scale at the end.
+// partials in stage order in f32 with round to nearest, and multiplies by the row scale at the end
+// (8 bits), or folds each partial in with one fma by its group's scale (4 bits: a 64-column stage
+// lies inside one 128-column group).
 // (The tensor core's own f32 accumulation is not round-to-nearest: letting one accumulator run over
 // all of K gave a one-signed error that grew with K.)
 //
@@ -124,9 +129,29 @@ __device__ __forceinline__ uint2 codes_to_bf16x4(uint32_t w) {
                       __byte_perm(__float_as_uint(hi.x), __float_as_uint(hi.y), 0x7632));
 }
 
+// Eight 4-bit two's-complement codes (a word, nibble 0 first) as four words of bf16 pairs, exactly.
+__device__ __forceinline__ uint4 nibbles_to_bf16x8(uint32_t w) {
+    const uint32_t b = w ^ 0x88888888u;                  // code + 8 in every nibble
+    const uint32_t ev = b & 0x0F0F0F0Fu;                 // codes 0, 2, 4, 6 as bytes
+    const uint32_t od = (b >> 4) & 0x0F0F0F0Fu;          // codes 1, 3, 5, 7
+    const float2 bias = make_float2(-8388616.0f, -8388616.0f);       // -(2^23 + 8)
+    uint32_t out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t sel = 0x7440u + static_cast<uint32_t>(j);
+        const float2 f = fadd2(make_float2(__uint_as_float(__byte_perm(ev, 0x4B000000u, sel)),
+                                           __uint_as_float(__byte_perm(od, 0x4B000000u, sel))),
+                               bias);
+        out[j] = __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
-wq8_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restrict__ w, const float* __restrict__ scale,
-               float* __restrict__ y, int T, int N, int K) {
+wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restrict__ w, const float* __restrict__ scale,
+              float* __restrict__ y, int T, int N, int K) {
+    constexpr int kLd = BITS == 8 ? 4 : 2;               // uint4 loads per row and stage (64 codes)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = base;                                      // [kStages][kTileA]
@@ -204,13 +229,14 @@ wq8_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restri
         // ---------------- weight producers: row r's 64 codes of the stage as bf16, two stages ahead
         const int r = threadIdx.x - kWarpP0 * 32;               // 0..127
         const int n = min(n0 + r, N - 1);                       // past-the-end rows: produced, not stored
-        const int chunks = K / 16;                              // 16 codes per uint4; a K % 64 == 32 tail reads zeros
+        const int chunks = K * BITS / 128;                      // uint4s per row; a K % 64 == 32 tail reads zeros
         const uint4* row = reinterpret_cast<const uint4*>(w) + static_cast<size_t>(n) * chunks;
-        uint4 pf[2][4];
+        uint4 pf[2][kLd];
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) pf[a][i] = (4 * a + i < chunks) ? __ldg(row + 4 * a + i) : make_uint4(0u, 0u, 0u, 0u);
+            for (int i = 0; i < kLd; ++i)
+                pf[a][i] = (kLd * a + i < chunks) ? __ldg(row + kLd * a + i) : make_uint4(0u, 0u, 0u, 0u);
         uint8_t* trow = sA + (r >> 3) * 1024 + (r & 7) * 128;
         bool live = true;
         for (int k0 = 0; k0 < stages && live; k0 += 2) {
@@ -224,20 +250,33 @@ wq8_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restri
                     live = false;
                     break;
                 }
-                uint4 cw[4];
+                uint4 cw[kLd];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < kLd; ++i) {
                     cw[i] = pf[kk][i];
-                    pf[kk][i] = (4 * (k + 2) + i < chunks) ? __ldg(row + 4 * (k + 2) + i) : make_uint4(0u, 0u, 0u, 0u);
+                    pf[kk][i] = (kLd * (k + 2) + i < chunks) ? __ldg(row + kLd * (k + 2) + i)
+                                                              : make_uint4(0u, 0u, 0u, 0u);
                 }
                 uint8_t* tileA = trow + s * kTileA;
+                if constexpr (BITS == 8) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {          // 16 codes -> two 16-byte chunks of 8 bf16
-                    const uint2 a0 = codes_to_bf16x4(cw[i].x), a1 = codes_to_bf16x4(cw[i].y);
-                    const uint2 a2 = codes_to_bf16x4(cw[i].z), a3 = codes_to_bf16x4(cw[i].w);
-                    const int c0 = 2 * i, c1 = 2 * i + 1;
-                    *reinterpret_cast<uint4*>(tileA + ((c0 ^ (r & 7)) << 4)) = make_uint4(a0.x, a0.y, a1.x, a1.y);
-                    *reinterpret_cast<uint4*>(tileA + ((c1 ^ (r & 7)) << 4)) = make_uint4(a2.x, a2.y, a3.x, a3.y);
+                    for (int i = 0; i < 4; ++i) {          // 16 codes -> two 16-byte chunks of 8 bf16
+                        const uint2 a0 = codes_to_bf16x4(cw[i].x), a1 = codes_to_bf16x4(cw[i].y);
+                        const uint2 a2 = codes_to_bf16x4(cw[i].z), a3 = codes_to_bf16x4(cw[i].w);
+                        const int c0 = 2 * i, c1 = 2 * i + 1;
+                        *reinterpret_cast<uint4*>(tileA + ((c0 ^ (r & 7)) << 4)) = make_uint4(a0.x, a0.y, a1.x, a1.y);
+                        *reinterpret_cast<uint4*>(tileA + ((c1 ^ (r & 7)) << 4)) = make_uint4(a2.x, a2.y, a3.x, a3.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {          // 32 codes -> four 16-byte chunks of 8 bf16
+                        const uint32_t ws[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int c = 4 * i + j;
+                            *reinterpret_cast<uint4*>(tileA + ((c ^ (r & 7)) << 4)) = nibbles_to_bf16x8(ws[j]);
+                        }
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -245,7 +284,8 @@ wq8_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restri
             }
         }
     } else {
-        // ---------------- epilogue: y = scale * (sum over stages of the stage partials)
+        // ---------------- epilogue: y = scale * (sum over stages of the stage partials) (8 bits), or
+        //                  the fma chain of group scale * stage partial (4 bits)
         const int q = warp & 3;                                  // TMEM lanes 32q..32q+31
         const int h = (warp - kWarpE0) / 4;                      // tokens 64h..64h+63 of the tile
         const int r = q * 32 + lane;
@@ -254,8 +294,11 @@ wq8_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restri
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
         bool ok = true;
+        const int groups = (K + 127) / 128;
+        const float* gscale = scale + static_cast<size_t>(min(n, N - 1)) * groups;   // 4 bits
         for (int k = 0; k < stages; ++k) {
             const int a = k % kAccs;
+            const float sg = BITS == 4 ? __ldg(gscale + k / 2) : 0.0f;
             if (!wait_or_abort(&bars->accfull[a], static_cast<uint32_t>(k / kAccs) & 1u, abort) || *abort) {
                 ok = false;
                 break;
@@ -266,18 +309,19 @@ wq8_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restri
                 float v[32];
                 tc_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BN + h * 64 + c * 32), v);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[c * 32 + i] = __fadd_rn(acc[c * 32 + i], v[i]);
+                for (int i = 0; i < 32; ++i)
+                    acc[c * 32 + i] = BITS == 8 ? __fadd_rn(acc[c * 32 + i], v[i]) : __fmaf_rn(sg, v[i], acc[c * 32 + i]);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->accempty[a]);
         }
         if (ok && n < N) {
-            const float sc = __ldg(scale + n);
+            const float sc = BITS == 8 ? __ldg(scale + n) : 1.0f;
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
                 const int t = t0 + h * 64 + i;
-                if (t < T) y[static_cast<size_t>(t) * N + n] = __fmul_rn(sc, acc[i]);
+                if (t < T) y[static_cast<size_t>(t) * N + n] = BITS == 8 ? __fmul_rn(sc, acc[i]) : acc[i];
             }
         }
     }
@@ -330,8 +374,8 @@ __global__ void split_planes_kernel(const float4* __restrict__ x, uint2* __restr
 
 size_t wq_mma_workspace_bytes(int T, int K) { return static_cast<size_t>(kPlanes) * T * K * 2; }
 
-cudaError_t launch_wq8_mma(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
-                           void* workspace, cudaStream_t s) {
+cudaError_t launch_wq_mma(int bits, const uint32_t* w, const float* scale, const float* x, float* y, int T, int N,
+                          int K, void* workspace, cudaStream_t s) {
     const size_t quads = static_cast<size_t>(T) * K / 4;
     split_planes_kernel<<<static_cast<unsigned>(std::min<size_t>((quads + 255) / 256, 4096)), 256, 0, s>>>(
         reinterpret_cast<const float4*>(x), static_cast<uint2*>(workspace), quads);
@@ -342,16 +386,21 @@ cudaError_t launch_wq8_mma(const uint32_t* w, const float* scale, const float* x
                       static_cast<uint64_t>(kPlanes) * T, static_cast<uint64_t>(K) * 2, BK, BN, true))
         return cudaErrorInvalidValue;
     const size_t smem = 1024 + static_cast<size_t>(kStages) * (kTileA + kPlanes * kTileB) + sizeof(Bars);
-    static int configured_dev = -1;
+    static int configured_dev[2] = {-1, -1};
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(wq8_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    const int b = bits == 8 ? 0 : 1;
+    if (configured_dev[b] != dev) {
+        e = cudaFuncSetAttribute(bits == 8 ? wq_mma_kernel<8> : wq_mma_kernel<4>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
+        configured_dev[b] = dev;
     }
     const dim3 grid((N + BM - 1) / BM, (T + BN - 1) / BN);
-    wq8_mma_kernel<<<grid, kThreads, smem, s>>>(tmB, w, scale, y, T, N, K);
+    if (bits == 8)
+        wq_mma_kernel<8><<<grid, kThreads, smem, s>>>(tmB, w, scale, y, T, N, K);
+    else
+        wq_mma_kernel<4><<<grid, kThreads, smem, s>>>(tmB, w, scale, y, T, N, K);
     return cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-// Tensor-core W8A32 matmul (wq_mma.cu): the activation split into three bf16 planes in a caller's
+// Tensor-core W8A32 / W4A32 group-128 matmuls (wq_mma.cu): the activation split into three bf16 planes in a caller's
 // workspace, then one tcgen05 kernel.
 #pragma once
 #include <cstddef>
@@ -8,8 +8,9 @@
 
 namespace gq {
 size_t wq_mma_workspace_bytes(int T, int K);
-// K % 32 == 0, K >= 64; x and workspace 16-byte aligned, workspace of wq_mma_workspace_bytes(T, K).
-cudaError_t launch_wq8_mma(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
-                           void* workspace, cudaStream_t s);
+// bits 8 or 4; K % 32 == 0, K >= 64; w, x and workspace 16-byte aligned, workspace of
+// wq_mma_workspace_bytes(T, K).
+cudaError_t launch_wq_mma(int bits, const uint32_t* w, const float* scale, const float* x, float* y, int T, int N,
+                          int K, void* workspace, cudaStream_t s);
 unsigned error_read_clear_wq_mma();
 }  // namespace gq

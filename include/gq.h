@@ -233,24 +233,28 @@ int matvec_q4g128(const uint32_t* w_device, const float* scale_device, const flo
 int matmul_q4g128(const uint32_t* w_device, const float* scale_device, const float* x_device, float* y_device,
                   int T, int N, int K, gq_stream_t stream);
 
-/* matmul_q8 on the tensor cores (same operation and code layout as matmul_q8 above).  Each
+/* matmul_q8 / matmul_q4g128 on the tensor cores (same operations and code layouts as above).  Each
  * activation x is split exactly into three bf16 parts (hi = bf16(x), mid = bf16(x - hi),
  * lo = bf16(x - hi - mid), each rounded to nearest; hi + mid + lo == x for normal x), the int8
  * codes are exact in bf16, and the tensor cores accumulate the code * part products of one
- * 64-column stage (three parts x 64 columns) into an f32 partial; the partials are added in f32
- * with round to nearest, stage after stage, and y = scale[n] * sum.  The result lies within
+ * 64-column stage (three parts x 64 columns) into an f32 partial; 8 bits: the partials are added
+ * in f32 with round to nearest, stage after stage, and y = scale[n] * sum; 4 bits: acc =
+ * fma(scale[n, g], partial, acc) stage after stage (a stage lies inside one 128-column group g),
+ * y = acc.  The result lies within
  * c * 2^-24 * sum |scale * code * x| of the exact value with c = ceil(K/64) + 32 (two units per
  * tensor-core step, whose f32 accumulation rounding is not published), and the same inputs give
  * the same bits on every call.  Activations below 2^-126 * 2^16 in magnitude may lose their lowest bits
  * (the residual planes are bf16, whose exponent range is f32's).
  *   workspace_device: gq_wq_mma_workspace_bytes(T, K) bytes (3 * T * K bf16), 16-byte aligned,
- *   overwritten; the other arguments as matmul_q8.  Two launches on `stream` (the split, then the
+ *   overwritten; the other arguments as matmul_q8 / matmul_q4g128.  Two launches on `stream` (the split, then the
  *   tensor-core kernel).
  * Errors: GQ_EINVAL_SHAPE unless N >= 1, 1 <= T <= 65535 * 128, 64 <= K <= 65536 and K % 32 == 0;
  *         GQ_EINVAL_PTR for a NULL or misaligned pointer; GQ_ECUDA. */
 size_t gq_wq_mma_workspace_bytes(int T, int K);     /* 0 for an invalid shape */
 int matmul_q8_mma(const uint32_t* w_device, const float* scale_device, const float* x_device, float* y_device,
                   int T, int N, int K, void* workspace_device, gq_stream_t stream);
+int matmul_q4g128_mma(const uint32_t* w_device, const float* scale_device, const float* x_device, float* y_device,
+                      int T, int N, int K, void* workspace_device, gq_stream_t stream);
 
 /* Prefill GEMM over `cols` Q8_0 activation vectors ([P1] Q1_MM_WGSL / Q1_MM4_WGSL): every
  * (row, column) is the GEMV chain above, stored at y[c * rows + r].

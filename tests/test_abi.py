@@ -84,6 +84,10 @@ X = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
     (lambda L: L.matvec_q8(ctypes.c_void_p(0x1008), X, X, X, 8, 64, N), 2),
     (lambda L: L.matmul_q4g128(X, X, ctypes.c_void_p(0x1004), X, 3, 8, 64, N), 2),
     (lambda L: L.matvec_q4g128(X, N, X, X, 8, 64, N), 2),
+    (lambda L: L.matmul_q8_mma(X, X, X, X, 4, 8, 32, X, N), 1),
+    (lambda L: L.matmul_q8_mma(X, X, X, X, 4, 8, 96, N, N), 2),
+    (lambda L: L.matmul_q4g128_mma(X, X, X, X, 4, 8, 128, ctypes.c_void_p(0x1008), N), 2),
+    (lambda L: L.matmul_q4g128_mma(X, X, X, X, 0, 8, 128, X, N), 1),
     (lambda L: L.q1s32_f32_gemm(X, X, X, X, 1, 8, 48, 0, N), 1),
     (lambda L: L.q1s32_f32_gemm(X, X, X, X, 0, 8, 64, 0, N), 1),
     (lambda L: L.q1s32_f32_gemm(X, X, X, X, 1, 0, 64, 0, N), 1),
@@ -102,6 +106,12 @@ def test_host_validation_rejects_without_launching(L, call, expect):
 def test_workspace_bytes(L):
     assert L.gq_q1_q8_workspace_bytes(2560) == 80 * 96 + 16
     assert L.gq_q1_q8_workspace_bytes(100) == 0
+
+
+def test_wq_mma_workspace_bytes(L):
+    assert L.gq_wq_mma_workspace_bytes(512, 4096) == 3 * 512 * 4096 * 2
+    assert L.gq_wq_mma_workspace_bytes(1, 32) == 0
+    assert L.gq_wq_mma_workspace_bytes(0, 64) == 0
 
 
 def test_packed_bytes(L):

@@ -61,7 +61,7 @@ def _run(gq, bits, w, scale, x, mma=False):
     T = x.shape[0]
     args = (to_dev(w.view(np.int32)), to_dev(scale), to_dev(x))
     if mma:
-        return gq.matmul_q8_mma(*args).cpu().numpy()
+        return (gq.matmul_q8_mma if bits == 8 else gq.matmul_q4g128_mma)(*args).cpu().numpy()
     if bits == 8:
         y = gq.matvec_q8(*args) if T == 1 else gq.matmul_q8(*args)
     else:
@@ -124,26 +124,31 @@ def test_matmul_full_size_sampled(gq, bits):
     _check(bits, y[np.ix_(ts, ns)], want, w[ns], scale[ns], x[ts], T, ns.size, K)
 
 
-# ---- the tensor-core W8A32 matmul -------------------------------------------------------------
+# ---- the tensor-core matmuls -------------------------------------------------------------------
 
+@pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("T,N,K", [(1, 1, 64), (5, 257, 96), (33, 130, 1056), (128, 128, 64), (129, 129, 4128),
                                    (130, 300, 512), (300, 1000, 2048), (7, 3000, 16384)])
-def test_mma_within_bound(gq, T, N, K):
-    """Ragged tokens and rows across the 128 x 128 tile, K % 64 == 32 tails, one to many K stages."""
-    w, scale, x = wl.wq_inputs(wl.Rng(7000 + T + N + K), T, K, N, 8, p_m8=0.02)
-    _check(8, _run(gq, 8, w, scale, x, mma=True), _oracle(8, w, scale, x, T, N, K), w, scale, x, T, N, K, mma=True)
+def test_mma_within_bound(gq, bits, T, N, K):
+    """Ragged tokens and rows across the 128 x 128 tile, K % 64 == 32 tails (and, for 4 bits, a
+    last group shorter than 128), one to many K stages."""
+    w, scale, x = wl.wq_inputs(wl.Rng(7000 + bits + T + N + K), T, K, N, bits, p_m8=0.02)
+    _check(bits, _run(gq, bits, w, scale, x, mma=True), _oracle(bits, w, scale, x, T, N, K), w, scale, x, T, N, K,
+           mma=True)
 
 
+@pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("T", [1, 9, 200])
-def test_mma_exact_special_case(gq, T):
+def test_mma_exact_special_case(gq, bits, T):
     """Integer x in [-8, 8] and power-of-two scales: the bf16 split is x itself and every partial
     sum is exact, so the tensor cores give the oracle's value bit for bit."""
     N, K = 300, 1024
-    rng = wl.Rng(80 + T)
-    w, scale, _ = wl.wq_inputs(rng, T, K, N, 8, p_m8=0.05)
+    rng = wl.Rng(80 + bits + T)
+    w, scale, _ = wl.wq_inputs(rng, T, K, N, bits, p_m8=0.05)
     scale = (2.0 ** -(1 + (rng.u32(scale.size) % 6).astype(np.int64))).astype(np.float32).reshape(scale.shape)
     x = ((rng.u32(T * K) % 17).astype(np.int64) - 8).astype(np.float32).reshape(T, K)
-    assert np.array_equal(_run(gq, 8, w, scale, x, mma=True).astype(np.float64), _oracle(8, w, scale, x, T, N, K))
+    assert np.array_equal(_run(gq, bits, w, scale, x, mma=True).astype(np.float64),
+                          _oracle(bits, w, scale, x, T, N, K))
 
 
 def test_mma_split_is_exact(gq):
@@ -160,24 +165,44 @@ def test_mma_split_is_exact(gq):
     assert np.array_equal(y, x[:, np.arange(N) % K])
 
 
-def test_mma_deterministic_and_workspace(gq):
+def test_mma_q4_code_range(gq):
+    """Every 4-bit code -8..7 once per row position (a raw 0x8 reads as -8), integer x: exact."""
+    T, N, K = 3, 16, 128
+    codes = (np.arange(N * K) % 16).reshape(N, K).astype(np.uint32)
+    w = np.zeros((N, K // 8), np.uint32)
+    for j in range(8):
+        w |= codes[:, j::8] << np.uint32(4 * j)
+    scale = np.ones((N, 1), np.float32)
+    x = np.zeros((T, K), np.float32)
+    x[0, :] = 1.0
+    x[1, np.arange(K) % 16 == 8] = 1.0
+    x[2, :] = np.arange(K) % 5 - 2
+    y = _run(gq, 4, w, scale, x, mma=True)
+    assert np.array_equal(y.astype(np.float64), _oracle(4, w, scale, x, T, N, K))
+    assert np.all(y[1] == -8.0 * (K // 16))
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_mma_deterministic_and_workspace(gq, bits):
     import torch
     T, N, K = 260, 700, 2048
-    w, scale, x = wl.wq_inputs(wl.Rng(17), T, K, N, 8)
+    w, scale, x = wl.wq_inputs(wl.Rng(17), T, K, N, bits)
     dw, ds, dx = to_dev(w.view(np.int32)), to_dev(scale), to_dev(x)
+    fn = gq.matmul_q8_mma if bits == 8 else gq.matmul_q4g128_mma
     ws = torch.full((gq.wq_mma_workspace_bytes(T, K) + 64,), 0x7F, dtype=torch.uint8, device="cuda")
-    a = gq.matmul_q8_mma(dw, ds, dx, workspace=ws).cpu().numpy()
-    b = gq.matmul_q8_mma(dw, ds, dx).cpu().numpy()
+    a = fn(dw, ds, dx, workspace=ws).cpu().numpy()
+    b = fn(dw, ds, dx).cpu().numpy()
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
     assert gq.device_error() == 0
 
 
-def test_mma_full_size_sampled(gq):
+@pytest.mark.parametrize("bits", [8, 4])
+def test_mma_full_size_sampled(gq, bits):
     """512 tokens x 14336 rows x 4096 on the tensor cores: sampled rows and tokens against the oracle."""
     T, N, K = 512, 14336, 4096
-    w, scale, x = wl.wq_inputs(wl.Rng(6), T, K, N, 8)
-    y = _run(gq, 8, w, scale, x, mma=True)
+    w, scale, x = wl.wq_inputs(wl.Rng(6), T, K, N, bits)
+    y = _run(gq, bits, w, scale, x, mma=True)
     ns = np.unique(np.concatenate([np.arange(0, N, 911), [127, 128, N - 1]]))
     ts = np.unique(np.concatenate([np.arange(0, T, 41), [63, 64, 127, 128, T - 1]]))
-    want = _oracle(8, w[ns], scale[ns], x[ts], ts.size, ns.size, K)
-    _check(8, y[np.ix_(ts, ns)], want, w[ns], scale[ns], x[ts], T, ns.size, K, mma=True)
+    want = _oracle(bits, w[ns], scale[ns], x[ts], ts.size, ns.size, K)
+    _check(bits, y[np.ix_(ts, ns)], want, w[ns], scale[ns], x[ts], T, ns.size, K, mma=True)
