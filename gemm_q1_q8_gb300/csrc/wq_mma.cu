@@ -7,22 +7,24 @@
 // The activations are f32, the tensor cores take bf16: each x is split exactly into three bf16
 // parts, hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid) (round to nearest each time; the
 // two subtractions are exact), so hi + mid + lo = x for every normal x.  The int8 codes are exact in
-// bf16.  Every product code * part is exact in the tensor core.  The three parts of one 64-column
-// stage accumulate into a TMEM accumulator of their own (12 MMA steps); the epilogue adds the stage
-// partials in stage order in f32 with round to nearest, and multiplies by the row scale at the end
-// (8 bits), or folds each partial in with one fma by its group's scale (4 bits: a 64-column stage
-// lies inside one 128-column group).
-// (The tensor core's own f32 accumulation is not round-to-nearest: letting one accumulator run over
-// all of K gave a one-signed error that grew with K.)
+// bf16.  Every product code * part is exact in the tensor core.  The three parts of one 128-column
+// round (two 64-column smem stages, 24 MMA steps) accumulate into a TMEM accumulator of their own;
+// the epilogue adds the round partials in round order in f32 with round to nearest and multiplies
+// by the row scale at the end (8 bits), or folds each partial in with one fma by the scale of its
+// group (4 bits: a round is exactly one 128-column group).  (The tensor core's own f32 accumulation
+// is not round-to-nearest: letting one accumulator run over all of K gave a one-signed error that
+// grew with K.)
 //
 // Thread block (one per SM): 128 weight rows x 128 tokens, K in stages of 64.
-//   warp 0      : TMA producer of the three bf16 planes of the activation tile (128B swizzle)
-//   warp 1      : TMEM allocator and MMA issuer (one elected thread): 3 planes x 4 K16 steps per
-//                 stage into accumulator (stage % 4)
-//   warps 2-5   : weight producers, one row per thread: the row's 64 codes of the stage become bf16
-//                 in the swizzled K-major layout the MMA reads
-//   warps 6-13  : epilogue: after every stage, tcgen05.ld of its accumulator (a warp holds 32 rows x
-//                 64 tokens) added into registers; at the end y = scale * sum
+//   warps 0, 1  : MMA issuers (one elected thread each), rounds alternating between them, so one
+//                 waits on its barriers while the other keeps the tensor pipe fed; warp 0 also
+//                 allocates and frees TMEM
+//   warps 2-5   : producer group 0 (even stages), warps 6-9: group 1 (odd stages): one weight row
+//                 per thread, the row's 64 codes become bf16 in the swizzled K-major layout the MMA
+//                 reads; the group's first lane also starts the TMA copy of the three activation
+//                 planes of the stage (128B swizzle) onto the same barrier
+//   warps 10-17 : epilogue: after every round, tcgen05.ld of its accumulator (a warp holds 32 rows
+//                 x 64 tokens) added into registers; at the end y = scale * sum
 // Three smem stages (A 16 KB + B 3 x 16 KB), four TMEM accumulators (512 columns).  Every wait is
 // bounded (~1 s); a role that gives up raises an abort flag the others honour, and the block drains
 // its copies and MMAs and frees TMEM before it exits.
@@ -41,9 +43,10 @@ constexpr int kStages = 3;
 constexpr int kPlanes = 3;
 constexpr int kTileA = BM * BK * 2;               // 16 KB
 constexpr int kTileB = BN * BK * 2;               // 16 KB per plane
-constexpr int kAccs = 4;                          // TMEM accumulators of BN columns, stage k -> k % kAccs
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpP0 = 2, kNumPWarps = 4, kWarpE0 = 6, kNumEWarps = 8;
-constexpr int kThreads = (kWarpE0 + kNumEWarps) * 32;    // 448
+constexpr int kAccs = 4;                          // TMEM accumulators of BN columns, round r -> r % kAccs
+constexpr int kRoundStages = 2;                   // 64-column stages per round (128 columns)
+constexpr int kWarpP0 = 2, kGroupWarps = 4, kWarpE0 = 10, kNumEWarps = 8;
+constexpr int kThreads = (kWarpE0 + kNumEWarps) * 32;    // 576
 constexpr int kTmemCols = kAccs * BN;                    // 512
 
 // instruction descriptor: D f32, A/B bf16, both K-major, N = 128, M = 128
@@ -51,9 +54,11 @@ constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | (static_cas
                                 (static_cast<uint32_t>(BM >> 4) << 24);
 
 struct Bars {
-    uint64_t fullA[kStages], fullB[kStages], done[kStages];
+    uint64_t full[kStages];          // 4 producer-warp arrivals + the copy's expect_tx arrival, and its bytes
+    uint64_t done[kStages];          // the stage's MMAs have completed (slot free)
     uint64_t accfull[kAccs], accempty[kAccs];
-    uint64_t final_;
+    uint64_t final_;                 // both issuers' last MMAs have completed
+    int last_copy_stage[kStages];    // the last stage whose activation copy went into each slot
     uint32_t tmem_base;
     int abort;
 };
@@ -82,21 +87,18 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {    // 32 lanes x 32 columns
-    uint32_t r[32];
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {    // 32 lanes x 16 columns
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -161,22 +163,23 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BM, t0 = blockIdx.y * BN;
     const int stages = (K + BK - 1) / BK;     // the activation tile past K is zero-filled by the copy
+    const int rounds = (stages + kRoundStages - 1) / kRoundStages;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->fullA[s], kNumPWarps);
-            mbar_init(&bars->fullB[s], 1);
+            mbar_init(&bars->full[s], kGroupWarps + 1);
             mbar_init(&bars->done[s], 1);
+            bars->last_copy_stage[s] = -1;
         }
         for (int a = 0; a < kAccs; ++a) {
             mbar_init(&bars->accfull[a], 1);
             mbar_init(&bars->accempty[a], kNumEWarps);
         }
-        mbar_init(&bars->final_, 1);
+        mbar_init(&bars->final_, 2);
         bars->abort = 0;
         fence_barrier_init();
     }
-    if (warp == kWarpMma) {
+    if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars->tmem_base)),
                      "r"(kTmemCols)
                      : "memory");
@@ -187,130 +190,122 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    int tma_issued = 0;
-    if (warp == kWarpTma) {
+    if (warp < kWarpP0) {
+        // ---------------- MMA issuers: issuer j takes rounds j, j + 2, ...
         if (lane == 0) {
-            prefetch_tmap(&tmB);
-            for (int k = 0; k < stages; ++k) {
-                const int s = k % kStages;
-                if (k >= kStages &&
-                    !wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStages - 1) & 1u, abort))
+            for (int r = warp; r < rounds && !*abort; r += 2) {
+                const int a = r % kAccs;
+                if (r >= kAccs &&
+                    !wait_or_abort(&bars->accempty[a], static_cast<uint32_t>(r / kAccs - 1) & 1u, abort))
                     break;
-                mbar_arrive_expect_tx(&bars->fullB[s], kPlanes * kTileB);
-                for (int p = 0; p < kPlanes; ++p)
-                    tma_load_2d(sB + (s * kPlanes + p) * kTileB, &tmB, k * BK, p * T + t0, &bars->fullB[s]);
-                ++tma_issued;
-            }
-        }
-    } else if (warp == kWarpMma) {
-        if (lane == 0) {
-            for (int k = 0; k < stages && !*abort; ++k) {
-                const int s = k % kStages;
-                const int a = k % kAccs;
-                const uint32_t ph = static_cast<uint32_t>(k / kStages) & 1u;
-                if (!wait_or_abort(&bars->fullA[s], ph, abort) || !wait_or_abort(&bars->fullB[s], ph, abort)) break;
-                if (k >= kAccs &&
-                    !wait_or_abort(&bars->accempty[a], static_cast<uint32_t>(k / kAccs - 1) & 1u, abort))
-                    break;
-                tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(a * BN);
+                bool ok = true;
+                for (int k = r * kRoundStages; k < min(stages, (r + 1) * kRoundStages); ++k) {
+                    const int s = k % kStages;
+                    if (!wait_or_abort(&bars->full[s], static_cast<uint32_t>(k / kStages) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const bool first = k == r * kRoundStages;
 #pragma unroll
-                for (int p = 0; p < kPlanes; ++p)
+                    for (int p = 0; p < kPlanes; ++p)
 #pragma unroll
-                    for (int j = 0; j < BK / 16; ++j)
-                        tc_mma(d, smem_desc(sA + s * kTileA + j * 32), smem_desc(sB + (s * kPlanes + p) * kTileB + j * 32),
-                               (p > 0 || j > 0) ? 1u : 0u);
-                tc_commit(&bars->done[s]);
+                        for (int j = 0; j < BK / 16; ++j)
+                            tc_mma(d, smem_desc(sA + s * kTileA + j * 32),
+                                   smem_desc(sB + (s * kPlanes + p) * kTileB + j * 32),
+                                   (first && p == 0 && j == 0) ? 0u : 1u);
+                    tc_commit(&bars->done[s]);
+                }
+                if (!ok) break;
                 tc_commit(&bars->accfull[a]);
             }
             tc_commit(&bars->final_);
         }
     } else if (warp < kWarpE0) {
-        // ---------------- weight producers: row r's 64 codes of the stage as bf16, two stages ahead
-        const int r = threadIdx.x - kWarpP0 * 32;               // 0..127
+        // ---------------- producers: group g takes stages g, g + 2, ...
+        const int g = (warp - kWarpP0) / kGroupWarps;
+        const bool copier = lane == 0 && warp == kWarpP0 + g * kGroupWarps;
+        const int r = threadIdx.x - (kWarpP0 + g * kGroupWarps) * 32;    // row 0..127 of the tile
         const int n = min(n0 + r, N - 1);                       // past-the-end rows: produced, not stored
         const int chunks = K * BITS / 128;                      // uint4s per row; a K % 64 == 32 tail reads zeros
         const uint4* row = reinterpret_cast<const uint4*>(w) + static_cast<size_t>(n) * chunks;
-        uint4 pf[2][kLd];
+        if (copier) prefetch_tmap(&tmB);
+        uint4 pf[kLd];
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int i = 0; i < kLd; ++i)
-                pf[a][i] = (kLd * a + i < chunks) ? __ldg(row + kLd * a + i) : make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < kLd; ++i)
+            pf[i] = (g < stages && kLd * g + i < chunks) ? __ldg(row + kLd * g + i) : make_uint4(0u, 0u, 0u, 0u);
         uint8_t* trow = sA + (r >> 3) * 1024 + (r & 7) * 128;
-        bool live = true;
-        for (int k0 = 0; k0 < stages && live; k0 += 2) {
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                const int k = k0 + kk;
-                if (k >= stages) break;
-                const int s = k % kStages;
-                if (k >= kStages &&
-                    !wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStages - 1) & 1u, abort)) {
-                    live = false;
-                    break;
-                }
-                uint4 cw[kLd];
-#pragma unroll
-                for (int i = 0; i < kLd; ++i) {
-                    cw[i] = pf[kk][i];
-                    pf[kk][i] = (kLd * (k + 2) + i < chunks) ? __ldg(row + kLd * (k + 2) + i)
-                                                              : make_uint4(0u, 0u, 0u, 0u);
-                }
-                uint8_t* tileA = trow + s * kTileA;
-                if constexpr (BITS == 8) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {          // 16 codes -> two 16-byte chunks of 8 bf16
-                        const uint2 a0 = codes_to_bf16x4(cw[i].x), a1 = codes_to_bf16x4(cw[i].y);
-                        const uint2 a2 = codes_to_bf16x4(cw[i].z), a3 = codes_to_bf16x4(cw[i].w);
-                        const int c0 = 2 * i, c1 = 2 * i + 1;
-                        *reinterpret_cast<uint4*>(tileA + ((c0 ^ (r & 7)) << 4)) = make_uint4(a0.x, a0.y, a1.x, a1.y);
-                        *reinterpret_cast<uint4*>(tileA + ((c1 ^ (r & 7)) << 4)) = make_uint4(a2.x, a2.y, a3.x, a3.y);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {          // 32 codes -> four 16-byte chunks of 8 bf16
-                        const uint32_t ws[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int c = 4 * i + j;
-                            *reinterpret_cast<uint4*>(tileA + ((c ^ (r & 7)) << 4)) = nibbles_to_bf16x8(ws[j]);
-                        }
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->fullA[s]);
+        for (int k = g; k < stages; k += 2) {
+            const int s = k % kStages;
+            if (k >= kStages && !wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStages - 1) & 1u, abort))
+                break;
+            if (copier) {
+                mbar_arrive_expect_tx(&bars->full[s], kPlanes * kTileB);
+                for (int p = 0; p < kPlanes; ++p)
+                    tma_load_2d(sB + (s * kPlanes + p) * kTileB, &tmB, k * BK, p * T + t0, &bars->full[s]);
+                bars->last_copy_stage[s] = k;
             }
+            uint4 cw[kLd];
+#pragma unroll
+            for (int i = 0; i < kLd; ++i) {
+                cw[i] = pf[i];
+                const int c = kLd * (k + 2) + i;
+                pf[i] = (c < chunks) ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            uint8_t* tileA = trow + s * kTileA;
+            if constexpr (BITS == 8) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {          // 16 codes -> two 16-byte chunks of 8 bf16
+                    const uint2 a0 = codes_to_bf16x4(cw[i].x), a1 = codes_to_bf16x4(cw[i].y);
+                    const uint2 a2 = codes_to_bf16x4(cw[i].z), a3 = codes_to_bf16x4(cw[i].w);
+                    const int c0 = 2 * i, c1 = 2 * i + 1;
+                    *reinterpret_cast<uint4*>(tileA + ((c0 ^ (r & 7)) << 4)) = make_uint4(a0.x, a0.y, a1.x, a1.y);
+                    *reinterpret_cast<uint4*>(tileA + ((c1 ^ (r & 7)) << 4)) = make_uint4(a2.x, a2.y, a3.x, a3.y);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {          // 32 codes -> four 16-byte chunks of 8 bf16
+                    const uint32_t ws[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int c = 4 * i + j;
+                        *reinterpret_cast<uint4*>(tileA + ((c ^ (r & 7)) << 4)) = nibbles_to_bf16x8(ws[j]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->full[s]);
         }
     } else {
-        // ---------------- epilogue: y = scale * (sum over stages of the stage partials) (8 bits), or
-        //                  the fma chain of group scale * stage partial (4 bits)
+        // ---------------- epilogue: y = scale * (sum over rounds of the round partials) (8 bits), or
+        //                  the fma chain of group scale * round partial (4 bits)
         const int q = warp & 3;                                  // TMEM lanes 32q..32q+31
         const int h = (warp - kWarpE0) / 4;                      // tokens 64h..64h+63 of the tile
-        const int r = q * 32 + lane;
-        const int n = n0 + r;
+        const int rr = q * 32 + lane;
+        const int n = n0 + rr;
         float acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
         bool ok = true;
         const int groups = (K + 127) / 128;
         const float* gscale = scale + static_cast<size_t>(min(n, N - 1)) * groups;   // 4 bits
-        for (int k = 0; k < stages; ++k) {
-            const int a = k % kAccs;
-            const float sg = BITS == 4 ? __ldg(gscale + k / 2) : 0.0f;
-            if (!wait_or_abort(&bars->accfull[a], static_cast<uint32_t>(k / kAccs) & 1u, abort) || *abort) {
+        for (int r = 0; r < rounds; ++r) {
+            const int a = r % kAccs;
+            const float sg = BITS == 4 ? __ldg(gscale + r) : 0.0f;
+            if (!wait_or_abort(&bars->accfull[a], static_cast<uint32_t>(r / kAccs) & 1u, abort) || *abort) {
                 ok = false;
                 break;
             }
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tc_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BN + h * 64 + c * 32), v);
+            for (int c = 0; c < 4; ++c) {
+                float v[16];
+                tc_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BN + h * 64 + c * 16), v);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    acc[c * 32 + i] = BITS == 8 ? __fadd_rn(acc[c * 32 + i], v[i]) : __fmaf_rn(sg, v[i], acc[c * 32 + i]);
+                for (int i = 0; i < 16; ++i)
+                    acc[c * 16 + i] = BITS == 8 ? __fadd_rn(acc[c * 16 + i], v[i]) : __fmaf_rn(sg, v[i], acc[c * 16 + i]);
             }
             tc_fence_before();
             __syncwarp();
@@ -328,22 +323,26 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
 
     // ---------------- teardown
     __syncwarp();
-    if (warp == kWarpMma) {
+    if (warp == 0) {
         // every MMA issued has completed before TMEM is freed
         if (lane == 0 && !mbar_wait(&bars->final_, 0)) report_error(kErrMmaTimeout);
         __syncwarp();
     }
-    if (warp == kWarpTma && lane == 0) {
-        const int first = tma_issued > kStages ? tma_issued - kStages : 0;
-        for (int k = first; k < tma_issued; ++k)
-            if (!mbar_wait(&bars->fullB[k % kStages], static_cast<uint32_t>(k / kStages) & 1u))
-                report_error(kErrDrainTimeout);
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kWarpMma)
+    if (threadIdx.x == 32 && *abort) {
+        // an aborted block may hold activation copies no MMA waited for: the last copy into each
+        // slot lands before the block's shared memory goes away
+        for (int s = 0; s < kStages; ++s) {
+            const int k = bars->last_copy_stage[s];
+            if (k >= 0 && !mbar_wait(&bars->full[s], static_cast<uint32_t>(k / kStages) & 1u))
+                report_error(kErrDrainTimeout);
+        }
+    }
+    if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    __syncthreads();
 }
 
 // x [T, K] f32 -> planes [3][T][K] bf16: hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid).

@@ -237,13 +237,12 @@ int matmul_q4g128(const uint32_t* w_device, const float* scale_device, const flo
  * activation x is split exactly into three bf16 parts (hi = bf16(x), mid = bf16(x - hi),
  * lo = bf16(x - hi - mid), each rounded to nearest; hi + mid + lo == x for normal x), the int8
  * codes are exact in bf16, and the tensor cores accumulate the code * part products of one
- * 64-column stage (three parts x 64 columns) into an f32 partial; 8 bits: the partials are added
- * in f32 with round to nearest, stage after stage, and y = scale[n] * sum; 4 bits: acc =
- * fma(scale[n, g], partial, acc) stage after stage (a stage lies inside one 128-column group g),
- * y = acc.  The result lies within
- * c * 2^-24 * sum |scale * code * x| of the exact value with c = ceil(K/64) + 32 (two units per
- * tensor-core step, whose f32 accumulation rounding is not published), and the same inputs give
- * the same bits on every call.  Activations below 2^-126 * 2^16 in magnitude may lose their lowest bits
+ * 128-column round (three parts x 128 columns) into an f32 partial; 8 bits: the partials are added
+ * in f32 with round to nearest, round after round, and y = scale[n] * sum; 4 bits: acc =
+ * fma(scale[n, g], partial, acc) round after round (round g is group g), y = acc.  The result lies
+ * within c * 2^-24 * sum |scale * code * x| of the exact value with c = ceil(K/128) + 56 (two units
+ * per tensor-core step, whose f32 accumulation rounding is not published), and the same inputs
+ * give the same bits on every call.  Activations below 2^-126 * 2^16 in magnitude may lose their lowest bits
  * (the residual planes are bf16, whose exponent range is f32's).
  *   workspace_device: gq_wq_mma_workspace_bytes(T, K) bytes (3 * T * K bf16), 16-byte aligned,
  *   overwritten; the other arguments as matmul_q8 / matmul_q4g128.  Two launches on `stream` (the split, then the

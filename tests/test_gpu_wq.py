@@ -37,12 +37,13 @@ def _depth(bits, T, K, mma=False):
     16-term chain per chunk, one fma with the group scale per chunk, the butterfly and tree.
     T > 4 (GEMM): one fma per column, plus the scale multiply (8 bits) or the dequantizing product
     code * scale (4 bits).
-    Tensor cores (matmul_q8_mma): per 64-column stage, 12 MMA steps (three planes x 4 K16 steps)
+    Tensor cores (matmul_*_mma): per 128-column round, 24 MMA steps (three planes x 8 K16 steps)
     into a fresh accumulator -- the hardware's accumulation rounding is not published, so each step
-    is allowed two units -- then a round-to-nearest f32 add of each stage partial in stage order
-    (ceil(K/64)), the scale multiply, and 7 units of slack for the sums inside a step."""
+    is allowed two units -- then a round-to-nearest f32 add (or fma with the group scale) of each
+    round partial in round order (ceil(K/128)), the scale multiply, and 7 units of slack for the
+    sums inside a step."""
     if mma:
-        return -(-K // 64) + 2 * 12 + 8
+        return -(-K // 128) + 2 * 24 + 8
     if T <= 4:
         return 16 * -(-K // 4096) + 10 if bits == 8 else 28 + -(-K // 512)
     return K + 2
