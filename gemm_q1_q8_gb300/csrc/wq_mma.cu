@@ -15,19 +15,22 @@
 // is not round-to-nearest: letting one accumulator run over all of K gave a one-signed error that
 // grew with K.)
 //
-// Thread block (one per SM): 128 weight rows x 128 tokens, K in stages of 64.
+// Thread block (one per SM): 128 weight rows x 128 tokens, K in stages of 64.  The weight operand
+// (A) lives in tensor memory, written there by the producers with tcgen05.st; shared memory holds
+// only the activation planes (B), so the MMAs' shared-memory reads are B's alone.
 //   warps 0, 1  : MMA issuers (one elected thread each), rounds alternating between them, so one
 //                 waits on its barriers while the other keeps the tensor pipe fed; warp 0 also
 //                 allocates and frees TMEM
 //   warps 2-5   : producer group 0 (even stages), warps 6-9: group 1 (odd stages): one weight row
-//                 per thread, the row's 64 codes become bf16 in the swizzled K-major layout the MMA
-//                 reads; the group's first lane also starts the TMA copy of the three activation
-//                 planes of the stage (128B swizzle) onto the same barrier
+//                 per thread (the TMEM lane its warp may write), the row's 64 codes of the stage
+//                 become 32 columns of bf16 pairs in the stage's A slot; the group's first lane also
+//                 starts the TMA copy of the three activation planes of the stage (128B swizzle)
+//                 onto the same barrier
 //   warps 10-17 : epilogue: after every round, tcgen05.ld of its accumulator (a warp holds 32 rows
 //                 x 64 tokens) added into registers; at the end y = scale * sum
-// Three smem stages (A 16 KB + B 3 x 16 KB), four TMEM accumulators (512 columns).  Every wait is
-// bounded (~1 s); a role that gives up raises an abort flag the others honour, and the block drains
-// its copies and MMAs and frees TMEM before it exits.
+// Four stage slots (B 3 x 16 KB in shared memory, A 32 TMEM columns each) and three TMEM
+// accumulators of 128 columns.  Every wait is bounded (~1 s); a role that gives up raises an abort
+// flag the others honour, and the block drains its copies and MMAs and frees TMEM before it exits.
 #include "gq_internal.cuh"
 #include "wq_mma.cuh"
 
@@ -39,17 +42,19 @@ GQ_ERROR_ACCESSOR(wq_mma)
 namespace {
 
 constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kPlanes = 3;
-constexpr int kTileA = BM * BK * 2;               // 16 KB
 constexpr int kTileB = BN * BK * 2;               // 16 KB per plane
-constexpr int kAccs = 4;                          // TMEM accumulators of BN columns, round r -> r % kAccs
+constexpr int kAccs = 3;                          // TMEM accumulators of BN columns, round r -> r % kAccs
+constexpr int kAColsPerStage = BK / 2;            // A slot: 64 bf16 per row = 32 columns of pairs
+constexpr int kACol0 = kAccs * BN;                // A slots after the accumulators (384 + 4 x 32 = 512)
 constexpr int kRoundStages = 2;                   // 64-column stages per round (128 columns)
 constexpr int kWarpP0 = 2, kGroupWarps = 4, kWarpE0 = 10, kNumEWarps = 8;
 constexpr int kThreads = (kWarpE0 + kNumEWarps) * 32;    // 576
-constexpr int kTmemCols = kAccs * BN;                    // 512
+constexpr int kTmemCols = 512;
+static_assert(kACol0 + kStages * kAColsPerStage <= kTmemCols, "TMEM columns");
 
-// instruction descriptor: D f32, A/B bf16, both K-major, N = 128, M = 128
+// instruction descriptor: D f32, A/B bf16, both K-major, N = 128, M = 128 (A from TMEM)
 constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
                                 (static_cast<uint32_t>(BM >> 4) << 24);
 
@@ -75,12 +80,24 @@ __device__ __forceinline__ uint64_t smem_desc(const void* p) {   // 128B swizzle
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(kIdescBf16), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(kIdescBf16), "r"(accumulate)
+        : "memory");
+}
+// 32 lanes x 32 columns from registers (thread t -> lane t of its warp's quarter)
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -156,8 +173,7 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
     constexpr int kLd = BITS == 8 ? 4 : 2;               // uint4 loads per row and stage (64 codes)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = base;                                      // [kStages][kTileA]
-    uint8_t* sB = base + kStages * kTileA;                   // [kStages][kPlanes][kTileB]
+    uint8_t* sB = base;                                      // [kStages][kPlanes][kTileB]
     Bars* bars = reinterpret_cast<Bars*>(sB + kStages * kPlanes * kTileB);
     volatile int* abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -208,13 +224,14 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
                     }
                     tc_fence_after();
                     const bool first = k == r * kRoundStages;
+                    const uint32_t aslot = tmem + static_cast<uint32_t>(kACol0 + s * kAColsPerStage);
 #pragma unroll
                     for (int p = 0; p < kPlanes; ++p)
 #pragma unroll
                         for (int j = 0; j < BK / 16; ++j)
-                            tc_mma(d, smem_desc(sA + s * kTileA + j * 32),
-                                   smem_desc(sB + (s * kPlanes + p) * kTileB + j * 32),
-                                   (first && p == 0 && j == 0) ? 0u : 1u);
+                            tc_mma_ts(d, aslot + static_cast<uint32_t>(j * 8),
+                                      smem_desc(sB + (s * kPlanes + p) * kTileB + j * 32),
+                                      (first && p == 0 && j == 0) ? 0u : 1u);
                     tc_commit(&bars->done[s]);
                 }
                 if (!ok) break;
@@ -226,7 +243,7 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
         // ---------------- producers: group g takes stages g, g + 2, ...
         const int g = (warp - kWarpP0) / kGroupWarps;
         const bool copier = lane == 0 && warp == kWarpP0 + g * kGroupWarps;
-        const int r = threadIdx.x - (kWarpP0 + g * kGroupWarps) * 32;    // row 0..127 of the tile
+        const int r = (warp & 3) * 32 + lane;                   // row = the TMEM lane this warp may write
         const int n = min(n0 + r, N - 1);                       // past-the-end rows: produced, not stored
         const int chunks = K * BITS / 128;                      // uint4s per row; a K % 64 == 32 tail reads zeros
         const uint4* row = reinterpret_cast<const uint4*>(w) + static_cast<size_t>(n) * chunks;
@@ -235,7 +252,7 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
 #pragma unroll
         for (int i = 0; i < kLd; ++i)
             pf[i] = (g < stages && kLd * g + i < chunks) ? __ldg(row + kLd * g + i) : make_uint4(0u, 0u, 0u, 0u);
-        uint8_t* trow = sA + (r >> 3) * 1024 + (r & 7) * 128;
+        const uint32_t tlane = static_cast<uint32_t>((warp & 3) * 32) << 16;
         for (int k = g; k < stages; k += 2) {
             const int s = k % kStages;
             if (k >= kStages && !wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStages - 1) & 1u, abort))
@@ -253,28 +270,35 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
                 const int c = kLd * (k + 2) + i;
                 pf[i] = (c < chunks) ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
             }
-            uint8_t* tileA = trow + s * kTileA;
+            uint32_t av[32];                               // bf16 pairs (codes 2i, 2i + 1) of the row
             if constexpr (BITS == 8) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {          // 16 codes -> two 16-byte chunks of 8 bf16
-                    const uint2 a0 = codes_to_bf16x4(cw[i].x), a1 = codes_to_bf16x4(cw[i].y);
-                    const uint2 a2 = codes_to_bf16x4(cw[i].z), a3 = codes_to_bf16x4(cw[i].w);
-                    const int c0 = 2 * i, c1 = 2 * i + 1;
-                    *reinterpret_cast<uint4*>(tileA + ((c0 ^ (r & 7)) << 4)) = make_uint4(a0.x, a0.y, a1.x, a1.y);
-                    *reinterpret_cast<uint4*>(tileA + ((c1 ^ (r & 7)) << 4)) = make_uint4(a2.x, a2.y, a3.x, a3.y);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {          // 32 codes -> four 16-byte chunks of 8 bf16
+                for (int i = 0; i < 4; ++i) {
                     const uint32_t ws[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int c = 4 * i + j;
-                        *reinterpret_cast<uint4*>(tileA + ((c ^ (r & 7)) << 4)) = nibbles_to_bf16x8(ws[j]);
+                        const uint2 pr = codes_to_bf16x4(ws[j]);
+                        av[8 * i + 2 * j] = pr.x;
+                        av[8 * i + 2 * j + 1] = pr.y;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const uint32_t ws[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 pr = nibbles_to_bf16x8(ws[j]);
+                        av[16 * i + 4 * j] = pr.x;
+                        av[16 * i + 4 * j + 1] = pr.y;
+                        av[16 * i + 4 * j + 2] = pr.z;
+                        av[16 * i + 4 * j + 3] = pr.w;
                     }
                 }
             }
-            fence_proxy_async_smem();
+            tc_st32(tmem + tlane + static_cast<uint32_t>(kACol0 + s * kAColsPerStage), av);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->full[s]);
         }
@@ -384,7 +408,7 @@ cudaError_t launch_wq_mma(int bits, const uint32_t* w, const float* scale, const
     if (!make_tmap_2d(&tmB, workspace, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(K),
                       static_cast<uint64_t>(kPlanes) * T, static_cast<uint64_t>(K) * 2, BK, BN, true))
         return cudaErrorInvalidValue;
-    const size_t smem = 1024 + static_cast<size_t>(kStages) * (kTileA + kPlanes * kTileB) + sizeof(Bars);
+    const size_t smem = 1024 + static_cast<size_t>(kStages) * kPlanes * kTileB + sizeof(Bars);
     static int configured_dev[2] = {-1, -1};
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
