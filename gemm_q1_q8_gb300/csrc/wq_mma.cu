@@ -23,13 +23,16 @@
 //                 allocates and frees TMEM
 //   warps 2-5   : producer group 0 (even stages), warps 6-9: group 1 (odd stages): one weight row
 //                 per thread (the TMEM lane its warp may write), the row's 64 codes of the stage
-//                 become 32 columns of bf16 pairs in the stage's A slot; the group's first lane also
-//                 starts the TMA copy of the three activation planes of the stage (128B swizzle)
-//                 onto the same barrier
+//                 become 32 columns of bf16 pairs in the stage's A slot; each thread fetches its
+//                 row's codes two of its stages ahead with cp.async into a private shared-memory
+//                 ring (no registers held, no barrier: only the thread reads what it copied); the
+//                 group's first lane also starts the TMA copy of the three activation planes of the
+//                 stage (128B swizzle) onto the same barrier
 //   warps 10-17 : epilogue: after every round, tcgen05.ld of its accumulator (a warp holds 32 rows
 //                 x 64 tokens) added into registers; at the end y = scale * sum
-// Four stage slots (B 3 x 16 KB in shared memory, A 32 TMEM columns each) and three TMEM
-// accumulators of 128 columns.  Every wait is bounded (~1 s); a role that gives up raises an abort
+// Four stage slots (B 3 x 16 KB in shared memory, A 32 TMEM columns each), three TMEM
+// accumulators of 128 columns, 32 KB of code rings.  The kernel is launched as a programmatic
+// dependent of the split: everything but the activation copies starts before the split finishes.  Every wait is bounded (~1 s); a role that gives up raises an abort
 // flag the others honour, and the block drains its copies and MMAs and frees TMEM before it exits.
 #include "gq_internal.cuh"
 #include "wq_mma.cuh"
@@ -52,6 +55,8 @@ constexpr int kRoundStages = 2;                   // 64-column stages per round 
 constexpr int kWarpP0 = 2, kGroupWarps = 4, kWarpE0 = 10, kNumEWarps = 8;
 constexpr int kThreads = (kWarpE0 + kNumEWarps) * 32;    // 576
 constexpr int kTmemCols = 512;
+constexpr int kRing = 2;                          // code-ring slots per producer thread (its stages ahead)
+constexpr int kRingBytes = 2 * kRing * 4 * 128 * 16;   // 2 groups x slots x 4 chunks x 128 rows x 16 B
 static_assert(kACol0 + kStages * kAColsPerStage <= kTmemCols, "TMEM columns");
 
 // instruction descriptor: D f32, A/B bf16, both K-major, N = 128, M = 128 (A from TMEM)
@@ -99,6 +104,14 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* r) {
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -174,7 +187,8 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sB = base;                                      // [kStages][kPlanes][kTileB]
-    Bars* bars = reinterpret_cast<Bars*>(sB + kStages * kPlanes * kTileB);
+    uint8_t* sC = sB + kStages * kPlanes * kTileB;           // [group][kRing][4 chunks][128 rows] x 16 B
+    Bars* bars = reinterpret_cast<Bars*>(sC + kRingBytes);
     volatile int* abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BM, t0 = blockIdx.y * BN;
@@ -248,28 +262,40 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
         const int chunks = K * BITS / 128;                      // uint4s per row; a K % 64 == 32 tail reads zeros
         const uint4* row = reinterpret_cast<const uint4*>(w) + static_cast<size_t>(n) * chunks;
         if (copier) prefetch_tmap(&tmB);
-        uint4 pf[kLd];
+        uint8_t* ring = sC + (g * kRing * 4 * 128 + r) * 16;      // + (slot * 4 + chunk) * 128 * 16
+        auto fetch = [&](int kk, int slot) {                     // this thread's codes of stage kk
 #pragma unroll
-        for (int i = 0; i < kLd; ++i)
-            pf[i] = (g < stages && kLd * g + i < chunks) ? __ldg(row + kLd * g + i) : make_uint4(0u, 0u, 0u, 0u);
+            for (int i = 0; i < kLd; ++i) {
+                const int c = kLd * kk + i;
+                if (kk < stages && c < chunks) cp_async16(ring + (slot * 4 + i) * 128 * 16, row + c);
+            }
+            cp_async_commit();
+        };
+        fetch(g, 0);
+        fetch(g + 2, 1);
         const uint32_t tlane = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        for (int k = g; k < stages; k += 2) {
+        bool waited = false;                                     // the split has finished (copier only)
+        for (int k = g, m = 0; k < stages; k += 2, ++m) {
             const int s = k % kStages;
             if (k >= kStages && !wait_or_abort(&bars->done[s], static_cast<uint32_t>(k / kStages - 1) & 1u, abort))
                 break;
             if (copier) {
+                if (!waited) {
+                    asm volatile("griddepcontrol.wait;" ::: "memory");   // the activation planes are written
+                    waited = true;
+                }
                 mbar_arrive_expect_tx(&bars->full[s], kPlanes * kTileB);
                 for (int p = 0; p < kPlanes; ++p)
                     tma_load_2d(sB + (s * kPlanes + p) * kTileB, &tmB, k * BK, p * T + t0, &bars->full[s]);
                 bars->last_copy_stage[s] = k;
             }
+            cp_async_wait<kRing - 1>();                           // this stage's codes have landed
+            const int slot = m % kRing;
             uint4 cw[kLd];
 #pragma unroll
-            for (int i = 0; i < kLd; ++i) {
-                cw[i] = pf[i];
-                const int c = kLd * (k + 2) + i;
-                pf[i] = (c < chunks) ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int i = 0; i < kLd; ++i)
+                cw[i] = (kLd * k + i < chunks) ? *reinterpret_cast<const uint4*>(ring + (slot * 4 + i) * 128 * 16)
+                                               : make_uint4(0u, 0u, 0u, 0u);
             uint32_t av[32];                               // bf16 pairs (codes 2i, 2i + 1) of the row
             if constexpr (BITS == 8) {
 #pragma unroll
@@ -301,7 +327,9 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->full[s]);
+            fetch(k + 2 * kRing, slot);                          // the slot's codes are consumed
         }
+        cp_async_wait<0>();                                      // no copy lands after the block is gone
     } else {
         // ---------------- epilogue: y = scale * (sum over rounds of the round partials) (8 bits), or
         //                  the fma chain of group scale * round partial (4 bits)
@@ -371,6 +399,8 @@ wq_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restric
 
 // x [T, K] f32 -> planes [3][T][K] bf16: hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid).
 __global__ void split_planes_kernel(const float4* __restrict__ x, uint2* __restrict__ planes, size_t quads) {
+    // the matmul grid may launch now; its activation copies still wait for this grid's writes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < quads;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         const float4 v = x[i];
@@ -408,7 +438,7 @@ cudaError_t launch_wq_mma(int bits, const uint32_t* w, const float* scale, const
     if (!make_tmap_2d(&tmB, workspace, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(K),
                       static_cast<uint64_t>(kPlanes) * T, static_cast<uint64_t>(K) * 2, BK, BN, true))
         return cudaErrorInvalidValue;
-    const size_t smem = 1024 + static_cast<size_t>(kStages) * kPlanes * kTileB + sizeof(Bars);
+    const size_t smem = 1024 + static_cast<size_t>(kStages) * kPlanes * kTileB + kRingBytes + sizeof(Bars);
     static int configured_dev[2] = {-1, -1};
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -419,11 +449,19 @@ cudaError_t launch_wq_mma(int bits, const uint32_t* w, const float* scale, const
         if (e != cudaSuccess) return e;
         configured_dev[b] = dev;
     }
-    const dim3 grid((N + BM - 1) / BM, (T + BN - 1) / BN);
-    if (bits == 8)
-        wq_mma_kernel<8><<<grid, kThreads, smem, s>>>(tmB, w, scale, y, T, N, K);
-    else
-        wq_mma_kernel<4><<<grid, kThreads, smem, s>>>(tmB, w, scale, y, T, N, K);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + BM - 1) / BM, (T + BN - 1) / BN);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = bits == 8 ? cudaLaunchKernelEx(&cfg, wq_mma_kernel<8>, tmB, w, scale, y, T, N, K)
+                  : cudaLaunchKernelEx(&cfg, wq_mma_kernel<4>, tmB, w, scale, y, T, N, K);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-"""The decode kernels that are launched as programmatic dependents (weights requested before the
+"""The kernels that are launched as programmatic dependents (weights requested before the
 wait for the preceding grids, activations read and outputs written after it) must still see an
 activation produced by the operation just before them on the stream, and their output writes
 must land after the previous call's.  Each case overwrites the activation buffer on the stream
@@ -75,4 +75,20 @@ def test_w1a32_decode_dependent(gq):
     x = to_dev(xa)
     y = _chain(lambda xd: gq.q1s32_f32_gemm(sa, wa, xd), lambda xd, out: gq.q1s32_f32_gemm(sb, wb, xd, out=out), x, xb)
     lone = gq.q1s32_f32_gemm(sb, wb, to_dev(xb)).cpu().numpy()
+    assert np.array_equal(y.view(np.uint32), lone.view(np.uint32))
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_wq_mma_dependent(gq, bits):
+    """The tensor-core matmul starts before its activation split finishes (only its activation
+    copies wait): a rewritten activation and a shared workspace must still give the lone result."""
+    T, N, K = 300, 2000, 2048
+    w1, c1, xa = wl.wq_inputs(wl.Rng(9), T, K, N, bits)
+    w2, c2, xb = wl.wq_inputs(wl.Rng(10), T, K, N, bits)
+    mm = gq.matmul_q8_mma if bits == 8 else gq.matmul_q4g128_mma
+    wa, ca, wb, cb = to_dev(w1.view(np.int32)), to_dev(c1), to_dev(w2.view(np.int32)), to_dev(c2)
+    ws = torch.empty(gq.wq_mma_workspace_bytes(T, K), dtype=torch.uint8, device="cuda")
+    x = to_dev(xa)
+    y = _chain(lambda xd: mm(wa, ca, xd, workspace=ws), lambda xd, out: mm(wb, cb, xd, out=out, workspace=ws), x, xb)
+    lone = mm(wb, cb, to_dev(xb)).cpu().numpy()
     assert np.array_equal(y.view(np.uint32), lone.view(np.uint32))
