@@ -366,12 +366,13 @@ def ternary_bitplane_gemv(P: torch.Tensor, N: torch.Tensor, X: torch.Tensor, out
 # ----------------------------------------------------------------------------- prefill
 
 def quantize_q8_0(x: torch.Tensor, mma_operand: bool = False):
-    """(d [m, k/32] f16 bits as int16, q [m, k] int8, operand [m, k] f16 bits or None)."""
+    """(d [m, k/32] f16 bits as int16, q [m, k] int8, operand [3, m, k] bf16 bits or None: the
+    three bf16 parts of f16(d) * q that the prefill MMA path reads)."""
     m, k = x.shape
     _need(x, torch.float32, m * k, "x")
     d = torch.empty((m, k // 32), dtype=torch.int16, device=x.device)
     q = torch.empty((m, k), dtype=torch.int8, device=x.device)
-    op = torch.empty((m, k), dtype=torch.int16, device=x.device) if mma_operand else None
+    op = torch.empty((3, m, k), dtype=torch.int16, device=x.device) if mma_operand else None
     _check(lib().gq_quantize_q8_0(_ptr(x), m, k, _ptr(d), _ptr(q), _ptr(op), _stream()), "gq_quantize_q8_0")
     return d, q, op
 
@@ -379,7 +380,8 @@ def quantize_q8_0(x: torch.Tensor, mma_operand: bool = False):
 def q1s32_q8_gemm(signs: torch.Tensor, wscale: torch.Tensor, xd: torch.Tensor, xq: torch.Tensor,
                   xq_mma: torch.Tensor | None = None, path: int = PATH_AUTO, out: torch.Tensor | None = None):
     """y [M, N] f32 for 1-bit weights (signs [N, K/32] words, wscale [N, K/32] f32) and Q8_0
-    activations (xd [M, K/32] f16 bits, xq [M, K] int8, optional MMA operand [M, K])."""
+    activations (xd [M, K/32] f16 bits, xq [M, K] int8, optional MMA operand [3, M, K] from
+    quantize_q8_0)."""
     M, K = xq.shape
     N = signs.shape[0]
     if signs.dtype not in (torch.int32, torch.uint32):
@@ -389,7 +391,7 @@ def q1s32_q8_gemm(signs: torch.Tensor, wscale: torch.Tensor, xd: torch.Tensor, x
     _need(xd, torch.int16, M * (K // 32), "xd")
     _need(xq, torch.int8, M * K, "xq")
     if xq_mma is not None:
-        _need(xq_mma, torch.int16, M * K, "xq_mma")
+        _need(xq_mma, torch.int16, 3 * M * K, "xq_mma")
     y = torch.empty((M, N), dtype=torch.float32, device=xq.device) if out is None else out
     _need(y, torch.float32, M * N, "out")
     _check(lib().q1s32_q8_gemm(_ptr(signs), _ptr(wscale), _ptr(xd), _ptr(xq), _ptr(xq_mma), _ptr(y), M, N, K,

@@ -10,6 +10,8 @@
 // one lookup, and eight lookups make S exactly (integer), shared by every weight row of the tile.
 #include "gq_internal.cuh"
 
+#include <cuda_bf16.h>
+
 namespace gq {
 namespace {
 
@@ -32,8 +34,20 @@ quantize_kernel(const float* __restrict__ x, int m, int k, uint16_t* __restrict_
     q[base + lane] = static_cast<int8_t>(qi);
     if (lane == 0) d[gw] = __half_as_ushort(__float2half_rn(dd));
     if (op) {
+        // the MMA operand: pv = f16(d) * q (exact: 11 x 7 significant bits), split exactly into
+        // three bf16 parts hi = bf16(pv), mid = bf16(pv - hi), lo = bf16(pv - hi - mid) (each
+        // rounded to nearest; the subtractions are exact and pv has at most 18 significant bits,
+        // so hi + mid + lo = pv), one plane each, the 32-block's elements interleaved
         const int pos = lane < 16 ? 2 * lane : 2 * (lane - 16) + 1;
-        op[base + pos] = __half_as_ushort(__float2half_rn(static_cast<float>(qi)));   // |qi| <= 127: exact
+        const float pv = __fmul_rn(__half2float(__float2half_rn(dd)), static_cast<float>(qi));
+        const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
+        const float r1 = __fsub_rn(pv, __bfloat162float(hi));
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(r1, __bfloat162float(mid)));
+        const size_t plane = static_cast<size_t>(m) * k;
+        op[base + pos] = __bfloat16_as_ushort(hi);
+        op[plane + base + pos] = __bfloat16_as_ushort(mid);
+        op[2 * plane + base + pos] = __bfloat16_as_ushort(lo);
     }
 }
 

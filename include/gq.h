@@ -303,9 +303,11 @@ int ternary_bitplane_gemv(const uint32_t* P_device, const uint32_t* N_device,
  * scale is f16(d) rounded to nearest even; q = clamp(floor(v) + (v - floor(v) >= 0.5), -127,
  * 127) with v = x / d (round to nearest, the f32 d); amax == 0 gives d = 0 and q = 0.
  *   x_device [m, k] f32; d_device [m, k/32] f16 bits; q_device [m, k] int8 (16-byte aligned);
- *   mma_operand_device: NULL, or [m, k] f16 (16-byte aligned) receiving q as f16 with the
- *   elements of each 32-block interleaved (position 2u <- element u, 2u+1 <- element u+16):
- *   the operand layout q1s32_q8_gemm's MMA path reads.
+ *   mma_operand_device: NULL, or [3, m, k] bf16 (16-byte aligned) receiving the operand
+ *   q1s32_q8_gemm's MMA path reads: pv = f16(d) * q (exact) split into three bf16 parts,
+ *   hi = bf16(pv), mid = bf16(pv - hi), lo = bf16(pv - hi - mid) (each rounded to nearest, so
+ *   hi + mid + lo = pv), plane p at offset p * m * k, with the elements of each 32-block
+ *   interleaved (position 2u <- element u, 2u+1 <- element u+16).
  * Errors: GQ_EINVAL_SHAPE if m or k < 1, k % 32 != 0 or k > 65536; GQ_EINVAL_PTR. */
 int gq_quantize_q8_0(const float* x_device, int m, int k, uint16_t* d_device, int8_t* q_device,
                      uint16_t* mma_operand_device, gq_stream_t stream);
@@ -316,9 +318,11 @@ int gq_quantize_q8_0(const float* x_device, int m, int k, uint16_t* d_device, in
  *   signs_device   [N, K/32] u32, bit t of word b = weight 32b+t, 1 -> +1 (16-byte aligned)
  *   wscale_device  [N, K/32] f32
  *   xd_device      [M, K/32] f16 bits (4-byte aligned), xq_device [M, K] int8 (16-byte aligned)
- *   xq_mma_device  the interleaved f16 operand from gq_quantize_q8_0 (required for
- *                  GQ_PATH_MMA, else may be NULL); it must hold the same q as xq_device, all in
- *                  [-127, 127] (as the quantizer produces)
+ *   xq_mma_device  the three-plane bf16 operand from gq_quantize_q8_0 (required for
+ *                  GQ_PATH_MMA, else may be NULL), made from the same d and q as xd_device and
+ *                  xq_device, all q in [-127, 127] (as the quantizer produces).  The tensor
+ *                  cores form p = f16(d) * S itself: every term and partial sum is a multiple of
+ *                  the ulp of f16(d) below 2^12 f16(d), so its f32 accumulation is exact.
  *   y_device       [M, N] f32 row-major
  *   path: GQ_PATH_LUT4, GQ_PATH_MMA, or GQ_PATH_AUTO (MMA when M >= 64 and the operand is
  *   given, else LUT4).  Both paths are bit-identical to the order above.

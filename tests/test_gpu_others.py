@@ -96,6 +96,12 @@ def _interleave(q: np.ndarray) -> np.ndarray:
     return np.stack([b[:, :, 0, :], b[:, :, 1, :]], axis=-1).reshape(m, k)
 
 
+def _bf16_rn(x: np.ndarray) -> np.ndarray:
+    """Upper 16 bits of f32 values rounded to nearest, ties to even (finite inputs)."""
+    b = x.astype(np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
 @pytest.mark.parametrize("m,k", [(1, 32), (5, 96), (512, 4096)])
 def test_quantize_bit_exact(gq, m, k):
     x = wl.f32_normal(wl.Rng(m + k), m * k).reshape(m, k)
@@ -106,8 +112,14 @@ def test_quantize_bit_exact(gq, m, k):
     dw, qw = oracle.quantize_q8_0(x, m, k)
     assert np.array_equal(d.cpu().numpy().view(np.uint16), dw)
     assert np.array_equal(q.cpu().numpy(), qw)
-    opf = op.cpu().numpy().view(np.float16).astype(np.float32)
-    assert np.array_equal(opf, _interleave(qw.astype(np.float32)))
+    # the MMA operand: three bf16 planes whose sum is f16(d) * q exactly, hi the nearest bf16
+    planes = op.cpu().numpy().view(np.uint16).reshape(3, m, k)
+    pf = (planes.astype(np.uint32) << 16).view(np.float32).astype(np.float64)      # bf16 -> f64, exact
+    dx = np.repeat(dw.view(np.float16).astype(np.float64), 32, axis=1)
+    want = _interleave(dx * qw.astype(np.float64))
+    assert np.array_equal(pf[0] + pf[1] + pf[2], want)
+    assert np.array_equal(planes[0], _bf16_rn(want.astype(np.float32)))
+    assert np.all(np.abs(pf[1]) <= np.abs(pf[0]) * 2.0 ** -8) and np.all(np.abs(pf[2]) <= np.abs(pf[1]) * 2.0 ** -8)
 
 
 # ----------------------------------------------------------------------------- prefill
