@@ -281,6 +281,11 @@ def bench_w1a32(gq, torch, dev, hbm_peak, steps=40, warmup=5):
                        stream) / n
         pre[f"{name}_us"] = round(t * 1e6, 1)
         pre[f"{name}_Glookups_per_s"] = round(M * N * K / 4 / t / 1e9, 1)
+    ws_mma = torch.empty(gq.q1s32_mma_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+    t = time_steps(lambda: gq.q1s32_f32_gemm_mma(copies[0][0], copies[0][1], xp, out=yp, workspace=ws_mma), 10, 3,
+                   stream) / 10
+    pre["mma_us"] = round(t * 1e6, 1)                          # the activation split included
+    pre["mma_bf16_TFLOPs"] = round(3 * 2.0 * M * N * K / t / 1e12, 2)
     return {"w1a32_decode_14336x4096": dec, "w1a32_prefill_512x4096x14336": pre}
 
 

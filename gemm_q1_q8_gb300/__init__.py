@@ -20,7 +20,7 @@ __all__ = [
     "q1_q8_gemm", "ACT_Q8_0", "ACT_F32",
     "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm", "q1s32_f32_gemm",
     "matvec_q8", "matmul_q8", "matmul_q8_mma", "wq_mma_workspace_bytes", "matvec_q4g128", "matmul_q4g128",
-    "matmul_q4g128_mma",
+    "matmul_q4g128_mma", "q1s32_f32_gemm_mma", "q1s32_mma_workspace_bytes",
     "device_error", "version",
 ]
 
@@ -68,6 +68,8 @@ def lib():
             "gq_wq_mma_workspace_bytes": (S, [I, I]),
             "matmul_q8_mma": (I, [P, P, P, P, I, I, I, P, P]),
             "matmul_q4g128_mma": (I, [P, P, P, P, I, I, I, P, P]),
+            "gq_q1s32_mma_workspace_bytes": (S, [I, I]),
+            "q1s32_f32_gemm_mma": (I, [P, P, P, P, I, I, I, P, P]),
             "matvec_q4g128": (I, [P, P, P, P, I, I, P]),
             "matmul_q4g128": (I, [P, P, P, P, I, I, I, P]),
             "q1_q8_gemv_grouped": (I, [P, I, I, P, P]),
@@ -235,6 +237,38 @@ def q1s32_f32_gemm(signs: torch.Tensor, wscale: torch.Tensor, x: torch.Tensor, p
     _need(y, torch.float32, M * N, "out")
     _check(lib().q1s32_f32_gemm(_ptr(signs), _ptr(wscale), _ptr(x), _ptr(y), M, N, K, path, _stream()),
            "q1s32_f32_gemm")
+    return y
+
+
+def q1s32_mma_workspace_bytes(M: int, K: int) -> int:
+    """Bytes of the workspace q1s32_f32_gemm_mma needs for M tokens of K columns (3 * M * K bf16)."""
+    return lib().gq_q1s32_mma_workspace_bytes(M, K)
+
+
+def q1s32_f32_gemm_mma(signs: torch.Tensor, wscale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None):
+    """q1s32_f32_gemm on the tensor cores (x split exactly into three bf16 planes): signs [N, K/32]
+    int32, wscale [N, K/32] f32, x [M, K] f32 -> y [M, N] f32.  workspace: a uint8 CUDA tensor of at
+    least q1s32_mma_workspace_bytes(M, K) bytes (allocated here when None)."""
+    N, nbk = signs.shape
+    M, K = x.shape
+    _need(signs, torch.int32, N * nbk, "signs")
+    _need(wscale, torch.float32, N * nbk, "wscale")
+    _need(x, torch.float32, M * K, "x")
+    if K != 32 * nbk:
+        raise GQError("q1s32_f32_gemm_mma: x has K columns, signs K/32 words per row")
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if out is None else out
+    _need(y, torch.float32, M * N, "out")
+    need = q1s32_mma_workspace_bytes(M, K)
+    if need == 0:
+        raise GQError("q1s32_f32_gemm_mma: invalid shape")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _need(workspace, torch.uint8, workspace.numel(), "workspace")
+    if workspace.numel() < need:
+        raise GQError(f"q1s32_f32_gemm_mma: workspace holds {workspace.numel()} bytes, needs {need}")
+    _check(lib().q1s32_f32_gemm_mma(_ptr(signs), _ptr(wscale), _ptr(x), _ptr(y), M, N, K, _ptr(workspace),
+                                    _stream()), "q1s32_f32_gemm_mma")
     return y
 
 

@@ -5,6 +5,7 @@
 
 #include "gq_internal.cuh"
 #include "wq_mma.cuh"
+#include "w1a32_mma.cuh"
 
 namespace {
 
@@ -152,6 +153,21 @@ int q1s32_f32_gemm(const uint32_t* signs, const float* wscale, const float* x, f
         gq::launch_q1s32_f32(signs, wscale, x, y, M, N, K, path, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t gq_q1s32_mma_workspace_bytes(int M, int K) {
+    if (M < 1 || M > 65535 * 128 || K < 64 || K % 64 != 0 || K > kMaxK) return 0;
+    return gq::w1a32_mma_workspace_bytes(M, K);
+}
+
+int q1s32_f32_gemm_mma(const uint32_t* signs, const float* wscale, const float* x, float* y, int M, int N, int K,
+                       void* workspace, gq_stream_t stream) {
+    if (N < 1 || M < 1 || M > 65535 * 128 || K < 64 || K % 64 != 0 || K > kMaxK) return GQ_EINVAL_SHAPE;
+    if (!signs || !wscale || !x || !y || !workspace) return GQ_EINVAL_PTR;
+    if (!aligned(signs, 16) || !aligned(wscale, 8) || !aligned(x, 4) || !aligned(y, 4) || !aligned(workspace, 16))
+        return GQ_EINVAL_PTR;
+    return cuda_status(
+        gq::launch_w1a32_mma(signs, wscale, x, y, M, N, K, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static int wq_call(int bits, const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
                    gq_stream_t stream) {
     if (N < 1 || T < 1 || T > 65535 * 128 || K < 32 || K % 32 != 0 || K > kMaxK) return GQ_EINVAL_SHAPE;
@@ -224,7 +240,7 @@ int q1s32_q8_gemm(const uint32_t* signs, const float* wscale, const uint16_t* xd
         return GQ_EINVAL_PTR;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (path == GQ_PATH_MMA) {
-        if (!xq_mma || !aligned(xq_mma, 16)) return GQ_EINVAL_PTR;
+        if (!xq_mma || !aligned(xq_mma, 16) || !aligned(wscale, 8)) return GQ_EINVAL_PTR;   // row scales as pairs
         const cudaError_t e = gq::launch_prefill_mma(signs, wscale, xd, xq_mma, y, M, N, K, s);
         if (e == cudaErrorNotSupported) return GQ_EUNSUPPORTED;
         return cuda_status(e);

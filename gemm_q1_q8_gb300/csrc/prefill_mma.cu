@@ -39,6 +39,9 @@
 // is bounded (~1 s); a role that gives up raises an abort flag the others honour, and the block
 // drains its copies and MMAs and frees TMEM before it exits.
 #include "gq_internal.cuh"
+#include "w1a32_mma.cuh"
+
+#include <cuda_bf16.h>
 
 namespace gq {
 GQ_ERROR_ACCESSOR(prefill_mma)
@@ -410,6 +413,45 @@ cudaError_t launch_prefill_mma(const uint32_t* signs, const float* ws, const uin
     const dim3 grid((N + BM - 1) / BM, (M + BN - 1) / BN);
     prefill_mma_kernel<<<grid, kThreads, smem, s>>>(tmB, signs, ws, y, M, N, K);
     return cudaGetLastError();
+}
+
+// x [M, K] f32 -> planes [3][M][K] bf16 in the prefill operand's order: within each 32-block,
+// position 2u <- element u, 2u+1 <- element u+16.  hi = bf16(x), mid = bf16(x - hi),
+// lo = bf16(x - hi - mid), each rounded to nearest (hi + mid + lo = x for normal x).  One thread
+// per pair (u, u+16): a 32-bit store per plane.
+__global__ void split_interleave_kernel(const float* __restrict__ x, uint32_t* __restrict__ planes, size_t pairs) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < pairs;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t blk = i >> 4;                  // 32-block (row-major over M and K/32)
+        const int u = static_cast<int>(i & 15);
+        const float v0 = x[blk * 32 + u], v1 = x[blk * 32 + u + 16];
+        uint32_t part[3][2];
+        const float vv[2] = {v0, v1};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(vv[e]);
+            const float r1 = __fsub_rn(vv[e], __bfloat162float(h));
+            const __nv_bfloat16 md = __float2bfloat16_rn(r1);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(r1, __bfloat162float(md)));
+            part[0][e] = __bfloat16_as_ushort(h);
+            part[1][e] = __bfloat16_as_ushort(md);
+            part[2][e] = __bfloat16_as_ushort(lo);
+        }
+#pragma unroll
+        for (int p = 0; p < kPlanes; ++p) planes[p * pairs + i] = part[p][0] | (part[p][1] << 16);
+    }
+}
+
+size_t w1a32_mma_workspace_bytes(int M, int K) { return static_cast<size_t>(kPlanes) * M * K * 2; }
+
+cudaError_t launch_w1a32_mma(const uint32_t* signs, const float* ws, const float* x, float* y, int M, int N, int K,
+                             void* workspace, cudaStream_t s) {
+    const size_t pairs = static_cast<size_t>(M) * K / 2;
+    split_interleave_kernel<<<static_cast<unsigned>(std::min<size_t>((pairs + 255) / 256, 8192)), 256, 0, s>>>(
+        x, static_cast<uint32_t*>(workspace), pairs);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_prefill_mma(signs, ws, nullptr, static_cast<const uint16_t*>(workspace), y, M, N, K, s);
 }
 
 }  // namespace gq

@@ -206,6 +206,23 @@ int q1_q8_gemv_grouped(const gq_gemv_desc* descs_device, int count, int total_ti
 int q1s32_f32_gemm(const uint32_t* signs_device, const float* wscale_device, const float* x_device,
                    float* y_device, int M, int N, int K, int path, gq_stream_t stream);
 
+/* q1s32_f32_gemm on the tensor cores (the prefill path; same operation and weight arrays).  The
+ * activations are split exactly into three bf16 parts (hi = bf16(x), mid = bf16(x - hi),
+ * lo = bf16(x - hi - mid), each rounded to nearest; hi + mid + lo = x for normal x) in the
+ * workspace; the tensor cores form each 32-block's p = sum_t s * x (the +-1 weights are exact in
+ * bf16), and acc = fma(wscale, p, acc) runs in block order.  The result lies within
+ * c * 2^-24 * sum_b |wscale| * sum_t |x| of the exact value with c = nb + 16 (nb = K/32: one fma
+ * per block, two units for each of the six tensor-core steps of a block, whose f32 accumulation
+ * rounding is not published), and the same inputs give the same bits on every call.
+ *   workspace_device: gq_q1s32_mma_workspace_bytes(M, K) bytes (3 * M * K bf16), 16-byte aligned,
+ *   overwritten; signs_device 16-byte and wscale_device 8-byte aligned; x_device 4-byte aligned.
+ *   Two launches on `stream` (the split, then the prefill MMA kernel).
+ * Errors: GQ_EINVAL_SHAPE unless N >= 1, 1 <= M <= 65535 * 128, 64 <= K <= 65536 and K % 64 == 0;
+ *         GQ_EINVAL_PTR for a NULL or misaligned pointer; GQ_ECUDA. */
+size_t gq_q1s32_mma_workspace_bytes(int M, int K);     /* 0 for an invalid shape */
+int q1s32_f32_gemm_mma(const uint32_t* signs_device, const float* wscale_device, const float* x_device,
+                       float* y_device, int M, int N, int K, void* workspace_device, gq_stream_t stream);
+
 /* Block-quantized weights times f32 activations (web-xpu-ops README: the op table rows
  * matvecQ8 / matmulQ8 and matvecQ4G128 / matmulQ4G128, and "The q4 format"):
  *   matvec_q8 / matmul_q8 (W8A32, per-row scale):
@@ -316,7 +333,7 @@ int gq_quantize_q8_0(const float* x_device, int m, int k, uint16_t* d_device, in
  *     S = sum_t (sign bit ? q : -q) (int8-wrapping negate), p = f16(xd[m,b]) * S (exact),
  *     acc = fma(w_scale[n, b], p, acc) (correctly rounded), acc from +0.
  *   signs_device   [N, K/32] u32, bit t of word b = weight 32b+t, 1 -> +1 (16-byte aligned)
- *   wscale_device  [N, K/32] f32
+ *   wscale_device  [N, K/32] f32 (4-byte aligned; 8-byte aligned for GQ_PATH_MMA)
  *   xd_device      [M, K/32] f16 bits (4-byte aligned), xq_device [M, K] int8 (16-byte aligned)
  *   xq_mma_device  the three-plane bf16 operand from gq_quantize_q8_0 (required for
  *                  GQ_PATH_MMA, else may be NULL), made from the same d and q as xd_device and

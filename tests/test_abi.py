@@ -88,6 +88,10 @@ X = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
     (lambda L: L.matmul_q8_mma(X, X, X, X, 4, 8, 96, N, N), 2),
     (lambda L: L.matmul_q4g128_mma(X, X, X, X, 4, 8, 128, ctypes.c_void_p(0x1008), N), 2),
     (lambda L: L.matmul_q4g128_mma(X, X, X, X, 0, 8, 128, X, N), 1),
+    (lambda L: L.q1s32_f32_gemm_mma(X, X, X, X, 4, 8, 96, X, N), 1),
+    (lambda L: L.q1s32_f32_gemm_mma(X, ctypes.c_void_p(0x1004), X, X, 4, 8, 128, X, N), 2),
+    (lambda L: L.q1s32_f32_gemm_mma(X, X, X, X, 4, 8, 128, N, N), 2),
+    (lambda L: L.q1s32_q8_gemm(X, ctypes.c_void_p(0x1004), X, X, X, X, 8, 8, 128, 3, N), 2),
     (lambda L: L.q1s32_f32_gemm(X, X, X, X, 1, 8, 48, 0, N), 1),
     (lambda L: L.q1s32_f32_gemm(X, X, X, X, 0, 8, 64, 0, N), 1),
     (lambda L: L.q1s32_f32_gemm(X, X, X, X, 1, 0, 64, 0, N), 1),

@@ -191,7 +191,11 @@ def _w1a32_depth(path, M, nbk):
     LUT4 decode (M <= 4, K % 128 == 0): two adds in a table entry, seven between the eight
     lookups, one fma per block of the warp's share (16 per 32-block stage of its K slice, K cut in
     up to eight slices), one add of the two halves, up to seven adds across the slices.
-    LUT4 otherwise: two adds in a table entry, seven between lookups, one fma per block."""
+    LUT4 otherwise: two adds in a table entry, seven between lookups, one fma per block.
+    Tensor cores ("mma"): six tensor-core steps per block (three bf16 parts x two K16 steps, two
+    units each: their accumulation rounding is not published), one fma per block, and slack."""
+    if path == "mma":
+        return nbk + 16
     if path == gqmod.PATH_FMA:
         return 40 + -(-nbk // 32)
     if M <= 4 and nbk % 4 == 0:
@@ -267,3 +271,51 @@ def test_w1a32_prefill_full_size_sampled(gq):
     ms = np.unique(np.concatenate([np.arange(0, M, 37), [31, 32, M - 1]]))
     want = oracle.q1s32_f32_gemv(signs[ns], ws[ns], x[ms], ms.size, ns.size, K)
     _w1a32_check(y[np.ix_(ms, ns)], want, ws[ns], x[ms], gqmod.PATH_LUT4, M)
+
+
+# ---- W1A32 on the tensor cores ---------------------------------------------------------------
+
+def _w1a32_mma(gq, signs, ws, x, **kw):
+    return gq.q1s32_f32_gemm_mma(to_dev(signs.view(np.int32)), to_dev(ws), to_dev(x), **kw).cpu().numpy()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 64), (5, 130, 128), (33, 257, 1024), (129, 300, 4096), (200, 129, 2560),
+                                   (7, 1000, 16384), (130, 128, 64)])
+def test_w1a32_mma_within_bound(gq, M, N, K):
+    """Ragged tokens and rows across the 128 x 128 tile, one to many stages."""
+    signs, ws, x = wl.prefill_inputs(wl.Rng(3000 + M + N + K), M, K, N)
+    _w1a32_check(_w1a32_mma(gq, signs, ws, x), oracle.q1s32_f32_gemv(signs, ws, x, M, N, K), ws, x, "mma", M)
+
+
+@pytest.mark.parametrize("M", [1, 40, 200])
+def test_w1a32_mma_exact_special_case(gq, M):
+    """Integer activations and power-of-two scales: the bf16 split is x itself and every partial
+    sum is exact, so the tensor-core path equals the exact value bit for bit."""
+    N, K = 77, 1024
+    rng = wl.Rng(44 + M)
+    signs = rng.u32(N * K // 32).reshape(N, K // 32)
+    ws = (2.0 ** -(2 + (rng.u32(N * K // 32) % 5).astype(np.int64))).astype(np.float32).reshape(N, K // 32)
+    x = ((rng.u32(M * K) % 17).astype(np.int64) - 8).astype(np.float32).reshape(M, K)
+    assert np.array_equal(_w1a32_mma(gq, signs, ws, x).astype(np.float64), oracle.q1s32_f32_gemv(signs, ws, x, M, N, K))
+
+
+def test_w1a32_mma_deterministic_and_workspace(gq):
+    import torch
+    M, N, K = 150, 700, 2048
+    signs, ws, x = wl.prefill_inputs(wl.Rng(78), M, K, N)
+    dirty = torch.full((gq.q1s32_mma_workspace_bytes(M, K) + 32,), 0x7F, dtype=torch.uint8, device="cuda")
+    a = _w1a32_mma(gq, signs, ws, x, workspace=dirty)
+    b = _w1a32_mma(gq, signs, ws, x)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert gq.device_error() == 0
+
+
+def test_w1a32_mma_full_size_sampled(gq):
+    """M = 512 tokens x 14336 rows x K = 4096 on the tensor cores; sampled rows and tokens."""
+    M, N, K = 512, 14336, 4096
+    signs, ws, x = wl.prefill_inputs(wl.Rng(4), M, K, N)
+    y = _w1a32_mma(gq, signs, ws, x)
+    ns = np.unique(np.concatenate([np.arange(0, N, 997), [127, 128, N - 1]]))
+    ms = np.unique(np.concatenate([np.arange(0, M, 37), [127, 128, M - 1]]))
+    want = oracle.q1s32_f32_gemv(signs[ns], ws[ns], x[ms], ms.size, ns.size, K)
+    _w1a32_check(y[np.ix_(ms, ns)], want, ws[ns], x[ms], "mma", M)
