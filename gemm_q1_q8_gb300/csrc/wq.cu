@@ -208,6 +208,109 @@ wq_gemv_kernel(const uint32_t* __restrict__ w, const float* __restrict__ scale, 
     }
 }
 
+// W4 GEMV for one token: the same bytes in flight per lane as the 8-bit kernel.  A lane takes 32
+// consecutive columns (16 bytes) of a row, so a warp step covers 1024 columns; a thread block
+// covers 48 rows in batches of 16, and warp w takes row half w >> 2 of each batch and the 1024-column chunks (w & 3), (w & 3) + 4, ... of K.  Per
+// (row, chunk) a lane forms the 32-column sum as an even/odd f32 pair (16-term chains), adds the
+// pair and folds it in with one fma by the group scale (32 columns lie in one 128-column group);
+// then the halving exchanges, and a fixed tree of the four chunk phases' partials.
+constexpr int kG4Chunk = 1024;
+constexpr int kG4Rows = 48;                        // rows per thread block, three batches of 16
+__global__ void __launch_bounds__(kGvWarps * 32, 2)   // two blocks per SM: 14,336 rows in one wave
+wq4_gemv1_kernel(const uint32_t* __restrict__ w, const float* __restrict__ scale, const float* __restrict__ x,
+                 float* __restrict__ y, int N, int K) {
+    constexpr int R = kG4Rows;
+    __shared__ float part[4][R];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = warp >> 2, phase = warp & 3;
+    const int n0 = blockIdx.x * R;
+    const size_t wpr = static_cast<size_t>(K) / 8;            // words per row
+    const int G = (K + 127) / 128;
+    const int nchunks = (K + kG4Chunk - 1) / kG4Chunk;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    bool waited = false;
+#pragma unroll 1
+    for (int rb = 0; rb < R; rb += 16) {
+        const int r0 = rb + 8 * half;             // this warp's 8 rows: r0 .. r0 + 7
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int c = phase; c < nchunks; c += 4) {
+            const int k0 = c * kG4Chunk + 32 * lane;
+            if (k0 < K) {                         // K % 32 == 0: a live lane has all 32 columns
+                uint32_t wd[8][4];
+                float sc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int n = min(n0 + r0 + i, N - 1);        // past-the-end rows: computed, not stored
+                    const uint4 a = __ldg(reinterpret_cast<const uint4*>(w + static_cast<size_t>(n) * wpr + k0 / 8));
+                    wd[i][0] = a.x; wd[i][1] = a.y; wd[i][2] = a.z; wd[i][3] = a.w;
+                    sc[i] = __ldg(scale + static_cast<size_t>(n) * G + k0 / 128);
+                }
+                if (!waited) {
+                    asm volatile("griddepcontrol.wait;" ::: "memory");   // the preceding grids are done
+                    waited = true;
+                }
+                const float4* xp = reinterpret_cast<const float4*>(x + k0);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {  // columns 16 hh .. 16 hh + 15
+                    float2 xv[8];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 a = __ldg(xp + 4 * hh + q);
+                        xv[2 * q] = make_float2(a.x, a.y);
+                        xv[2 * q + 1] = make_float2(a.z, a.w);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t wh[2] = {wd[i][2 * hh], wd[i][2 * hh + 1]};
+                        float2 cf[8];
+                        decode16x2<4>(wh, cf);
+                        // the even/odd chains run on over the second 16 columns (the first
+                        // half's pair is parked in the consumed code words)
+                        float2 p = (hh == 0) ? fmul2(cf[0], xv[0])
+                                             : ffma2(cf[0], xv[0], make_float2(__uint_as_float(wd[i][0]),
+                                                                               __uint_as_float(wd[i][1])));
+#pragma unroll
+                        for (int j = 1; j < 8; ++j) p = ffma2(cf[j], xv[j], p);
+                        if (hh == 0) {
+                            wd[i][0] = __float_as_uint(p.x);
+                            wd[i][1] = __float_as_uint(p.y);
+                        } else {
+                            acc[i] = __fmaf_rn(sc[i], __fadd_rn(p.x, p.y), acc[i]);
+                        }
+                    }
+                }
+            }
+        }
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = acc[i];
+        // halving exchanges over lane bits 4, 3, 2, then butterflies over bits 1, 0
+#pragma unroll
+        for (int h = 4, m = 16; h >= 1; h >>= 1, m >>= 1) {
+            const bool hi = (lane & m) != 0;
+#pragma unroll
+            for (int j = 0; j < h; ++j) {
+                const float send = hi ? v[j] : v[j + h];
+                const float keep = hi ? v[j + h] : v[j];
+                v[j] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, m));
+            }
+        }
+#pragma unroll
+        for (int m = 2; m >= 1; m >>= 1) v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], m));
+        if ((lane & 3) == 0) part[phase][r0 + (lane >> 2)] = v[0];
+    }
+    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");   // warps with no chunk
+    __syncthreads();
+    if (threadIdx.x < R) {
+        const int n = n0 + threadIdx.x;
+        if (n < N)
+            y[n] = __fadd_rn(__fadd_rn(part[0][threadIdx.x], part[1][threadIdx.x]),
+                             __fadd_rn(part[2][threadIdx.x], part[3][threadIdx.x]));
+    }
+}
+
 // ------------------------------------------------------------------------------------- GEMM
 
 constexpr int kGmN = 128, kGmT = 128, kGmK = 32;  // tile: rows x tokens x columns per stage
@@ -318,6 +421,18 @@ cudaError_t launch_gemv(const uint32_t* w, const float* scale, const float* x, f
 template <int BITS>
 cudaError_t launch_bits(const uint32_t* w, const float* scale, const float* x, float* y, int T, int N, int K,
                         cudaStream_t s) {
+    if (T == 1 && BITS == 4) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((N + kG4Rows - 1) / kG4Rows);
+        cfg.blockDim = dim3(kGvWarps * 32);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, wq4_gemv1_kernel, w, scale, x, y, N, K);
+    }
     if (T == 1) return launch_gemv<BITS, 1>(w, scale, x, y, N, K, T, s);
     if (T == 2) return launch_gemv<BITS, 2>(w, scale, x, y, N, K, T, s);
     if (T <= 4) return launch_gemv<BITS, 4>(w, scale, x, y, N, K, T, s);
