@@ -203,7 +203,7 @@ block_q8_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants
 // the preceding grids, the activations read and the outputs written after it.
 constexpr int kRwWarps = 8;
 
-// rows per warp: one independent block-sum chain each.  Seven for one token: 94 registers, two
+// rows per warp: one independent block-sum chain each.  Seven for one token: 126 registers, two
 // thread blocks per SM, and for n = 49152 about 2.9 waves of warps (eight rows: 2.5 waves, whose
 // half-empty last wave cost ~8%)
 template <int MT>
