@@ -70,3 +70,15 @@ def test_reference_arm_line():
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "higher_is_better", "cpu_baseline", "e2e"):
         assert key in line
     assert line["value"] > 0 and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_parallel_cpu_baseline():
+    """The parallel CPU baseline runs the unchanged oracle in spawned processes started together and
+    reports all their bytes over the slowest one's time."""
+    sys.path.insert(0, ROOT)
+    import bench
+    r = bench.cpu_baseline_parallel(budget_s=0.5)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s"
+    assert r["cores"] == max(1, min(os.cpu_count() or 1, 64))
+    assert r["value"] > 0 and r["seconds"] >= 0.5
+    assert str(r["cores"]) in r["sample"]
