@@ -118,7 +118,7 @@ __device__ __forceinline__ void act_lane_consts_f32(const float* x, int kg, int 
 // layout), as four f32 pairs (lanes 0-1, 2-3, 4-5, 6-7).
 __device__ __forceinline__ void lane_values(uint32_t w, const uint4& q0, const uint4& q1, const uint4& s0,
                                             const uint4& s1, float2 t[4]) {
-    const int r0 = dp4a_us((w << 1) & 0x02020202u, q0.x, static_cast<int>(s0.x));
+    const int r0 = dp4a_us(__funnelshift_l(0u, w, 1) & 0x02020202u, q0.x, static_cast<int>(s0.x));   // SHF: ALU pipe
     const int r1 = dp4a_us(w & 0x02020202u, q0.y, static_cast<int>(s0.y));
     const int r2 = dp4a_us(w & 0x04040404u, q0.z, static_cast<int>(s0.z));
     const int r3 = dp4a_us(w & 0x08080808u, q0.w, static_cast<int>(s0.w));
