@@ -114,10 +114,10 @@ __device__ __forceinline__ void act_lane_consts_f32(const float* x, int kg, int 
     lane_consts(__half_as_ushort(__float2half_rn(dd)), qw, l, qt, seed, d1s);
 }
 
-// The eight lane values t_l = (sigma_l/2) * s_l of one 32-weight sub-block word (transposed
-// layout), as four f32 pairs (lanes 0-1, 2-3, 4-5, 6-7).
-__device__ __forceinline__ void lane_values(uint32_t w, const uint4& q0, const uint4& q1, const uint4& s0,
-                                            const uint4& s1, float2 t[4]) {
+// The eight dp4a results of one 32-weight sub-block word (transposed layout) read as f32, i.e.
+// 1.5 * 2^23 + (sigma_l/2) * s_l, as four pairs (lanes 0-1, 2-3, 4-5, 6-7).
+__device__ __forceinline__ void lane_words(uint32_t w, const uint4& q0, const uint4& q1, const uint4& s0,
+                                           const uint4& s1, float2 f[4]) {
     const int r0 = dp4a_us(__funnelshift_l(0u, w, 1) & 0x02020202u, q0.x, static_cast<int>(s0.x));   // SHF: ALU pipe
     const int r1 = dp4a_us(w & 0x02020202u, q0.y, static_cast<int>(s0.y));
     const int r2 = dp4a_us(w & 0x04040404u, q0.z, static_cast<int>(s0.z));
@@ -126,11 +126,19 @@ __device__ __forceinline__ void lane_values(uint32_t w, const uint4& q0, const u
     const int r5 = dp4a_us(w & 0x20202020u, q1.y, static_cast<int>(s1.y));
     const int r6 = dp4a_us(w & 0x40404040u, q1.z, static_cast<int>(s1.z));
     const int r7 = dp4a_us(w & 0x80808080u, q1.w, static_cast<int>(s1.w));
+    f[0] = make_float2(__int_as_float(r0), __int_as_float(r1));
+    f[1] = make_float2(__int_as_float(r2), __int_as_float(r3));
+    f[2] = make_float2(__int_as_float(r4), __int_as_float(r5));
+    f[3] = make_float2(__int_as_float(r6), __int_as_float(r7));
+}
+
+// The eight lane values t_l = (sigma_l/2) * s_l (the words minus 1.5 * 2^23, exactly).
+__device__ __forceinline__ void lane_values(uint32_t w, const uint4& q0, const uint4& q1, const uint4& s0,
+                                            const uint4& s1, float2 t[4]) {
+    lane_words(w, q0, q1, s0, s1, t);
     const float2 nm = make_float2(-kMagic, -kMagic);
-    t[0] = fadd2(make_float2(__int_as_float(r0), __int_as_float(r1)), nm);
-    t[1] = fadd2(make_float2(__int_as_float(r2), __int_as_float(r3)), nm);
-    t[2] = fadd2(make_float2(__int_as_float(r4), __int_as_float(r5)), nm);
-    t[3] = fadd2(make_float2(__int_as_float(r6), __int_as_float(r7)), nm);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) t[p] = fadd2(t[p], nm);
 }
 
 __device__ __forceinline__ float final_reduce(const float2 acc[4]) {
@@ -379,17 +387,30 @@ q1_gemv_kernel(GemvArgs a) {
                 const float2 D23 = make_float2(__uint_as_float(dd0.z), __uint_as_float(dd0.w));
                 const float2 D45 = make_float2(__uint_as_float(dd1.x), __uint_as_float(dd1.y));
                 const float2 D67 = make_float2(__uint_as_float(dd1.z), __uint_as_float(dd1.w));
+                // k = 0: ab = D * (F - 1.5*2^23) as one fma, fma(D, F, -(D * 1.5*2^23)): D has at most
+                // 11 significant bits, so -(D * 1.5*2^23) is exact, and the fma returns the exact
+                // D * t (only an exact zero may come out as +0 instead of -0, which no later add can
+                // carry into y, since acc starts at +0).  The four constants serve all rows.
+                float2 N01, N23, N45, N67;
+                if (k == 0) {
+                    const float2 nm = make_float2(-kMagic, -kMagic);
+                    N01 = fmul2(D01, nm);
+                    N23 = fmul2(D23, nm);
+                    N45 = fmul2(D45, nm);
+                    N67 = fmul2(D67, nm);
+                }
 #pragma unroll
                 for (int j = 0; j < kGemvR; ++j) {
                     const uint32_t w = (k == 0) ? wb[j].x : (k == 1) ? wb[j].y : (k == 2) ? wb[j].z : wb[j].w;
                     float2 tv[4];
-                    lane_values(w, q0, q1, s0, s1, tv);
                     if (k == 0) {
-                        ab[j][0] = fmul2(D01, tv[0]);
-                        ab[j][1] = fmul2(D23, tv[1]);
-                        ab[j][2] = fmul2(D45, tv[2]);
-                        ab[j][3] = fmul2(D67, tv[3]);
+                        lane_words(w, q0, q1, s0, s1, tv);
+                        ab[j][0] = ffma2(D01, tv[0], N01);
+                        ab[j][1] = ffma2(D23, tv[1], N23);
+                        ab[j][2] = ffma2(D45, tv[2], N45);
+                        ab[j][3] = ffma2(D67, tv[3], N67);
                     } else {
+                        lane_values(w, q0, q1, s0, s1, tv);
                         ab[j][0] = ffma2(D01, tv[0], ab[j][0]);
                         ab[j][1] = ffma2(D23, tv[1], ab[j][1]);
                         ab[j][2] = ffma2(D45, tv[2], ab[j][2]);
