@@ -365,8 +365,11 @@ q1_gemv_kernel(GemvArgs a) {
             const int s = chunk % kStages;
             if (blk0 > 0 && !wait_chunk(ws, chunk, lane)) return;
             const int nblk = min(kStageBlocks, t.nb - blk0);
-          for (int bb = 0; bb < nblk; ++bb) {   // the stage's blocks, in order
-            const uint8_t* stage = ws.ring[s] + bb * (kTileBits + kTileD0);
+            const uint8_t* ring_s = ws.ring[s];
+#pragma unroll
+          for (int bb = 0; bb < kStageBlocks; ++bb) {   // the stage's blocks, in order
+            if (bb >= nblk) break;                      // (unrolled: the offsets are constants)
+            const uint8_t* stage = ring_s + bb * (kTileBits + kTileD0);
             uint4 wb[kGemvR];
             float d0[kGemvR];
 #pragma unroll
@@ -374,7 +377,7 @@ q1_gemv_kernel(GemvArgs a) {
                 wb[j] = reinterpret_cast<const uint4*>(stage)[lane + 32 * j];
                 d0[j] = f16_to_f32(reinterpret_cast<const uint16_t*>(stage + kTileBits)[lane + 32 * j]);
             }
-            const uint4* cst = reinterpret_cast<const uint4*>(ws.ring[s] + kStageBlocks * (kTileBits + kTileD0) +
+            const uint4* cst = reinterpret_cast<const uint4*>(ring_s + kStageBlocks * (kTileBits + kTileD0) +
                                                               bb * kCstBytes);
 
             float2 ab[kGemvR][4];
