@@ -44,6 +44,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-aligned byte of a dynamic shared-memory array (the launch reserves 1 KB of slack).
+// The __shared__ array itself is offset (its address is not rounded as an integer), so the pointer
+// stays in the shared address space and accesses through it compile to shared-memory loads and
+// stores rather than generic ones with 64-bit address arithmetic.
+__device__ __forceinline__ uint8_t* smem_align1024(uint8_t* p) {
+    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
+
 // --------------------------------------------------------------------------------------------
 // mbarrier + bulk asynchronous copies (the TMA engine, untiled form)
 // --------------------------------------------------------------------------------------------

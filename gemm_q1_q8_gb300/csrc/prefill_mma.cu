@@ -160,7 +160,7 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
                    const float* __restrict__ ws, float* __restrict__ y, int M, int N,
                    int K) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* base = smem_align1024(smem_raw);
     uint8_t* sB = base;                                   // [kStagesM][kPlanes][kTileB]
     Bars* bars = reinterpret_cast<Bars*>(sB + kStagesM * kPlanes * kTileB);
     float* sws = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + ((sizeof(Bars) + 15) & ~size_t(15)));

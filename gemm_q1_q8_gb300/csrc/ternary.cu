@@ -54,7 +54,7 @@ ternary_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ 
                const __grid_constant__ CUtensorMap tmX, int32_t* __restrict__ y, int rows, int k, int batch,
                int rt, int accumulate) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* base = smem_align1024(smem_raw);
     const TernLayout L = tern_layout(rt, batch);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
     int* red = reinterpret_cast<int*>(base + L.red_off);      // [batch][rt]

@@ -232,7 +232,7 @@ lut4_decode_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constan
                    const float* __restrict__ x, float* __restrict__ y, int N, int K, int M, int ks) {
     using L = DecLayout<T>;
     extern __shared__ __align__(1024) uint8_t dsm[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+    uint8_t* base = smem_align1024(dsm);
     FVec<T>* lut = reinterpret_cast<FVec<T>*>(base + L::lut);
     FVec<T>* part = reinterpret_cast<FVec<T>*>(base + L::part);
     FVec<T>* cl = reinterpret_cast<FVec<T>*>(base + L::cl);
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kPdWarps * 32, 1)
 lut4_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmW,
                               const float* __restrict__ x, float* __restrict__ y, int N, int K) {
     extern __shared__ __align__(1024) uint8_t psm1[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(psm1) + 1023) & ~uintptr_t(1023));
+    uint8_t* base = smem_align1024(psm1);
     const int nbk = K / 32;
     const PdLayout L = pd_layout(nbk);
     const int boxes = (nbk + kPdBoxWords - 1) / kPdBoxWords;
