@@ -155,6 +155,34 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     }
 }
 
+// The same for the epilogue warps, which mostly wait on the MMAs: each try carries a suspend-time
+// hint, so a waiting warp sleeps in the barrier unit instead of taking issue slots from the
+// producers and issuers on its SMSP.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool wait_or_abort_sleep(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > 1000000000ull) {
+            report_error(kErrMmaTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)   // 22 warps: at most 80 registers (6 warps on an SMSP)
 prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restrict__ signs,
                    const float* __restrict__ ws, float* __restrict__ y, int M, int N,
@@ -325,7 +353,7 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __re
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) wsr[kk] = wslot[bi * BM + rloc[kk]];
                 // bdone: the block's sums are in its accumulator
-                if (!wait_or_abort(&bars->bdone[accx], static_cast<uint32_t>(b / kAccs) & 1u, abort)) {
+                if (!wait_or_abort_sleep(&bars->bdone[accx], static_cast<uint32_t>(b / kAccs) & 1u, abort)) {
                     ok = false;
                     break;
                 }
