@@ -341,7 +341,7 @@ def bench_prefill(gq, torch, dev, bf16_peak, steps=5, warmup=2, paths=("lut4", "
     tx = torch.from_numpy(x).to(dev)
     d, q, op = gq.quantize_q8_0(tx, mma_operand=True)
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
-    tq = time_steps(lambda: gq.quantize_q8_0(tx, mma_operand=True), 20, 3, stream) / 20
+    tq = time_graph(lambda: gq.quantize_q8_0(tx, mma_operand=True, out=(d, q, op)), 20, 3)   # device time per call
     ops = 2.0 * M * N * K
     res = {"quantize_us": round(tq * 1e6, 2)}
     ids = {"lut4": gq.PATH_LUT4, "mma": gq.PATH_MMA}
@@ -391,8 +391,8 @@ def bench_gemv_shapes(gq, torch, dev, hbm_peak, items, wbytes):
 def extras(gq, torch, dev, hbm_peak, bf16_peak):
     """Secondary kernels, each timed alone (not part of the headline step): block_q8 and ternary
     by CUDA-graph replay of rotating calls (device time), prefill by CUDA events around calls."""
-    out = {"timing": "block_q8, ternary, w1a32 decode, wq matvec: CUDA-graph replay (device time per call); "
-                     "prefill and matmuls: CUDA events per call"}
+    out = {"timing": "block_q8, ternary, w1a32 decode, wq matvec, quantizer: CUDA-graph replay (device time "
+                     "per call); prefill GEMMs and matmuls: CUDA events per call"}
     out.update(bench_block_q8(gq, torch, dev, hbm_peak))
     out.update(bench_ternary(gq, torch, dev, hbm_peak))
     out.update(bench_w1a32(gq, torch, dev, hbm_peak))

@@ -399,14 +399,24 @@ def ternary_bitplane_gemv(P: torch.Tensor, N: torch.Tensor, X: torch.Tensor, out
 
 # ----------------------------------------------------------------------------- prefill
 
-def quantize_q8_0(x: torch.Tensor, mma_operand: bool = False):
+def quantize_q8_0(x: torch.Tensor, mma_operand: bool = False, out=None):
     """(d [m, k/32] f16 bits as int16, q [m, k] int8, operand [3, m, k] bf16 bits or None: the
-    three bf16 parts of f16(d) * q that the prefill MMA path reads)."""
+    three bf16 parts of f16(d) * q that the prefill MMA path reads).  `out` = (d, q, op) reuses
+    caller buffers of those shapes (op None unless mma_operand)."""
     m, k = x.shape
     _need(x, torch.float32, m * k, "x")
-    d = torch.empty((m, k // 32), dtype=torch.int16, device=x.device)
-    q = torch.empty((m, k), dtype=torch.int8, device=x.device)
-    op = torch.empty((3, m, k), dtype=torch.int16, device=x.device) if mma_operand else None
+    if out is None:
+        d = torch.empty((m, k // 32), dtype=torch.int16, device=x.device)
+        q = torch.empty((m, k), dtype=torch.int8, device=x.device)
+        op = torch.empty((3, m, k), dtype=torch.int16, device=x.device) if mma_operand else None
+    else:
+        d, q, op = out
+        _need(d, torch.int16, m * (k // 32), "d")
+        _need(q, torch.int8, m * k, "q")
+        if mma_operand:
+            _need(op, torch.int16, 3 * m * k, "op")
+        else:
+            op = None
     _check(lib().gq_quantize_q8_0(_ptr(x), m, k, _ptr(d), _ptr(q), _ptr(op), _stream()), "gq_quantize_q8_0")
     return d, q, op
 

@@ -16,38 +16,50 @@ namespace gq {
 namespace {
 
 // ----------------------------------------------------------------------------- quantizer
-// One warp per 32-block: amax by shuffles, d = amax/127, q = round-half-up(x/d) clamped.
+// A warp takes kQBlocks consecutive 32-blocks, one value per lane of each, all loaded before any
+// is quantized (one memory round trip per warp instead of one per block); per block: amax by
+// shuffles, d = amax/127, q = round-half-up(x/d) clamped -- every value's arithmetic as before.
+constexpr int kQBlocks = 8;
+
 __global__ void __launch_bounds__(256)
 quantize_kernel(const float* __restrict__ x, int m, int k, uint16_t* __restrict__ d, int8_t* __restrict__ q,
                 uint16_t* __restrict__ op) {
     const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int nbk = k / 32;
-    if (gw >= static_cast<long long>(m) * nbk) return;
-    const size_t base = static_cast<size_t>(gw) * 32;          // row * k + b * 32
-    const float v = x[base + lane];
-    float amax = fabsf(v);
+    const long long nblocks = static_cast<long long>(m) * (k / 32);
+    const long long b0 = gw * kQBlocks;
+    if (b0 >= nblocks) return;                                  // whole warps only
+    float v[kQBlocks];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float dd = q8_0_scale(amax);
-    const int qi = q8_0_quant(v, amax, dd);
-    q[base + lane] = static_cast<int8_t>(qi);
-    if (lane == 0) d[gw] = __half_as_ushort(__float2half_rn(dd));
-    if (op) {
-        // the MMA operand: pv = f16(d) * q (exact: 11 x 7 significant bits), split exactly into
-        // three bf16 parts hi = bf16(pv), mid = bf16(pv - hi), lo = bf16(pv - hi - mid) (each
-        // rounded to nearest; the subtractions are exact and pv has at most 18 significant bits,
-        // so hi + mid + lo = pv), one plane each, the 32-block's elements interleaved
-        const int pos = lane < 16 ? 2 * lane : 2 * (lane - 16) + 1;
-        const float pv = __fmul_rn(__half2float(__float2half_rn(dd)), static_cast<float>(qi));
-        const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
-        const float r1 = __fsub_rn(pv, __bfloat162float(hi));
-        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(r1, __bfloat162float(mid)));
-        const size_t plane = static_cast<size_t>(m) * k;
-        op[base + pos] = __bfloat16_as_ushort(hi);
-        op[plane + base + pos] = __bfloat16_as_ushort(mid);
-        op[2 * plane + base + pos] = __bfloat16_as_ushort(lo);
+    for (int i = 0; i < kQBlocks; ++i)
+        v[i] = (b0 + i < nblocks) ? x[static_cast<size_t>(b0 + i) * 32 + lane] : 0.0f;
+    const size_t plane = static_cast<size_t>(m) * k;
+#pragma unroll
+    for (int i = 0; i < kQBlocks; ++i) {
+        if (b0 + i >= nblocks) break;                           // uniform across the warp
+        const size_t base = static_cast<size_t>(b0 + i) * 32;   // row * k + b * 32
+        float amax = fabsf(v[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float dd = q8_0_scale(amax);
+        const int qi = q8_0_quant(v[i], amax, dd);
+        q[base + lane] = static_cast<int8_t>(qi);
+        if (lane == 0) d[b0 + i] = __half_as_ushort(__float2half_rn(dd));
+        if (op) {
+            // the MMA operand: pv = f16(d) * q (exact: 11 x 7 significant bits), split exactly into
+            // three bf16 parts hi = bf16(pv), mid = bf16(pv - hi), lo = bf16(pv - hi - mid) (each
+            // rounded to nearest; the subtractions are exact and pv has at most 18 significant bits,
+            // so hi + mid + lo = pv), one plane each, the 32-block's elements interleaved
+            const int pos = lane < 16 ? 2 * lane : 2 * (lane - 16) + 1;
+            const float pv = __fmul_rn(__half2float(__float2half_rn(dd)), static_cast<float>(qi));
+            const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
+            const float r1 = __fsub_rn(pv, __bfloat162float(hi));
+            const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(r1, __bfloat162float(mid)));
+            op[base + pos] = __bfloat16_as_ushort(hi);
+            op[plane + base + pos] = __bfloat16_as_ushort(mid);
+            op[2 * plane + base + pos] = __bfloat16_as_ushort(lo);
+        }
     }
 }
 
@@ -125,7 +137,7 @@ prefill_lut4_kernel(const uint32_t* __restrict__ signs, const float* __restrict_
 }  // namespace
 
 cudaError_t launch_quantize(const float* x, int m, int k, uint16_t* d, int8_t* q, uint16_t* op, cudaStream_t s) {
-    const long long warps = static_cast<long long>(m) * (k / 32);
+    const long long warps = (static_cast<long long>(m) * (k / 32) + kQBlocks - 1) / kQBlocks;
     const long long blocks = (warps * 32 + 255) / 256;
     quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(x, m, k, d, q, op);
     return cudaGetLastError();
