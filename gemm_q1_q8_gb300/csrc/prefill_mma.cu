@@ -39,6 +39,7 @@
 // is bounded (~1 s); a role that gives up raises an abort flag the others honour, and the block
 // drains its copies and MMAs and frees TMEM before it exits.
 #include "gq_internal.cuh"
+#include "tc_common.cuh"
 #include "w1a32_mma.cuh"
 
 #include <cuda_bf16.h>
@@ -81,20 +82,7 @@ struct Bars {
     int abort;
 };
 
-// 64-bit shared-memory matrix descriptor: 128-byte swizzle, K-major, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t smem_desc(const void* p) {
-    const uint64_t addr = smem_u32(p);
-    uint64_t d = 0;
-    d |= (addr >> 4) & 0x3FFFull;               // start address
-    d |= static_cast<uint64_t>(1) << 16;        // leading byte offset (unused for swizzled K-major)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;  // stride byte offset: next 8-row group
-    d |= static_cast<uint64_t>(1) << 46;        // descriptor version (sm_100 family)
-    d |= static_cast<uint64_t>(2) << 61;        // layout: 128-byte swizzle
-    return d;
-}
 
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
     asm volatile(
@@ -103,22 +91,6 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
         : "memory");
-}
-// 32 lanes x 32 columns from registers (thread t -> lane t of its warp's quarter)
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
 }
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -139,49 +111,7 @@ __device__ __forceinline__ void tc_ld16x256_x4(uint32_t taddr, float* v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Bounded wait that also gives up when another role has raised the abort flag.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > 1000000000ull) {
-            report_error(kErrMmaTimeout);
-            *abort = 1;
-            return false;
-        }
-    }
-}
 
-// The same for the epilogue warps, which mostly wait on the MMAs: each try carries a suspend-time
-// hint, so a waiting warp sleeps in the barrier unit instead of taking issue slots from the
-// producers and issuers on its SMSP.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool wait_or_abort_sleep(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait_sleep(bar, parity)) return true;
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > 1000000000ull) {
-            report_error(kErrMmaTimeout);
-            *abort = 1;
-            return false;
-        }
-    }
-}
 
 __global__ void __launch_bounds__(kThreads, 1)   // 22 warps: at most 80 registers (6 warps on an SMSP)
 prefill_mma_kernel(const __grid_constant__ CUtensorMap tmB, const uint32_t* __restrict__ signs,
