@@ -357,6 +357,27 @@ def bench_prefill(gq, torch, dev, bf16_peak, steps=5, warmup=2, paths=("lut4", "
     return {"prefill_512x4096x14336": res}
 
 
+def bench_q1_gemm(gq, torch, dev, hbm_peak, cols_list=(4, 64, 512)):
+    """Token-tiled Q1_0 . Q8_0 GEMM (q1_q8_gemm) on a BitNet-2B FFN shape, 6912 x 2560 weights, for
+    `cols` activation vectors, DP4A and LUT4 paths: device time per call by CUDA-graph replay."""
+    rows, n = 6912, 2560
+    rng = wl.Rng(7)
+    w = wl.q1_0_weights(rng, rows, n)
+    packed = gq.q1_0_pack(torch.from_numpy(w).to(dev), rows, n)
+    wbytes = rows * (n // 128) * 18
+    res = {}
+    for cols in cols_list:
+        act = torch.from_numpy(wl.q8_0_acts(rng, cols, n)).to(dev)
+        y = torch.empty((cols, rows), dtype=torch.float32, device=dev)
+        for name, path in (("dp4a", gq.PATH_DP4A), ("lut4", gq.PATH_LUT4)):
+            calls = 20 if cols <= 64 else 3
+            t = time_graph(lambda: gq.q1_q8_gemm(packed, act, rows, n, cols, path=path, out=y), calls, 2, reps=3)
+            res[f"cols{cols}_{name}_us"] = round(t * 1e6, 2)
+            res[f"cols{cols}_{name}_GOPs"] = round(2.0 * rows * n * cols / t / 1e9, 1)
+        res[f"cols{cols}_weight_GBps_best"] = round(wbytes / (min(res[f"cols{cols}_dp4a_us"], res[f"cols{cols}_lut4_us"]) * 1e-6) / 1e9, 1)
+    return {"q1_gemm_6912x2560": res}
+
+
 def bench_gemv_shapes(gq, torch, dev, hbm_peak, items, wbytes):
     """The decode GEMV outside the grouped launch: the 256 x 1024 case per call, and the whole
     BitNet sweep as 210 single-matrix calls captured in one CUDA graph, per token; device time
@@ -396,13 +417,14 @@ def bench_gemv_shapes(gq, torch, dev, hbm_peak, items, wbytes):
 def extras(gq, torch, dev, hbm_peak, bf16_peak):
     """Secondary kernels, each timed alone (not part of the headline step): block_q8 and ternary
     by CUDA-graph replay of rotating calls (device time), prefill by CUDA events around calls."""
-    out = {"timing": "block_q8, ternary, w1a32 decode, wq matvec, quantizer: CUDA-graph replay (device time "
-                     "per call); prefill GEMMs and matmuls: CUDA events per call"}
+    out = {"timing": "block_q8, ternary, w1a32 decode, wq matvec, quantizer, Q1_0 GEMM: CUDA-graph replay "
+                     "(device time per call); prefill GEMMs and matmuls: CUDA events per call"}
     out.update(bench_block_q8(gq, torch, dev, hbm_peak))
     out.update(bench_ternary(gq, torch, dev, hbm_peak))
     out.update(bench_w1a32(gq, torch, dev, hbm_peak))
     out.update(bench_wq(gq, torch, dev, hbm_peak))
     out.update(bench_prefill(gq, torch, dev, bf16_peak))
+    out.update(bench_q1_gemm(gq, torch, dev, hbm_peak))
     return out
 
 
@@ -420,6 +442,8 @@ def run_only(args):
         res = bench_w1a32(gq, torch, dev, hbm_peak, steps=args.steps, warmup=args.warmup)
     elif args.only == "wq":
         res = bench_wq(gq, torch, dev, hbm_peak, steps=args.steps, warmup=args.warmup)
+    elif args.only == "q1_gemm":
+        res = bench_q1_gemm(gq, torch, dev, hbm_peak)
     elif args.only == "prefill_mma":
         res = bench_prefill(gq, torch, dev, bf16_peak, steps=args.steps, warmup=args.warmup, paths=("mma",))
     else:
@@ -641,7 +665,7 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--probe", choices=PROBES, default=None,
                     help="run one kernel three times untimed on its workload (for ncu) and exit")
-    ap.add_argument("--only", choices=["block_q8", "ternary", "w1a32", "wq", "prefill_lut4", "prefill_mma"], default=None,
+    ap.add_argument("--only", choices=["block_q8", "ternary", "w1a32", "wq", "prefill_lut4", "prefill_mma", "q1_gemm"], default=None,
                     help="time one secondary kernel on its workload and print only that")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -469,6 +469,11 @@ q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restri
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = blockIdx.x * 32;
     const int rq = row0 % kTileRows;                                     // rows within their tile
+    // blockIdx.y: the column of a few-token GEMM (its activation and output row); 0 for a GEMV
+    if (blockIdx.y > 0) {
+        act += static_cast<size_t>(blockIdx.y) * nb * 4 * (ACT == GQ_ACT_F32 ? 128 : 34);
+        y += static_cast<size_t>(blockIdx.y) * rows;
+    }
     const uint8_t* tile_base = packed + static_cast<size_t>(row0 / kTileRows) * nb * kChunkBytes;
     // the cta's rows sit in a whole packed tile (packing pads the last tile), so every read below
     // stays inside the packed buffer; rows >= `rows` are computed and not stored
@@ -556,6 +561,7 @@ q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restri
 // built per block by the thread block itself.
 // --------------------------------------------------------------------------------------------
 constexpr int kTok = 4;
+constexpr int kFewTokens = 8;              // DP4A GEMMs up to this many tokens run as per-column GEMVs
 constexpr int kGemmStages = 4;
 
 // LUT4: table[t][k][l][nib] = d1 * s(nib) for the 4 activations of lane l, with the nibble's bit
@@ -813,6 +819,13 @@ cudaError_t launch_q1_gemv_grouped(const gq_gemv_desc* descs, int count, int tot
 
 cudaError_t launch_q1_gemm(const void* packed, const void* act, float* y, int rows, int n, int cols, int path,
                            cudaStream_t s) {
+    if (path == GQ_PATH_DP4A && cols <= kFewTokens) {
+        // a few tokens: each column is a GEMV in the same order, and the single-matrix GEMV kernel
+        // spreads 32-row tiles over the GPU (the 4-token tiles below would leave most SMs idle)
+        q1_gemv_small_kernel<GQ_ACT_Q8_0><<<dim3((rows + 31) / 32, cols), kSmallWarps * 32, 0, s>>>(
+            static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(act), y, rows, n / 128);
+        return cudaGetLastError();
+    }
     const dim3 grid((rows + kTileRows - 1) / kTileRows, (cols + kTok - 1) / kTok);
     if (path == GQ_PATH_LUT4)
         q1_gemm_kernel<GQ_PATH_LUT4><<<grid, 128, 0, s>>>(static_cast<const uint8_t*>(packed),
