@@ -102,6 +102,24 @@ def _bf16_rn(x: np.ndarray) -> np.ndarray:
     return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
 
 
+def test_quantize_out_buffers(gq):
+    """Caller buffers (out=) get the same bits as freshly allocated ones, also when reused for
+    another input (185 blocks: not a multiple of the eight a warp takes)."""
+    import torch
+    m, k = 37, 160
+    bufs = (torch.empty((m, k // 32), dtype=torch.int16, device="cuda"),
+            torch.empty((m, k), dtype=torch.int8, device="cuda"),
+            torch.empty((3, m, k), dtype=torch.int16, device="cuda"))
+    for seed in (1, 2):
+        x = to_dev(wl.f32_normal(wl.Rng(seed), m * k).reshape(m, k))
+        want = gq.quantize_q8_0(x, mma_operand=True)
+        got = gq.quantize_q8_0(x, mma_operand=True, out=bufs)
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+        d_only, q_only, none = gq.quantize_q8_0(x, out=(bufs[0], bufs[1], None))
+        assert none is None and torch.equal(d_only, want[0]) and torch.equal(q_only, want[1])
+
+
 @pytest.mark.parametrize("m,k", [(1, 32), (5, 96), (512, 4096)])
 def test_quantize_bit_exact(gq, m, k):
     x = wl.f32_normal(wl.Rng(m + k), m * k).reshape(m, k)
