@@ -82,3 +82,20 @@ def test_parallel_cpu_baseline():
     assert r["cores"] == max(1, min(os.cpu_count() or 1, 64))
     assert r["value"] > 0 and r["seconds"] >= 0.5
     assert str(r["cores"]) in r["sample"]
+
+
+def test_recorded_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """The DRAM-traffic figure in the bench line comes from the committed record only while the
+    GEMV's sources hash to the value stored with it; any other hash gives null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    current = bench.kernel_hash(*bench.GEMV_SOURCES)
+    assert len(current) == 16
+    rec = tmp_path / "profiles"
+    rec.mkdir()
+    (rec / "t.json").write_text(json.dumps({"kernel_source_hash": current, "dram_bytes_per_launch": 123}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("t.json", current) == 123
+    assert bench.recorded_traffic("t.json", "0" * 16) is None
+    assert bench.recorded_traffic("missing.json", current) is None
+
