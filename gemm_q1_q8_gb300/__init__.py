@@ -21,7 +21,7 @@ __all__ = [
     "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm", "q1s32_f32_gemm",
     "matvec_q8", "matmul_q8", "matmul_q8_mma", "wq_mma_workspace_bytes", "matvec_q4g128", "matmul_q4g128",
     "matmul_q4g128_mma", "q1s32_f32_gemm_mma", "q1s32_mma_workspace_bytes",
-    "device_error", "version",
+    "device_error", "version", "PROBE_KINDS", "probe_fill", "probe_read", "probe_issue", "probe_mma",
 ]
 
 PATH_AUTO, PATH_DP4A, PATH_LUT4, PATH_MMA, PATH_FMA = 0, 1, 2, 3, 4
@@ -78,6 +78,12 @@ def lib():
             "ternary_bitplane_gemv": (I, [P, P, P, P, I, I, I, P]),
             "gq_quantize_q8_0": (I, [P, I, I, P, P, P, P]),
             "q1s32_q8_gemm": (I, [P, P, P, P, P, P, I, I, I, I, P]),
+            "gq_probe_sm_count": (I, []),
+            "gq_probe_fill": (I, [P, S, ctypes.c_uint32, P]),
+            "gq_probe_read": (I, [P, S, P, I, I, P]),
+            "gq_probe_issue": (I, [I, I, P, P, P]),
+            "gq_probe_issue_insts": (ctypes.c_double, [I, I]),
+            "gq_probe_mma": (I, [I, I, I, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -441,3 +447,51 @@ def q1s32_q8_gemm(signs: torch.Tensor, wscale: torch.Tensor, xd: torch.Tensor, x
     _check(lib().q1s32_q8_gemm(_ptr(signs), _ptr(wscale), _ptr(xd), _ptr(xq), _ptr(xq_mma), _ptr(y), M, N, K,
                                path, _stream()), "q1s32_q8_gemm")
     return y
+
+
+# ----------------------------------------------------------------------------- roofline probes
+
+PROBE_KINDS = {
+    "ffma": 0, "ffma2": 1, "fadd2": 2, "fadd": 3, "dp4a": 4, "lop3": 5, "popc": 6, "prmt": 7, "shf": 8,
+    "imad": 9, "shfl": 10, "lds": 11, "dp4a+ffma2": 12, "lds+shfl": 13, "ffma+ffma2": 14, "lop3+dp4a": 15,
+    "fadd+ffma2": 16, "lop3+ffma2": 17,
+}
+PROBE_MMA_F16, PROBE_MMA_F8 = 0, 1
+
+
+def probe_fill(buf: torch.Tensor, seed: int = 1):
+    """Fill a contiguous CUDA tensor (size a multiple of 16 bytes) with a non-zero pattern."""
+    nbytes = buf.numel() * buf.element_size()
+    _check(lib().gq_probe_fill(_ptr(buf), nbytes, seed & 0xFFFFFFFF, _stream()), "gq_probe_fill")
+
+
+def probe_read(buf: torch.Tensor, sink: torch.Tensor, blocks_per_sm: int = 2, threads: int = 1024):
+    """One read-only pass over buf (XOR of everything read folded into the int32 sink)."""
+    _need(sink, torch.int32, 1, "sink")
+    nbytes = buf.numel() * buf.element_size()
+    _check(lib().gq_probe_read(_ptr(buf), nbytes, _ptr(sink), blocks_per_sm, threads, _stream()), "gq_probe_read")
+
+
+def probe_issue(kind: str, iters: int = 2000):
+    """Warp instructions per SM per cycle for one instruction kind (median over the SMs)."""
+    L = lib()
+    sms = L.gq_probe_sm_count()
+    if sms <= 0:
+        raise GQError("probe_issue: no device")
+    cyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k = PROBE_KINDS[kind]
+    _check(L.gq_probe_issue(k, iters, _ptr(cyc), _ptr(sink), _stream()), "gq_probe_issue")
+    c = cyc.cpu().double()
+    return L.gq_probe_issue_insts(k, iters) / float(c.median())
+
+
+def probe_mma(kind: int, n: int, iters: int = 2000):
+    """Dense MMA flops per SM per cycle (median over the SMs) for M = 128, N = n."""
+    L = lib()
+    sms = L.gq_probe_sm_count()
+    cyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    _check(L.gq_probe_mma(kind, n, iters, _ptr(cyc), _stream()), "gq_probe_mma")
+    c = float(cyc.cpu().double().median())
+    k = 16 if kind == PROBE_MMA_F16 else 32
+    return 2.0 * 128 * n * k * iters / c, c / iters

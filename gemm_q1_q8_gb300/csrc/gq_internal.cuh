@@ -33,6 +33,8 @@ __device__ __forceinline__ void report_error(unsigned code) { atomicOr(&g_device
 unsigned error_read_clear_q1();
 unsigned error_read_clear_ternary();
 unsigned error_read_clear_prefill_mma();
+unsigned error_read_clear_w1a32();
+unsigned error_read_clear_probes();
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;

@@ -706,6 +706,8 @@ cudaError_t launch_prefill(const uint32_t* signs, const float* ws, const float* 
 
 }  // namespace
 
+GQ_ERROR_ACCESSOR(w1a32)
+
 cudaError_t launch_q1s32_f32(const uint32_t* signs, const float* ws, const float* x, float* y, int M, int N, int K,
                              int path, cudaStream_t s) {
     if (path == GQ_PATH_LUT4) {

@@ -351,6 +351,79 @@ int q1s32_q8_gemm(const uint32_t* signs_device, const float* wscale_device,
                   const uint16_t* xq_mma_device, float* y_device, int M, int N, int K, int path,
                   gq_stream_t stream);
 
+/* ============================================================================================
+ * Roofline probes (measurement only; no hot-path entry point uses them).  The machine's own
+ * ceilings, measured in the same session as the kernels whose fractions are quoted against them:
+ * roofline.html's read-only bandwidth method (FILL a buffer with a non-zero pattern, then read it
+ * with every load live, best of five after a warm-up) and the web-xpu-ops README's "Performance,
+ * measured against the machine's own ceiling".
+ * ========================================================================================== */
+
+/* Number of SMs of the current device, or -1. */
+int gq_probe_sm_count(void);
+
+/* Writes a non-zero pattern derived from `seed` over `bytes` (a multiple of 16) of buf_device
+ * (16-byte aligned).  One launch on `stream`.
+ * Errors: GQ_EINVAL_SHAPE, GQ_EINVAL_PTR, GQ_ECUDA. */
+int gq_probe_fill(void* buf_device, size_t bytes, uint32_t seed, gq_stream_t stream);
+
+/* One read-only pass over `bytes` of buf_device with 16-byte loads that bypass L1 (eight in
+ * flight per thread, grid-stride over blocks_per_sm x SMs blocks of `threads` threads), XOR of
+ * everything read folded into *sink_device (one u32, 4-byte aligned, which the caller zeroes).
+ * The caller times the launch; bytes / time is the read bandwidth.  Use a buffer several times
+ * the L2 size.  Errors: GQ_EINVAL_SHAPE unless bytes is a positive multiple of 16,
+ * 1 <= blocks_per_sm <= 32 and threads is a multiple of 32 in [32, 1024]; GQ_EINVAL_PTR. */
+int gq_probe_read(const void* buf_device, size_t bytes, uint32_t* sink_device, int blocks_per_sm, int threads,
+                  gq_stream_t stream);
+
+/* Instruction kinds of gq_probe_issue: one kind alone, or two interleaved one to one. */
+enum gq_probe_kind {
+    GQ_PROBE_FFMA = 0,          /* fma.rn.f32                              */
+    GQ_PROBE_FFMA2 = 1,         /* fma.rn.f32x2                            */
+    GQ_PROBE_FADD2 = 2,         /* add.rn.f32x2                            */
+    GQ_PROBE_FADD = 3,          /* add.rn.f32                              */
+    GQ_PROBE_DP4A = 4,          /* dp4a.u32.s32                            */
+    GQ_PROBE_LOP3 = 5,          /* lop3.b32                                */
+    GQ_PROBE_POPC = 6,          /* popc.b32                                */
+    GQ_PROBE_PRMT = 7,          /* prmt.b32                                */
+    GQ_PROBE_SHF = 8,           /* shf.l.wrap.b32                          */
+    GQ_PROBE_IMAD = 9,          /* mad.lo.u32                              */
+    GQ_PROBE_SHFL = 10,         /* shfl.sync.idx.b32                       */
+    GQ_PROBE_LDS = 11,          /* ld.shared.u32, conflict-free (+ one lop3 each) */
+    GQ_PROBE_DP4A_FFMA2 = 12,   /* dp4a and fma.rn.f32x2 interleaved       */
+    GQ_PROBE_LDS_SHFL = 13,     /* ld.shared.u32 and shfl.sync interleaved */
+    GQ_PROBE_FFMA_FFMA2 = 14,   /* fma.rn.f32 and fma.rn.f32x2 interleaved */
+    GQ_PROBE_LOP3_DP4A = 15,    /* lop3 and dp4a interleaved               */
+    GQ_PROBE_FADD_FFMA2 = 16,   /* add.rn.f32 and fma.rn.f32x2 interleaved */
+    GQ_PROBE_LOP3_FFMA2 = 17,   /* lop3 and fma.rn.f32x2 interleaved       */
+    GQ_PROBE_ISSUE_KINDS = 18
+};
+
+/* Instruction issue rate: one block of 32 warps per SM runs `iters` loop iterations of 32
+ * instructions of `kind` per thread on eight independent chains; cycles_device[sm] receives the
+ * block's elapsed SM clock cycles (one u64 per SM, 8-byte aligned); sink_device is one u32 that
+ * keeps the chains live.  Warp instructions per SM per cycle = gq_probe_issue_insts(kind, iters)
+ * / cycles.  Errors: GQ_EINVAL_SHAPE for an unknown kind or iters outside [1, 2^24];
+ * GQ_EINVAL_PTR; GQ_ECUDA. */
+int gq_probe_issue(int kind, int iters, unsigned long long* cycles_device, uint32_t* sink_device,
+                   gq_stream_t stream);
+/* Warp instructions of the measured kind(s) that one block of gq_probe_issue executes. */
+double gq_probe_issue_insts(int kind, int iters);
+
+/* tcgen05 MMA kinds of gq_probe_mma.  There is no int8 kind: ptxas rejects tcgen05.mma
+ * kind::i8 for sm_103a. */
+enum gq_probe_mma_kind {
+    GQ_PROBE_MMA_F16 = 0,       /* kind::f16, bf16 operands, f32 accumulator, K = 16 per MMA  */
+    GQ_PROBE_MMA_F8 = 1         /* kind::f8f6f4, e4m3 operands, f32 accumulator, K = 32       */
+};
+
+/* tcgen05 MMA rate: on every SM one thread issues `iters` MMAs of M = 128, N = n, with both
+ * operands in shared memory, into one TMEM accumulator, then waits (bounded) for them to
+ * complete; cycles_device[sm] receives the SM clock cycles from the first issue to completion.
+ * Flops per MMA = 2 * 128 * n * K.  Errors: GQ_EUNSUPPORTED for another kind; GQ_EINVAL_SHAPE
+ * unless n is a multiple of 16 in [16, 256] and 1 <= iters <= 100000; GQ_EINVAL_PTR; GQ_ECUDA. */
+int gq_probe_mma(int kind, int n, int iters, unsigned long long* cycles_device, gq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -102,6 +102,17 @@ X = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
     (lambda L: L.q1s32_f32_gemm(X, X, X, ctypes.c_void_p(0x1002), 1, 8, 64, 4, N), 2),
     (lambda L: L.gq_q1_0_pack(X, 8, 100, X, N), 1),
     (lambda L: L.gq_q1_0_pack(X, 8, 128, ctypes.c_void_p(0x1004), N), 2),
+    (lambda L: L.gq_probe_fill(X, 24, 1, N), 1),
+    (lambda L: L.gq_probe_fill(ctypes.c_void_p(0x1008), 32, 1, N), 2),
+    (lambda L: L.gq_probe_read(X, 4096, X, 0, 256, N), 1),
+    (lambda L: L.gq_probe_read(X, 4096, X, 2, 100, N), 1),
+    (lambda L: L.gq_probe_read(X, 4096, N, 2, 256, N), 2),
+    (lambda L: L.gq_probe_issue(99, 10, X, X, N), 1),
+    (lambda L: L.gq_probe_issue(0, 0, X, X, N), 1),
+    (lambda L: L.gq_probe_issue(0, 10, ctypes.c_void_p(0x1004), X, N), 2),
+    (lambda L: L.gq_probe_mma(2, 64, 10, X, N), 3),
+    (lambda L: L.gq_probe_mma(0, 24, 10, X, N), 1),
+    (lambda L: L.gq_probe_mma(1, 64, 10, N, N), 2),
 ])
 def test_host_validation_rejects_without_launching(L, call, expect):
     assert call(L) == expect
