@@ -143,9 +143,16 @@ def test_quantize_bit_exact(gq, m, k):
 # ----------------------------------------------------------------------------- prefill
 
 def run_prefill(gq, signs, ws, x, path):
+    """Quantizes x on the GPU and runs the prefill; the GPU's d and q must equal the oracle's
+    quantization of the same x, and the oracle's d and q are what the expected values are built
+    from (no expected value takes an input from the CUDA path)."""
+    M, K = x.shape
     d, q, op = gq.quantize_q8_0(to_dev(x), mma_operand=True)
     y = gq.q1s32_q8_gemm(to_dev(signs), to_dev(ws), d, q, op, path=path)
-    return y.cpu().numpy(), d.cpu().numpy().view(np.uint16), q.cpu().numpy()
+    dw, qw = oracle.quantize_q8_0(x, M, K)
+    assert np.array_equal(d.cpu().numpy().view(np.uint16), dw), "quantizer scales differ from the oracle"
+    assert np.array_equal(q.cpu().numpy(), qw), "quantizer codes differ from the oracle"
+    return y.cpu().numpy(), dw, qw
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1, 64), (5, 130, 128), (33, 257, 1024), (64, 128, 4096)])
@@ -165,6 +172,22 @@ def test_prefill_lut4_full_size_sampled(gq):
     ns = np.sort(rng.choice(N, 96, replace=False))
     want = oracle.prefill_q1s32(signs[ns], ws[ns], d[ms], q[ms], ms.size, ns.size, K)
     assert_same_bits(y[np.ix_(ms, ns)], want, "lut4 full sampled")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 64), (7, 130, 256), (40, 257, 1024)])
+def test_prefill_lut4_caller_codes_with_minus128(gq, M, N, K):
+    """The LUT4 path on caller-supplied Q8_0 codes that include -128 (the page's randomCase draws
+    the byte 0x80 with probability 0.02): a -128 term is -128 whichever the sign bit (the int8
+    wrapping negate), bit for bit as the oracle.  The quantizer never emits -128, so only a caller's
+    own codes reach this rule."""
+    rng = wl.Rng(900 + M + N + K)
+    signs = rng.u32(N * K // 32).reshape(N, K // 32)
+    ws = wl.f32_uniform(rng, N * K // 32, 1e-3, 5e-2).reshape(N, K // 32)
+    xd = wl.f16_page_bits(rng, M * K // 32).reshape(M, K // 32)
+    xq = wl.int8_page(rng, M * K).reshape(M, K)
+    assert np.any(xq == -128)
+    y = gq.q1s32_q8_gemm(to_dev(signs), to_dev(ws), to_dev(xd), to_dev(xq), None, path=gq.PATH_LUT4)
+    assert_same_bits(y.cpu().numpy(), oracle.prefill_q1s32(signs, ws, xd, xq, M, N, K), f"lut4 -128 {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (1, 1, 64), (130, 257, 128), (64, 128, 1024), (300, 200, 4096)])

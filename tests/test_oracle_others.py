@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from tests.exact import f16_value, gamma
+from tests.exact import f16_value, gamma, round_f32
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden", "block_q8_cases.json")
 BQ_CASES = json.load(open(GOLD))["cases"]
@@ -151,6 +151,58 @@ def test_quantize_invariants():
     err = np.abs(qb * d32[..., None].astype(np.float64) - xb)
     assert np.all(err <= d32[..., None] * (0.5 + 1e-6) + 1e-45)
 
+
+
+def _exact_quantize_block(xb):
+    """The stated quantizer, in exact rationals: d = RN_f32(amax / 127); q = round half up of
+    RN_f32(x / d), clamped to [-127, 127]; the stored scale is numpy's RN-even f16 of d."""
+    amax = max(abs(Fraction(float(v))) for v in xb)
+    if amax == 0:
+        return 0, [0] * 32
+    d = round_f32(amax / 127)
+    qs = []
+    for v in xb:
+        vv = Fraction(round_f32(Fraction(float(v)) / Fraction(d)))
+        fl = vv.numerator // vv.denominator
+        qi = fl + (1 if vv - fl >= Fraction(1, 2) else 0)
+        qs.append(max(-127, min(127, qi)))
+    return int(np.array([d], np.float32).astype(np.float16).view(np.uint16)[0]), qs
+
+
+def test_quantize_general_d_exact_rational():
+    """q at a general scale d, against exact rational arithmetic.  Each block holds its amax and
+    values a few ulps either side of (n + 1/2) * d, where the IEEE division x / d and the multiply
+    by a reciprocal x * (1/d) round to different sides of the tie; at least some of those cases must
+    tell the two apart, so a quantizer that multiplied by 1/d (or by 127/amax) fails here."""
+    rng = np.random.default_rng(5)
+    blocks, alt_differs = [], 0
+    for _ in range(24):
+        amax = np.float32(rng.uniform(0.3, 900.0))
+        d = round_f32(Fraction(float(amax)) / 127)
+        inv = round_f32(1 / Fraction(d))
+        xb = [float(amax) * (1 if rng.random() < 0.5 else -1)]
+        while len(xb) < 32:
+            n = int(rng.integers(-126, 126))
+            t = np.float32(round_f32((n + Fraction(1, 2)) * Fraction(d)))
+            for ul in (-2, -1, 0, 1, 2):
+                x = float(np.nextafter(t, np.float32(np.inf * ul), dtype=np.float32)) if ul else float(t)
+                if abs(ul) == 2:
+                    x = float(np.nextafter(np.float32(x), np.float32(np.inf * ul), dtype=np.float32))
+                if len(xb) < 32 and abs(x) <= float(amax):
+                    xb.append(x)
+                    by_div = Fraction(round_f32(Fraction(x) / Fraction(d)))
+                    by_mul = Fraction(round_f32(Fraction(x) * Fraction(inv)))
+                    half_up = [v.numerator // v.denominator + (1 if v - v.numerator // v.denominator >= Fraction(1, 2)
+                                                               else 0) for v in (by_div, by_mul)]
+                    alt_differs += int(half_up[0] != half_up[1])
+        blocks.append(xb)
+    x = np.array(blocks, dtype=np.float32).reshape(1, -1)
+    d, q = oracle.quantize_q8_0(x, 1, x.size)
+    for b, xb in enumerate(blocks):
+        dw, qw = _exact_quantize_block(np.array(xb, np.float32))
+        assert d[0, b] == dw, b
+        assert q[0, 32 * b:32 * b + 32].tolist() == qw, b
+    assert alt_differs > 0
 
 # ----------------------------------------------------------------------------- prefill (Q1_S32 x Q8_0)
 
