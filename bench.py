@@ -176,6 +176,108 @@ def time_graph(fn, calls, warmup, reps=5):
     return start.elapsed_time(end) / 1e3 / (reps * calls)
 
 
+# ----------------------------------------------------------------------------- probes
+def run_probes(gq, torch, dev):
+    """The machine's own ceilings, measured in the same run as the kernels (roofline.html's read-only
+    method: FILL a buffer at least four times the L2 with a non-zero pattern, then read it with every
+    load live, best of five after a warm-up, over a few launch shapes; web-xpu-ops README,
+    "Performance, measured against the machine's own ceiling"): read-only HBM bandwidth, instruction
+    issue rates per SM and cycle for the kinds the kernels lean on, and tcgen05 MMA rates."""
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    l2 = int(getattr(props, "L2_cache_size", 0) or (126 << 20))
+    nbytes = max(4 * l2, 2 << 30) // 4096 * 4096
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    gq.probe_fill(buf, seed=0x5EED)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    shapes = {}
+    for bps, th in ((1, 1024), (2, 1024), (2, 512), (4, 512), (8, 256)):
+        gq.probe_read(buf, sink, bps, th)                   # warm-up
+        best = None
+        for _ in range(5):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            gq.probe_read(buf, sink, bps, th)
+            s1.record()
+            s1.synchronize()
+            ms = s0.elapsed_time(s1)
+            best = ms if best is None else min(best, ms)
+        shapes[f"{bps}x{th}"] = round(nbytes / (best * 1e-3) / 1e9, 1)
+    del buf
+    issue = {k: round(max(gq.probe_issue(k, 2000) for _ in range(2)), 3) for k in gq.PROBE_KINDS}
+    mma = {}
+    for kind, name in ((gq.PROBE_MMA_F16, "f16_bf16"), (gq.PROBE_MMA_F8, "f8f6f4_e4m3")):
+        for n in (16, 64, 256):
+            fl, cpm = gq.probe_mma(kind, n, 2000)
+            mma[f"{name}_n{n}"] = {"flop_per_sm_cycle": round(fl, 1), "cycles_per_mma": round(cpm, 1)}
+    f_hz = 2070e6                                             # the SM clock the per-second figures assume
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(dev.index or 0), "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+        f_hz = float(out.stdout.strip().splitlines()[0]) * 1e6
+    except Exception:
+        pass
+    per_s = lambda wi_per_sm_cycle, lanes=32: wi_per_sm_cycle * lanes * sms * f_hz
+    return {
+        "method": "read: FILL then XOR-reduced 16-byte non-allocating loads over %d MB, best of 5 per launch shape; "
+                  "issue: 32 warps per SM, 8 independent chains per thread, SM clock cycles; mma: one thread per "
+                  "SM issuing M=128 MMAs back to back from shared memory; per-second figures at %.0f MHz"
+                  % (nbytes >> 20, f_hz / 1e6),
+        "hbm_read_GBps": max(shapes.values()), "hbm_read_by_launch_shape": shapes,
+        "issue_warp_inst_per_sm_cycle": issue,
+        "fp32_lane_ops_per_s": per_s(max(issue["ffma"], issue["fadd"])),
+        "popc_per_s": per_s(issue["popc"]), "dp4a_per_s": per_s(issue["dp4a"]),
+        "lds32_lookups_per_s": per_s(issue["lds"]),
+        "mma": mma,
+        "tensor_bf16_flop_per_s": mma["f16_bf16_n256"]["flop_per_sm_cycle"] * sms * f_hz,
+        "tensor_e4m3_flop_per_s": mma["f8f6f4_e4m3_n256"]["flop_per_sm_cycle"] * sms * f_hz,
+        "tcgen05_kind_i8": "not available: ptxas rejects tcgen05.mma kind::i8 for sm_103a",
+        "sm_count": sms, "sm_clock_hz": f_hz,
+    }
+
+
+def add_bounds(kernels, probes):
+    """Each secondary measurement's fraction of its own bound, from the probes of this run."""
+    rd = probes["hbm_read_GBps"]
+    fp = probes["fp32_lane_ops_per_s"]
+    tc = probes["tensor_bf16_flop_per_s"]
+    lk = probes["lds32_lookups_per_s"]
+    for name, e in kernels.items():
+        if not isinstance(e, dict):
+            continue
+        if "weight_GBps" in e:                                   # weight-streaming decode kernels
+            e["bound"] = "hbm_read"
+            e["frac_of_bound"] = round(e["weight_GBps"] / rd, 4)
+        if name == "block_q8_m16":                               # unfused multiply and add per term
+            m, n, k = 16, 49152, 960
+            e["bound"] = "fp32_issue"
+            e["frac_of_bound"] = round(2.0 * m * n * k / (e["us"] * 1e-6) / fp, 4)
+        if name == "ternary_b16":
+            e["bound"] = "popc_issue"
+            e["frac_of_bound"] = round(e["Gpopc_per_s"] * 1e9 / probes["popc_per_s"], 4)
+        if name.startswith("w1a32_decode"):
+            e["bound"] = "hbm_read"
+            e["lut4_frac_of_bound"] = round(e["lut4_weight_GBps"] / rd, 4)
+        if name.startswith("w1a32_prefill"):
+            e["lut4_bound"] = "shared-memory lookups"
+            e["lut4_frac_of_bound"] = round(e["lut4_Glookups_per_s"] * 1e9 / lk, 4)
+            e["mma_bound"] = "tensor (bf16, three planes)"
+            e["mma_frac_of_bound"] = round(e["mma_bf16_TFLOPs"] * 1e12 / tc, 4)
+        if name.startswith("w8a32") or name.startswith("w4a32"):
+            e["matvec_bound"] = "hbm_read"
+            e["matvec_frac_of_bound"] = round(e["matvec_weight_GBps"] / rd, 4)
+            e["matmul512_bound"] = "fp32 fma issue"
+            e["matmul512_frac_of_bound"] = round(e["matmul512_TFLOPs"] * 1e12 / 2 / fp, 4)
+            e["matmul512_mma_bound"] = "tensor (bf16, three planes)"
+            e["matmul512_mma_frac_of_bound"] = round(e["matmul512_mma_bf16_TFLOPs"] * 1e12 / tc, 4)
+        if name.startswith("prefill_"):
+            e["mma_bound"] = "tensor (bf16, three planes)"
+            e["mma_frac_of_bound"] = round(3 * e["mma_GOPs"] * 1e9 / tc, 4)
+        if name.startswith("sweep_") and "weight_GBps" in e:
+            e["frac_of_bound"] = round(e["weight_GBps"] / rd, 4)
+    return kernels
+
+
 # ----------------------------------------------------------------------------- our arm
 def build_sweep(gq, torch, dev):
     """The sweep's matrices, with every activation a slice of one device buffer and every output a
@@ -540,6 +642,7 @@ def run_ours(args, rank, world, dist):
     e2e_value = whole_job_rate(world, wbytes, e2e_steps, te)
 
     khash = kernel_hash(*GEMV_SOURCES)
+    probes = run_probes(gq, torch, dev) if (rank == 0 and not args.no_probes) else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 4), "higher_is_better": True,
@@ -553,7 +656,9 @@ def run_ours(args, rank, world, dist):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peak_src} (hbm_gbs, copy)",
                      "traffic": recorded_traffic("gemv_bitnet_sweep.traffic.json", khash),
-                     "algorithmic_bytes_per_launch": wbytes + abytes + ybytes, "kernel_source_hash": khash},
+                     "algorithmic_bytes_per_launch": wbytes + abytes + ybytes, "kernel_source_hash": khash,
+                     "peak_read": probes["hbm_read_GBps"] if probes else None,
+                     "frac_read": round(achieved / probes["hbm_read_GBps"], 4) if probes else None},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": abytes, "d2h_bytes_per_step": ybytes,
                 "steps": e2e_steps},
         "gpu_launches": 2 * args.steps,     # per step: the activation-constants kernel and the GEMV
@@ -562,9 +667,13 @@ def run_ours(args, rank, world, dist):
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
         line["cpu_baseline_parallel"] = cpu_baseline_parallel(budget_s=max(1.0, args.cpu_seconds / 2))
+    if probes:
+        line["probes"] = probes
     if rank == 0 and not args.no_extras:
         line["kernels"] = extras(gq, torch, dev, hbm_peak, bf16_peak)
         line["kernels"].update(bench_gemv_shapes(gq, torch, dev, hbm_peak, items, wbytes))
+        if probes:
+            add_bounds(line["kernels"], probes)
     if gq.device_error() != 0:
         line["device_error"] = True
     return line
@@ -660,6 +769,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-probes", action="store_true", help="skip the roofline probes (read-only HBM, issue, MMA)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)

@@ -98,11 +98,10 @@ __device__ __forceinline__ void act_lane_consts(const uint16_t* blk, int l, uint
 }
 
 // The same from f32 activations, quantized to Q8_0 on the way (the values gq_quantize_q8_0 would
-// store): lane l of sub-block kg quantizes x[32 kg + 4 l .. + 3]; the sub-block's eight lanes are
-// eight consecutive, 8-aligned lanes of the warp, which exchange their amax.  x is 16-aligned.
-__device__ __forceinline__ void act_lane_consts_f32(const float* x, int kg, int l, uint32_t& qt, uint32_t& seed,
-                                                    float& d1s) {
-    const float4 v = *reinterpret_cast<const float4*>(x + static_cast<size_t>(kg) * 32 + 4 * l);
+// store): lane l of sub-block kg quantizes x[32 kg + 4 l .. + 3] (v, already loaded); the
+// sub-block's eight lanes are eight consecutive, 8-aligned lanes of the warp, which exchange their
+// amax.
+__device__ __forceinline__ void lane_consts_f32(const float4 v, int l, uint32_t& qt, uint32_t& seed, float& d1s) {
     float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -112,6 +111,10 @@ __device__ __forceinline__ void act_lane_consts_f32(const float* x, int kg, int 
                         ((static_cast<uint32_t>(q8_0_quant(v.z, amax, dd)) & 0xFFu) << 16) |
                         (static_cast<uint32_t>(q8_0_quant(v.w, amax, dd)) << 24);
     lane_consts(__half_as_ushort(__float2half_rn(dd)), qw, l, qt, seed, d1s);
+}
+__device__ __forceinline__ void act_lane_consts_f32(const float* x, int kg, int l, uint32_t& qt, uint32_t& seed,
+                                                    float& d1s) {
+    lane_consts_f32(*reinterpret_cast<const float4*>(x + static_cast<size_t>(kg) * 32 + 4 * l), l, qt, seed, d1s);
 }
 
 // The eight dp4a results of one 32-weight sub-block word (transposed layout) read as f32, i.e.
@@ -451,21 +454,30 @@ constexpr size_t kGemvSmem = sizeof(WarpSmem) * kGemvWarps + kCachedDescs * size
 // Decode GEMV for a problem that leaves SMs idle (a single matrix with fewer 128-row tiles than
 // the GPU has SMs): one launch, no workspace.  Only acc = fma(d0, ab, acc) runs in block order;
 // the lane sums ab of different blocks are independent.  A thread block covers 32 rows: its
-// kSmallWarps warps take the blocks in turn (warp w the blocks w, w + 16, ...), each lane one
-// row; a warp builds its block's activation constants itself (one (sub-block, lane) item per
-// lane), reads the rows' 16-byte sign words and d0 directly, and leaves ab and d0 in shared
-// memory; warp 0 then runs each row's chain over the pass's blocks in order.
+// kSmallWarps warps take the blocks in turn (warp w the blocks w, w + 16, ... of each group
+// of 32 or 64), each lane one row; a warp builds its block's activation constants itself (one (sub-block, lane) item per
+// lane), and leaves ab (as [block][lane group][row]) and d0 in shared memory.  Then warp l of the
+// first eight runs the chain of lane group l over the pass's blocks in order for the 32 rows, and
+// at the end warp 0 adds each row's eight chains in the pages' order.
+// The kernel is launched as a programmatic dependent: it lets the next launch on the stream start
+// at once, loads its first weights (which no preceding launch of this library writes) and only
+// then waits for the preceding grids before it reads the activation or writes y.  In a stream of
+// GEMVs (a decode step) the next matrix's weights are in flight while the current one finishes.
 // --------------------------------------------------------------------------------------------
 constexpr int kSmallWarps = 16;
-constexpr int kSmallPass = 32;            // blocks per pass through shared memory (42 KB static)
+constexpr int kSmallPass = 2 * kSmallWarps;   // blocks per pass through shared memory
 
-template <int ACT>   // GQ_ACT_Q8_0 or GQ_ACT_F32
+// J: blocks per warp in a group (2 for rows of at most 32 blocks, which keeps the kernel within 64
+// registers so that two thread blocks share an SM; 4 for longer rows)
+template <int ACT, int J>   // ACT: GQ_ACT_Q8_0 or GQ_ACT_F32
 __global__ void __launch_bounds__(kSmallWarps * 32)
 q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ act, float* __restrict__ y,
                      int rows, int nb) {
-    __shared__ __align__(16) float4 s_ab[kSmallPass][2][32];            // ab of (block, row): two float4
+    __shared__ float s_ab[kSmallPass][8][32];                           // ab of (block, lane group, row)
     __shared__ float s_d0[kSmallPass][32];
     __shared__ __align__(16) uint32_t s_cst[kSmallWarps][4 * kConstWords];  // a warp's current block
+    __shared__ float s_acc[8][32];                                      // the chains' results
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = blockIdx.x * 32;
     const int rq = row0 % kTileRows;                                     // rows within their tile
@@ -477,80 +489,137 @@ q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restri
     const uint8_t* tile_base = packed + static_cast<size_t>(row0 / kTileRows) * nb * kChunkBytes;
     // the cta's rows sit in a whole packed tile (packing pads the last tile), so every read below
     // stays inside the packed buffer; rows >= `rows` are computed and not stored
-    float2 acc[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) acc[p] = make_float2(0.0f, 0.0f);
+    float chain = 0.0f;              // warps 0..7: lane group `warp` of row `lane`
 
-    for (int p0 = 0; p0 < nb; p0 += kSmallPass) {
-        const int np = min(kSmallPass, nb - p0);
-        for (int bl = warp; bl < np; bl += kSmallWarps) {
-            const int b = p0 + bl;
-            const uint8_t* ch = tile_base + static_cast<size_t>(b) * kChunkBytes;
-            const uint4 wb = *reinterpret_cast<const uint4*>(ch + (rq + lane) * 16);
-            const float d0 = f16_to_f32(*reinterpret_cast<const uint16_t*>(ch + kTileRows * 16 + (rq + lane) * 2));
-            {
-                const int k = lane >> 3, l = lane & 7;
-                uint32_t qt, seed;
-                float d1s;
-                if constexpr (ACT == GQ_ACT_F32)
-                    act_lane_consts_f32(reinterpret_cast<const float*>(act), 4 * b + k, l, qt, seed, d1s);
-                else
-                    act_lane_consts(reinterpret_cast<const uint16_t*>(act + static_cast<size_t>(4 * b + k) * 34), l,
-                                    qt, seed, d1s);
-                s_cst[warp][k * kConstWords + l] = qt;
-                s_cst[warp][k * kConstWords + 8 + l] = seed;
-                s_cst[warp][k * kConstWords + 16 + l] = __float_as_uint(d1s);
-            }
-            __syncwarp();
-            const uint4* cst = reinterpret_cast<const uint4*>(s_cst[warp]);
-            float2 ab[4];
+    // groups of up to J * kSmallWarps blocks: warp w owns blocks w + 16 j (j < J) of a group, whose
+    // sign words, d0 and activation items it loads up front; the group then goes through shared
+    // memory in passes of 2 * kSmallWarps blocks
+    constexpr int kGroupBlocks = J * kSmallWarps;
+    for (int g0 = 0; g0 < nb; g0 += kGroupBlocks) {
+        const int ng = min(kGroupBlocks, nb - g0);
+        uint4 wbv[J];
+        uint32_t d0b[J];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint4* cs4 = cst + 6 * k;
-                const uint4 q0 = cs4[0], q1 = cs4[1], s0 = cs4[2], s1 = cs4[3];
-                const uint4 dd0 = cs4[4], dd1 = cs4[5];
-                const float2 D01 = make_float2(__uint_as_float(dd0.x), __uint_as_float(dd0.y));
-                const float2 D23 = make_float2(__uint_as_float(dd0.z), __uint_as_float(dd0.w));
-                const float2 D45 = make_float2(__uint_as_float(dd1.x), __uint_as_float(dd1.y));
-                const float2 D67 = make_float2(__uint_as_float(dd1.z), __uint_as_float(dd1.w));
-                const uint32_t w = (k == 0) ? wb.x : (k == 1) ? wb.y : (k == 2) ? wb.z : wb.w;
-                float2 tv[4];
-                lane_values(w, q0, q1, s0, s1, tv);
-                if (k == 0) {
-                    ab[0] = fmul2(D01, tv[0]);
-                    ab[1] = fmul2(D23, tv[1]);
-                    ab[2] = fmul2(D45, tv[2]);
-                    ab[3] = fmul2(D67, tv[3]);
+        for (int j = 0; j < J; ++j) {
+            const int bl = warp + kSmallWarps * j;
+            if (bl < ng) {
+                const uint8_t* ch = tile_base + static_cast<size_t>(g0 + bl) * kChunkBytes;
+                wbv[j] = *reinterpret_cast<const uint4*>(ch + (rq + lane) * 16);
+                d0b[j] = *reinterpret_cast<const uint16_t*>(ch + kTileRows * 16 + (rq + lane) * 2);
+            }
+        }
+        // the preceding grids' writes (the activation) are visible after this wait
+        if (g0 == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+        // the activation items of the warp's blocks (lane 8k + l: sub-block k, lane l)
+        const int k = lane >> 3, l = lane & 7;
+        float4 xv[J];
+        uint32_t d1raw[J], qwraw[J];
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int bl = warp + kSmallWarps * j;
+            if (bl < ng) {
+                const int kg = 4 * (g0 + bl) + k;
+                if constexpr (ACT == GQ_ACT_F32) {
+                    xv[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(act) +
+                                                             static_cast<size_t>(kg) * 32 + 4 * l);
                 } else {
-                    ab[0] = ffma2(D01, tv[0], ab[0]);
-                    ab[1] = ffma2(D23, tv[1], ab[1]);
-                    ab[2] = ffma2(D45, tv[2], ab[2]);
-                    ab[3] = ffma2(D67, tv[3], ab[3]);
+                    const uint16_t* blk = reinterpret_cast<const uint16_t*>(act + static_cast<size_t>(kg) * 34);
+                    d1raw[j] = blk[0];
+                    qwraw[j] = static_cast<uint32_t>(blk[1 + 2 * l]) | (static_cast<uint32_t>(blk[2 + 2 * l]) << 16);
                 }
             }
-            s_ab[bl][0][lane] = make_float4(ab[0].x, ab[0].y, ab[1].x, ab[1].y);
-            s_ab[bl][1][lane] = make_float4(ab[2].x, ab[2].y, ab[3].x, ab[3].y);
-            s_d0[bl][lane] = d0;
-            __syncwarp();                      // the warp's constants are read before the next block
         }
-        __syncthreads();
-        if (warp == 0) {
-            for (int bl = 0; bl < np; ++bl) {
-                const float d0 = s_d0[bl][lane];
-                const float4 lo = s_ab[bl][0][lane], hi = s_ab[bl][1][lane];
-                const float2 dd = make_float2(d0, d0);
-                acc[0] = ffma2(dd, make_float2(lo.x, lo.y), acc[0]);
-                acc[1] = ffma2(dd, make_float2(lo.z, lo.w), acc[1]);
-                acc[2] = ffma2(dd, make_float2(hi.x, hi.y), acc[2]);
-                acc[3] = ffma2(dd, make_float2(hi.z, hi.w), acc[3]);
+#pragma unroll
+        for (int half = 0; half < J / 2; ++half) {
+            const int p0 = half * kSmallPass;              // first block of the pass, within the group
+            if (p0 >= ng) break;
+            const int np = min(kSmallPass, ng - p0);
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * half + jj;
+                const int bl = warp + kSmallWarps * jj;     // block of the pass
+                if (bl >= np) break;
+                {
+                    uint32_t qt, seed;
+                    float d1s;
+                    if constexpr (ACT == GQ_ACT_F32)
+                        lane_consts_f32(xv[j], l, qt, seed, d1s);
+                    else
+                        lane_consts(d1raw[j], qwraw[j], l, qt, seed, d1s);
+                    s_cst[warp][k * kConstWords + l] = qt;
+                    s_cst[warp][k * kConstWords + 8 + l] = seed;
+                    s_cst[warp][k * kConstWords + 16 + l] = __float_as_uint(d1s);
+                }
+                __syncwarp();
+                const uint4 wb = wbv[j];
+                const uint4* cst = reinterpret_cast<const uint4*>(s_cst[warp]);
+                float2 ab[4];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint4* cs4 = cst + 6 * kk;
+                    const uint4 q0 = cs4[0], q1 = cs4[1], s0 = cs4[2], s1 = cs4[3];
+                    const uint4 dd0 = cs4[4], dd1 = cs4[5];
+                    const float2 D01 = make_float2(__uint_as_float(dd0.x), __uint_as_float(dd0.y));
+                    const float2 D23 = make_float2(__uint_as_float(dd0.z), __uint_as_float(dd0.w));
+                    const float2 D45 = make_float2(__uint_as_float(dd1.x), __uint_as_float(dd1.y));
+                    const float2 D67 = make_float2(__uint_as_float(dd1.z), __uint_as_float(dd1.w));
+                    const uint32_t w = (kk == 0) ? wb.x : (kk == 1) ? wb.y : (kk == 2) ? wb.z : wb.w;
+                    float2 tv[4];
+                    lane_values(w, q0, q1, s0, s1, tv);
+                    if (kk == 0) {
+                        ab[0] = fmul2(D01, tv[0]);
+                        ab[1] = fmul2(D23, tv[1]);
+                        ab[2] = fmul2(D45, tv[2]);
+                        ab[3] = fmul2(D67, tv[3]);
+                    } else {
+                        ab[0] = ffma2(D01, tv[0], ab[0]);
+                        ab[1] = ffma2(D23, tv[1], ab[1]);
+                        ab[2] = ffma2(D45, tv[2], ab[2]);
+                        ab[3] = ffma2(D67, tv[3], ab[3]);
+                    }
+                }
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    s_ab[bl][2 * p][lane] = ab[p].x;
+                    s_ab[bl][2 * p + 1][lane] = ab[p].y;
+                }
+                s_d0[bl][lane] = f16_to_f32(d0b[j]);
+                __syncwarp();                      // the warp's constants are read before the next block
             }
+            __syncthreads();
+            if (warp < 8) {
+#pragma unroll 8
+                for (int bl = 0; bl < np; ++bl) chain = __fmaf_rn(s_d0[bl][lane], s_ab[bl][warp][lane], chain);
+            }
+            __syncthreads();                       // the pass is consumed before the next overwrites it
         }
-        __syncthreads();                       // the pass is consumed before the next overwrites it
     }
+    if (warp < 8) s_acc[warp][lane] = chain;
+    __syncthreads();
     if (warp == 0) {
         const int row = row0 + lane;
-        if (row < rows) y[row] = final_reduce(acc);
+        // ((a0 + a4) + (a2 + a6)) + ((a1 + a5) + (a3 + a7))
+        const float lo = __fadd_rn(__fadd_rn(s_acc[0][lane], s_acc[4][lane]), __fadd_rn(s_acc[2][lane], s_acc[6][lane]));
+        const float hi = __fadd_rn(__fadd_rn(s_acc[1][lane], s_acc[5][lane]), __fadd_rn(s_acc[3][lane], s_acc[7][lane]));
+        if (row < rows) y[row] = __fadd_rn(lo, hi);
     }
+}
+
+// Launches `kernel` as a programmatic dependent of the work before it on `s` (the kernel itself
+// waits with griddepcontrol.wait before it depends on that work).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 // --------------------------------------------------------------------------------------------
@@ -786,13 +855,17 @@ cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int ro
     }
     if (tiles < sm_cached[dev]) {
         // fewer tiles than SMs: the block-parallel kernel (one launch, no workspace)
+        const dim3 grid((rows + 31) / 32), block(kSmallWarps * 32);
+        const uint8_t* pw = static_cast<const uint8_t*>(packed);
+        const uint8_t* pa = static_cast<const uint8_t*>(act);
+        const int nb = n / 128;
         if (act_format == GQ_ACT_F32)
-            q1_gemv_small_kernel<GQ_ACT_F32><<<(rows + 31) / 32, kSmallWarps * 32, 0, s>>>(
-                static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(act), y, rows, n / 128);
-        else
-            q1_gemv_small_kernel<GQ_ACT_Q8_0><<<(rows + 31) / 32, kSmallWarps * 32, 0, s>>>(
-                static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(act), y, rows, n / 128);
-        return cudaGetLastError();
+            return nb <= kSmallPass
+                       ? launch_dependent(q1_gemv_small_kernel<GQ_ACT_F32, 2>, grid, block, s, pw, pa, y, rows, nb)
+                       : launch_dependent(q1_gemv_small_kernel<GQ_ACT_F32, 4>, grid, block, s, pw, pa, y, rows, nb);
+        return nb <= kSmallPass
+                   ? launch_dependent(q1_gemv_small_kernel<GQ_ACT_Q8_0, 2>, grid, block, s, pw, pa, y, rows, nb)
+                   : launch_dependent(q1_gemv_small_kernel<GQ_ACT_Q8_0, 4>, grid, block, s, pw, pa, y, rows, nb);
     }
     int grid = 0, active = 0;
     cudaError_t e = gemv_grid(tiles, &grid, &active);
@@ -822,9 +895,13 @@ cudaError_t launch_q1_gemm(const void* packed, const void* act, float* y, int ro
     if (path == GQ_PATH_DP4A && cols <= kFewTokens) {
         // a few tokens: each column is a GEMV in the same order, and the single-matrix GEMV kernel
         // spreads 32-row tiles over the GPU (the 4-token tiles below would leave most SMs idle)
-        q1_gemv_small_kernel<GQ_ACT_Q8_0><<<dim3((rows + 31) / 32, cols), kSmallWarps * 32, 0, s>>>(
-            static_cast<const uint8_t*>(packed), static_cast<const uint8_t*>(act), y, rows, n / 128);
-        return cudaGetLastError();
+        const dim3 grid((rows + 31) / 32, cols), block(kSmallWarps * 32);
+        const uint8_t* pw = static_cast<const uint8_t*>(packed);
+        const uint8_t* pa = static_cast<const uint8_t*>(act);
+        const int nb = n / 128;
+        return nb <= kSmallPass
+                   ? launch_dependent(q1_gemv_small_kernel<GQ_ACT_Q8_0, 2>, grid, block, s, pw, pa, y, rows, nb)
+                   : launch_dependent(q1_gemv_small_kernel<GQ_ACT_Q8_0, 4>, grid, block, s, pw, pa, y, rows, nb);
     }
     const dim3 grid((rows + kTileRows - 1) / kTileRows, (cols + kTok - 1) / kTok);
     if (path == GQ_PATH_LUT4)
