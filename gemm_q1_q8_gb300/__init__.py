@@ -17,6 +17,7 @@ from . import build as _build
 __all__ = [
     "lib", "GQError", "PATH_AUTO", "PATH_DP4A", "PATH_LUT4", "PATH_MMA", "PATH_FMA",
     "q1_0_packed_bytes", "q1_0_pack", "q1_q8_gemv", "q1_q8_gemv_f32", "q1_q8_gemv_noalloc", "GroupedGemv",
+    "q1_q8_gemv_raw", "pack_q8_0",
     "q1_q8_gemm", "ACT_Q8_0", "ACT_F32",
     "block_q8_matmul_nt", "ternary_bitplane_gemv", "quantize_q8_0", "q1s32_q8_gemm", "q1s32_f32_gemm",
     "matvec_q8", "matmul_q8", "matmul_q8_mma", "wq_mma_workspace_bytes", "matvec_q4g128", "matmul_q4g128",
@@ -61,6 +62,8 @@ def lib():
             "q1_q8_gemv": (I, [P, P, P, I, I, P, P]),
             "q1_q8_gemv_noalloc": (I, [P, P, P, I, I, P]),
             "q1_q8_gemv_f32": (I, [P, P, P, I, I, P, P]),
+            "q1_q8_gemv_raw": (I, [P, P, P, I, I, P]),
+            "gq_pack_q8_0": (I, [P, I, I, P, P, P]),
             "gq_gemv_group_plan": (I, [P, I, P]),
             "q1s32_f32_gemm": (I, [P, P, P, P, I, I, I, I, P]),
             "matvec_q8": (I, [P, P, P, P, I, I, P]),
@@ -161,6 +164,27 @@ def q1_q8_gemv(packed: torch.Tensor, act: torch.Tensor, rows: int, n: int, out: 
     _need(ws, torch.uint8, workspace_bytes(n), "workspace")
     _check(lib().q1_q8_gemv(_ptr(packed), _ptr(act), _ptr(y), rows, n, _ptr(ws), _stream()), "q1_q8_gemv")
     return y
+
+
+def q1_q8_gemv_raw(w: torch.Tensor, act: torch.Tensor, rows: int, n: int, out: torch.Tensor | None = None):
+    """y[r] for a rows x n Q1_0 matrix in the pages' own 18-byte blocks (uint8, no repack) and one
+    Q8_0 vector (uint8, n/32*34 bytes)."""
+    _need(w, torch.uint8, rows * (n // 128) * 18 if n % 128 == 0 else -1, "w")
+    _need(act, torch.uint8, (n // 32) * 34, "act")
+    y = torch.empty(rows, dtype=torch.float32, device=act.device) if out is None else out
+    _need(y, torch.float32, rows, "out")
+    _check(lib().q1_q8_gemv_raw(_ptr(w), _ptr(act), _ptr(y), rows, n, _stream()), "q1_q8_gemv_raw")
+    return y
+
+
+def pack_q8_0(raw: torch.Tensor, cols: int, n: int):
+    """The pages' packQ8: `cols` Q8_0 vectors (uint8, cols*n/32*34 bytes) -> (d f32 [cols, n/32],
+    q int32 [cols, n/32, 8], the quant bytes four to a little-endian word)."""
+    _need(raw, torch.uint8, cols * (n // 32) * 34 if n % 32 == 0 else -1, "raw")
+    d = torch.empty((cols, n // 32), dtype=torch.float32, device=raw.device)
+    q = torch.empty((cols, n // 32, 8), dtype=torch.int32, device=raw.device)
+    _check(lib().gq_pack_q8_0(_ptr(raw), cols, n, _ptr(d), _ptr(q), _stream()), "gq_pack_q8_0")
+    return d, q
 
 
 def q1_q8_gemv_f32(packed: torch.Tensor, x: torch.Tensor, rows: int, n: int, out: torch.Tensor | None = None,

@@ -85,6 +85,18 @@ int q1_q8_gemv(const void* packed_w, const void* act, float* y, int rows, int n,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int q1_q8_gemv_raw(const void* w_q1_0, const void* act, float* y, int rows, int n, gq_stream_t stream) {
+    if (rows < 1 || n < 128 || n % 128 != 0 || n > gq::kMaxN) return GQ_EINVAL_SHAPE;
+    if (!w_q1_0 || !act || !y || !aligned(w_q1_0, 2) || !aligned(act, 2) || !aligned(y, 4)) return GQ_EINVAL_PTR;
+    return cuda_status(gq::launch_q1_gemv_raw(w_q1_0, act, y, rows, n, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int gq_pack_q8_0(const void* raw_q8_0, int cols, int n, float* d, uint32_t* q, gq_stream_t stream) {
+    if (cols < 1 || n < 32 || n % 32 != 0 || n > gq::kMaxN) return GQ_EINVAL_SHAPE;
+    if (!raw_q8_0 || !d || !q || !aligned(raw_q8_0, 2) || !aligned(d, 4) || !aligned(q, 4)) return GQ_EINVAL_PTR;
+    return cuda_status(gq::launch_pack_q8_0(raw_q8_0, cols, n, d, q, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int q1_q8_gemv_f32(const void* packed_w, const float* x, float* y, int rows, int n, void* workspace,
                    gq_stream_t stream) {
     const int st = check_q1(packed_w, x, y, rows, n);

@@ -177,6 +177,8 @@ cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int ro
 size_t gemv_workspace_bytes(int n);
 cudaError_t launch_q1s32_f32(const uint32_t* signs, const float* ws, const float* x, float* y, int M, int N, int K,
                              int path, cudaStream_t s);   // path: GQ_PATH_FMA or GQ_PATH_LUT4
+cudaError_t launch_q1_gemv_raw(const void* w, const void* act, float* y, int rows, int n, cudaStream_t s);
+cudaError_t launch_pack_q8_0(const void* raw, int cols, int n, float* d, uint32_t* q, cudaStream_t s);
 cudaError_t launch_q1_gemv_grouped(const gq_gemv_desc* descs, int count, int total_tiles, int* counter,
                                    cudaStream_t s);
 int gemv_tiles_for(int rows);

@@ -131,6 +131,28 @@ enum gq_act_format {
 int q1_q8_gemv_f32(const void* packed_w_device, const float* x_device, float* y_device, int rows, int n,
                    void* workspace_device, gq_stream_t stream);
 
+/* Decode GEMV on the pages' own bytes, with no repack of the weights ([P1] Q1_DOT_WGSL reads the
+ * 18-byte Q1_0 blocks as stored): the same result as gq_q1_0_pack followed by q1_q8_gemv, bit for
+ * bit, for callers that keep their weights in the pages' layout.  Slower than the resident layout
+ * (its sign bits are looked up by nibble in tables of the block's exact products d1 * s, built per
+ * thread block and 32 rows).
+ *   w_q1_0_device: rows * (n/128) * 18 bytes, the pages' AoS blocks, row-major, 2-byte aligned;
+ *   act_device: n/32 Q8_0 blocks (34 bytes), 2-byte aligned; y_device: rows f32, 4-byte aligned.
+ *   One launch on `stream`; no workspace.
+ * Errors: GQ_EINVAL_SHAPE if rows < 1, n < 128, n % 128 != 0 or n > 2^20; GQ_EINVAL_PTR for a
+ * NULL or misaligned pointer; GQ_ECUDA. */
+int q1_q8_gemv_raw(const void* w_q1_0_device, const void* act_device, float* y_device, int rows, int n,
+                   gq_stream_t stream);
+
+/* [P1] packQ8: `cols` activation vectors of n values, each n/32 Q8_0 blocks of 34 bytes (vector
+ * after vector, 2-byte aligned), repacked into d_device[c * n/32 + b] = the block's f16 scale as f32
+ * (exact) and q_device[(c * n/32 + b) * 8 + v] = its quant bytes 4v..4v+3 as one little-endian word
+ * (both 4-byte aligned).  The library's GEMV and GEMM read the 34-byte blocks directly; this is the
+ * pages' layout for callers that keep activations in it.
+ * Errors: GQ_EINVAL_SHAPE if cols < 1, n < 32, n % 32 != 0 or n > 2^20; GQ_EINVAL_PTR; GQ_ECUDA. */
+int gq_pack_q8_0(const void* raw_q8_0_device, int cols, int n, float* d_device, uint32_t* q_device,
+                 gq_stream_t stream);
+
 /* Largest n that q1_q8_gemv_noalloc accepts. */
 #define GQ_NOALLOC_MAX_N 16384
 

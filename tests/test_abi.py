@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for must in ("q1_q8_gemv", "q1_q8_gemm", "block_q8_matmul_nt", "ternary_bitplane_gemv",
-                 "gq_q1_0_pack", "q1_q8_gemv_grouped", "gq_quantize_q8_0", "q1s32_q8_gemm"):
+                 "gq_q1_0_pack", "q1_q8_gemv_grouped", "gq_quantize_q8_0", "q1s32_q8_gemm", "q1_q8_gemv_raw",
+                 "gq_pack_q8_0"):
         assert must in names
 
 
@@ -102,6 +103,13 @@ X = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
     (lambda L: L.q1s32_f32_gemm(X, X, X, ctypes.c_void_p(0x1002), 1, 8, 64, 4, N), 2),
     (lambda L: L.gq_q1_0_pack(X, 8, 100, X, N), 1),
     (lambda L: L.gq_q1_0_pack(X, 8, 128, ctypes.c_void_p(0x1004), N), 2),
+    (lambda L: L.q1_q8_gemv_raw(X, X, X, 0, 1024, N), 1),
+    (lambda L: L.q1_q8_gemv_raw(X, X, X, 8, 1000, N), 1),
+    (lambda L: L.q1_q8_gemv_raw(ctypes.c_void_p(0x1001), X, X, 8, 1024, N), 2),
+    (lambda L: L.q1_q8_gemv_raw(X, X, ctypes.c_void_p(0x1002), 8, 1024, N), 2),
+    (lambda L: L.gq_pack_q8_0(X, 1, 48, X, X, N), 1),
+    (lambda L: L.gq_pack_q8_0(X, 0, 64, X, X, N), 1),
+    (lambda L: L.gq_pack_q8_0(X, 1, 64, N, X, N), 2),
     (lambda L: L.gq_probe_fill(X, 24, 1, N), 1),
     (lambda L: L.gq_probe_fill(ctypes.c_void_p(0x1008), 32, 1, N), 2),
     (lambda L: L.gq_probe_read(X, 4096, X, 0, 256, N), 1),

@@ -232,3 +232,49 @@ def test_grouped_mixed_activation_formats(gq):
     g()
     for (_, _, y, rows, n), wv in zip(items, want):
         assert_same_bits(y.cpu().numpy(), wv, f"grouped mixed {rows}x{n}")
+
+
+# ----------------------------------------------------------------------------- the pages' own bytes
+
+@pytest.mark.parametrize("rows,n,dist,seed", [
+    (1, 128, "page", 40),
+    (33, 1024, "uniform", 41),        # one 8-block step
+    (300, 2560, "page", 42),          # ragged rows (300 = 9 x 32 + 12), 20 blocks: a ragged last step
+    (257, 1152, "page", 43),          # 9 blocks: a one-block last step
+    (1000, 6912, "uniform", 44),
+])
+def test_gemv_raw_bit_exact(gq, rows, n, dist, seed):
+    """q1_q8_gemv_raw reads the 18-byte Q1_0 blocks as stored (no repack): the oracle's bits, and
+    the same bits as the resident-layout GEMV."""
+    rng = wl.Rng(2000 + seed)
+    w = wl.q1_0_weights(rng, rows, n, scales=dist)
+    a = wl.q8_0_acts(rng, 1, n, scales=dist, quants=dist)
+    y = gq.q1_q8_gemv_raw(to_dev(w), to_dev(a), rows, n).cpu().numpy()
+    assert_same_bits(y, oracle.q1_q8_gemv(w, a, rows, n), f"raw {rows}x{n} {dist}")
+    assert_same_bits(y, gemv(gq, w, a, rows, n), f"raw vs packed {rows}x{n}")
+
+
+def test_gemv_raw_degenerate(gq):
+    """Every quant -128 and zero scales on the raw path."""
+    rows, n = 64, 512
+    rng = wl.Rng(78)
+    w = wl.q1_0_weights(rng, rows, n)
+    a = wl.q8_0_acts(rng, 1, n).reshape(-1, 34).copy()
+    a[:, 2:] = 0x80
+    a[::3, 0:2] = 0
+    a = a.reshape(-1)
+    y = gq.q1_q8_gemv_raw(to_dev(w), to_dev(a), rows, n).cpu().numpy()
+    assert_same_bits(y, oracle.q1_q8_gemv(w, a, rows, n), "raw degenerate")
+
+
+@pytest.mark.parametrize("cols,n", [(1, 32), (3, 2560), (5, 96)])
+def test_pack_q8_0_layout(gq, cols, n):
+    """packQ8: per 32-block the f16 scale decoded to f32 and the 32 quant bytes as eight
+    little-endian words; the expected arrays are the input bytes viewed through numpy."""
+    a = wl.q8_0_acts(wl.Rng(90 + cols), cols, n, scales="page", quants="page")
+    d, q = gq.pack_q8_0(to_dev(a), cols, n)
+    blocks = a.reshape(cols * n // 32, 34)
+    want_d = blocks[:, :2].copy().view(np.float16).astype(np.float32).reshape(cols, n // 32)
+    want_q = blocks[:, 2:].copy().view("<u4").reshape(cols, n // 32, 8)
+    assert np.array_equal(d.cpu().numpy().view(np.uint32), want_d.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy().view(np.uint32), want_q)
