@@ -554,7 +554,7 @@ def run_only(args):
 
 
 PROBES = ("lut4_decode", "lut4_prefill", "wq8_gemv", "wq4_gemv", "wq8_gemm", "wq4_gemm", "wq8_mma", "wq4_mma",
-          "bq8_m1", "bq8_m4")
+          "bq8_m1", "bq8_m4", "q1_gemm512_lut4", "q1_gemm512_dp4a", "q1_gemv_2560x6912")
 
 
 def run_probe(name):
@@ -563,7 +563,17 @@ def run_probe(name):
     import torch
     import gemm_q1_q8_gb300 as gq
     N, K = 14336, 4096
-    if name.startswith("bq8"):
+    if name.startswith("q1_"):
+        # the Q1_0 GEMM on a BitNet-2B FFN shape (6912 x 2560, 512 tokens), or one single-matrix GEMV
+        rows, n = (6912, 2560) if name.startswith("q1_gemm") else (2560, 6912)
+        cols = 512 if name.startswith("q1_gemm") else 1
+        rng = wl.Rng(7)
+        packed = gq.q1_0_pack(torch.from_numpy(wl.q1_0_weights(rng, rows, n)).cuda(), rows, n)
+        act = torch.from_numpy(wl.q8_0_acts(rng, cols, n)).cuda()
+        path = gq.PATH_LUT4 if name.endswith("lut4") else gq.PATH_DP4A
+        f = (lambda: gq.q1_q8_gemm(packed, act, rows, n, cols, path=path)) if cols > 1 else \
+            (lambda: gq.q1_q8_gemv(packed, act, rows, n))
+    elif name.startswith("bq8"):
         m = int(name[-1])
         x, q, sc = wl.block_q8_inputs(wl.Rng(20), m, 960, 49152)
         x, q, sc = (torch.from_numpy(a).cuda() for a in (x, q.view(np.int32), sc))
