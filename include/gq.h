@@ -14,6 +14,11 @@
  *    an error, not a dropped tail.
  *  - After GQ_ECUDA, gq_last_cuda_error() returns the cudaError_t of the failed launch (per
  *    calling thread).
+ *  - Decode kernels are launched as programmatic dependents of the work before them on the stream:
+ *    they may start, and read their weights, before that work has finished, and they wait for it
+ *    before they read an activation or write an output.  Weights must therefore not be written by
+ *    the immediately preceding launch on the stream if that launch signals programmatic completion
+ *    early (no launch of this library writes weights; an ordinary kernel or copy is waited for).
  *  - Kernels wait on nothing but their own asynchronous copies, and every such wait is bounded
  *    (about one second).  A wait that runs out sets a device-side error word and the kernel
  *    returns; gq_device_error() reads and clears it.
@@ -163,7 +168,8 @@ int gq_pack_q8_0(const void* raw_q8_0_device, int cols, int n, float* d_device, 
  * until the process exits).  The pages describe no such variant.
  *   Arguments as q1_q8_gemv without the workspace; n <= GQ_NOALLOC_MAX_N.
  *   The first call on each device looks up that block's address (cudaGetSymbolAddress, with the
- *   device current): make that first call before any stream capture on the device.
+ *   device current) and keeps it: make that first call before any stream capture on the device,
+ *   and do not reset the device (cudaDeviceReset) between calls.
  *   Every call shares the block, so calls whose work overlaps on the GPU (other streams, other
  *   host threads) race: issue them one after another.  The call itself clears what must start
  *   at zero.  It calls no allocator (no cudaMalloc / cudaFree, no library that allocates).
