@@ -666,7 +666,10 @@ q1_gemm_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ a
     __shared__ __align__(128) uint8_t ring[kGemmStages][kChunkBytes];
     __shared__ uint64_t bars[kGemmStages];
     // per token and sub-block: DP4A constants (24 words) or LUT4 tables (8 x 16 floats)
-    constexpr int kPerTokK = (kPath == GQ_PATH_LUT4) ? 128 : kConstWords;
+    // LUT4: eight tables of 16 entries, 17 words apart, so that the 32 builders of a token (one
+    // (sub-block, lane) table each) store to distinct banks; a lookup reads 16 words of one table
+    constexpr int kLutStride = 17;
+    constexpr int kPerTokK = (kPath == GQ_PATH_LUT4) ? 8 * kLutStride : kConstWords;
     __shared__ __align__(16) uint32_t tabs[2][kTok][4][kPerTokK];
 
     const int nb = n / 128;
@@ -701,7 +704,7 @@ q1_gemm_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ a
             const int c = min(c0 + t, cols - 1);
             const uint16_t* blk = reinterpret_cast<const uint16_t*>(act + c * act_bytes + static_cast<size_t>(4 * i + k) * 34);
             if (kPath == GQ_PATH_LUT4) {
-                lut_table(blk, l, reinterpret_cast<float*>(&tabs[buf][t][k][l * 16]));
+                lut_table(blk, l, reinterpret_cast<float*>(&tabs[buf][t][k][l * kLutStride]));
             } else {
                 uint32_t qt, seed;
                 float d1s;
@@ -746,8 +749,8 @@ q1_gemm_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ a
                     const float* tb = reinterpret_cast<const float*>(&tabs[buf][t][k][0]);
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
-                        const float2 v = make_float2(tb[(2 * p) * 16 + lane_nibble(w, 2 * p)],
-                                                     tb[(2 * p + 1) * 16 + lane_nibble(w, 2 * p + 1)]);
+                        const float2 v = make_float2(tb[(2 * p) * kLutStride + lane_nibble(w, 2 * p)],
+                                                     tb[(2 * p + 1) * kLutStride + lane_nibble(w, 2 * p + 1)]);
                         ab[p] = (k == 0) ? v : fadd2(v, ab[p]);
                     }
                 } else {
