@@ -456,9 +456,11 @@ constexpr size_t kGemvSmem = sizeof(WarpSmem) * kGemvWarps + kCachedDescs * size
 // the lane sums ab of different blocks are independent.  A thread block covers 32 rows: its
 // kSmallWarps warps take the blocks in turn (warp w the blocks w, w + 16, ... of each group
 // of 32 or 64), each lane one row; a warp builds its block's activation constants itself (one (sub-block, lane) item per
-// lane), and leaves ab (as [block][lane group][row]) and d0 in shared memory.  Then warp l of the
-// first eight runs the chain of lane group l over the pass's blocks in order for the 32 rows, and
-// at the end warp 0 adds each row's eight chains in the pages' order.
+// lane), and leaves ab (two float4 per row: lane groups 0-3 and 4-7) and d0 in shared memory.
+// Then warps 0 and 1 run the chains of lane groups 0-3 and 4-7 over the pass's blocks in order for
+// the 32 rows, and at the end warp 0 adds each row's eight chains in the pages' order.  (Eight
+// chain warps reading scalars cut one launch's latency no further and cost ~15% more instructions
+// per thread block, which launches of several waves -- a few-token GEMM -- pay in full.)
 // The kernel is launched as a programmatic dependent: it lets the next launch on the stream start
 // at once, loads its first weights (which no preceding launch of this library writes) and only
 // then waits for the preceding grids before it reads the activation or writes y.  In a stream of
@@ -473,7 +475,7 @@ template <int ACT, int J>   // ACT: GQ_ACT_Q8_0 or GQ_ACT_F32
 __global__ void __launch_bounds__(kSmallWarps * 32)
 q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ act, float* __restrict__ y,
                      int rows, int nb) {
-    __shared__ float s_ab[kSmallPass][8][32];                           // ab of (block, lane group, row)
+    __shared__ __align__(16) float4 s_ab[kSmallPass][2][32];            // ab of (block, row): two float4
     __shared__ float s_d0[kSmallPass][32];
     __shared__ __align__(16) uint32_t s_cst[kSmallWarps][4 * kConstWords];  // a warp's current block
     __shared__ float s_acc[8][32];                                      // the chains' results
@@ -489,7 +491,7 @@ q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restri
     const uint8_t* tile_base = packed + static_cast<size_t>(row0 / kTileRows) * nb * kChunkBytes;
     // the cta's rows sit in a whole packed tile (packing pads the last tile), so every read below
     // stays inside the packed buffer; rows >= `rows` are computed and not stored
-    float chain = 0.0f;              // warps 0..7: lane group `warp` of row `lane`
+    float4 chain = make_float4(0.0f, 0.0f, 0.0f, 0.0f);   // warps 0, 1: lane groups 4w..4w+3 of row `lane`
 
     // groups of up to J * kSmallWarps blocks: warp w owns blocks w + 16 j (j < J) of a group, whose
     // sign words, d0 and activation items it loads up front; the group then goes through shared
@@ -578,23 +580,32 @@ q1_gemv_small_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restri
                         ab[3] = ffma2(D67, tv[3], ab[3]);
                     }
                 }
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    s_ab[bl][2 * p][lane] = ab[p].x;
-                    s_ab[bl][2 * p + 1][lane] = ab[p].y;
-                }
+                s_ab[bl][0][lane] = make_float4(ab[0].x, ab[0].y, ab[1].x, ab[1].y);
+                s_ab[bl][1][lane] = make_float4(ab[2].x, ab[2].y, ab[3].x, ab[3].y);
                 s_d0[bl][lane] = f16_to_f32(d0b[j]);
                 __syncwarp();                      // the warp's constants are read before the next block
             }
             __syncthreads();
-            if (warp < 8) {
-#pragma unroll 8
-                for (int bl = 0; bl < np; ++bl) chain = __fmaf_rn(s_d0[bl][lane], s_ab[bl][warp][lane], chain);
+            if (warp < 2) {
+#pragma unroll 4
+                for (int bl = 0; bl < np; ++bl) {
+                    const float d0 = s_d0[bl][lane];
+                    const float4 v = s_ab[bl][warp][lane];
+                    chain.x = __fmaf_rn(d0, v.x, chain.x);
+                    chain.y = __fmaf_rn(d0, v.y, chain.y);
+                    chain.z = __fmaf_rn(d0, v.z, chain.z);
+                    chain.w = __fmaf_rn(d0, v.w, chain.w);
+                }
             }
             __syncthreads();                       // the pass is consumed before the next overwrites it
         }
     }
-    if (warp < 8) s_acc[warp][lane] = chain;
+    if (warp < 2) {
+        s_acc[4 * warp][lane] = chain.x;
+        s_acc[4 * warp + 1][lane] = chain.y;
+        s_acc[4 * warp + 2][lane] = chain.z;
+        s_acc[4 * warp + 3][lane] = chain.w;
+    }
     __syncthreads();
     if (warp == 0) {
         const int row = row0 + lane;
