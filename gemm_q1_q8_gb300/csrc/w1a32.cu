@@ -339,11 +339,14 @@ lut4_decode_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constan
     // the other blocks leave: nothing reads their shared memory
 }
 
-// Decode of one token, persistent: one thread block per SM builds the tables of all of K once (the
-// activation is the same for every row), then takes 32-row tiles in turn.  A tile's sign words and
-// scales come by TMA (four 128-byte-wide boxes of 32 rows each, 128B swizzle) into a three-stage
-// ring, two tiles ahead of the one being summed.  The sixteen warps split a tile's blocks (warp w
-// the blocks w*nb/16 ...), each lane one row; the warps' partial sums are added in a fixed tree.
+// Decode of one token, persistent: one thread block per SM takes 32-row tiles in turn.  A tile's
+// sign words and scales come by TMA (four 128-byte-wide boxes of 32 rows each, 128B swizzle) into a
+// three-stage ring, two tiles ahead of the one being summed.  The sixteen warps split a tile's
+// blocks (warp w the blocks w*nb/16 ...), each lane one row, and each warp builds the tables of its
+// own blocks only (the activation is the same for every row), so no warp waits for another before
+// its first tile.  The warps' partial sums are added in a fixed tree.  When a block has at most
+// three tiles (the usual case), each tile keeps its own stage and partial-sum slot and the block
+// meets at a barrier only once, at the end.
 // Launched as a programmatic dependent: the first tiles' copies are requested before the wait for
 // the preceding grids, the activations (tables) read and the outputs written after it.
 constexpr int kPdWarps = 16;
@@ -362,9 +365,22 @@ __host__ __device__ inline PdLayout pd_layout(int nbk) {
     L.lut = kPdStages * stage;
     L.part = L.lut + static_cast<uint32_t>(nbk) * 8u * kDecTab * 4u;
     L.part = (L.part + 15u) & ~15u;
-    L.bar = L.part + kPdWarps * 32u * 4u;
+    L.bar = L.part + kPdStages * kPdWarps * 32u * 4u;                   // one partial-sum slot per stage
     L.bytes = L.bar + kPdStages * 8u;
     return L;
+}
+
+// The warps' partial sums of one 32-row tile, added in a fixed tree, then stored.
+__device__ __forceinline__ void pd_reduce_store(const float* part, int t, int lane, float* y, int N) {
+    float v[kPdWarps];
+#pragma unroll
+    for (int w2 = 0; w2 < kPdWarps; ++w2) v[w2] = part[w2 * 32 + lane];
+#pragma unroll
+    for (int h = kPdWarps / 2; h >= 1; h >>= 1)
+#pragma unroll
+        for (int w2 = 0; w2 < h; ++w2) v[w2] = __fadd_rn(v[w2], v[w2 + h]);
+    const int n = t * 32 + lane;
+    if (n < N) y[n] = v[0];
 }
 
 __global__ void __launch_bounds__(kPdWarps * 32, 1)
@@ -377,10 +393,15 @@ lut4_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmS, const __g
     const int boxes = (nbk + kPdBoxWords - 1) / kPdBoxWords;
     const uint32_t half = static_cast<uint32_t>(boxes) * 32u * 128u;    // bytes of one tensor in a stage
     float* lut = reinterpret_cast<float*>(base + L.lut);                 // [block][group][kDecTab]
-    float* part = reinterpret_cast<float*>(base + L.part);               // [warp][lane]
+    float* part = reinterpret_cast<float*>(base + L.part);               // [stage][warp][lane]
     uint64_t* full = reinterpret_cast<uint64_t*>(base + L.bar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles = (N + 31) / 32;
+    const int my_tiles = (tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                         static_cast<int>(gridDim.x);
+    // every tile of this block has its own stage and partial-sum slot: no block-wide barrier until
+    // the end (the usual case: 14,336 rows are 448 tiles, at most three per block)
+    const bool oneshot = my_tiles <= kPdStages;
 
     auto issue = [&](int t, int s) {              // thread 0: tile t into stage s
         mbar_arrive_expect_tx(&full[s], 2u * half);
@@ -404,36 +425,43 @@ lut4_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmS, const __g
             }
         }
     }
+    __syncthreads();                                         // the barriers are initialised
     asm volatile("griddepcontrol.wait;" ::: "memory");       // the preceding grids are done
-    // the tables of all K: one (block, group) per item
-    for (int it = threadIdx.x; it < nbk * 8; it += blockDim.x) {
-        const int j = it >> 3, g = it & 7;
+    // whole 16-byte chunks (four blocks) per warp: nbk is a multiple of 4 (K % 128 == 0)
+    const int per = ((nbk + kPdWarps - 1) / kPdWarps + 3) & ~3;
+    const int jlo = warp * per, cnt = max(0, min(per, nbk - jlo));
+    // each warp builds the tables of its own blocks (no other warp reads them): one (block, group) per item
+    for (int it = lane; it < cnt * 8; it += 32) {
+        const int j = jlo + (it >> 3), g = it & 7;
         const float4 a = ldg_x4(x, 0, K, j, g);
         const float p0 = -(a.x + a.y), p1 = a.x - a.y;
         const float q0 = -(a.z + a.w), q1 = a.z - a.w;
         const float p[4] = {p0, p1, -p1, -p0};
         const float qq[4] = {q0, q1, -q1, -q0};
-        float* dst = lut + static_cast<size_t>(it) * kDecTab;
+        float* dst = lut + static_cast<size_t>(j * 8 + g) * kDecTab;
 #pragma unroll
         for (int i = 0; i < 16; ++i) dst[i] = __fadd_rn(p[i & 3], qq[i >> 2]);
     }
-    __syncthreads();
+    __syncwarp();
 
-    // whole 16-byte chunks (four blocks) per warp: nbk is a multiple of 4 (K % 128 == 0)
-    const int per = ((nbk + kPdWarps - 1) / kPdWarps + 3) & ~3;
-    const int jlo = warp * per, cnt = max(0, min(per, nbk - jlo));
     int i = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
         const int s = i % kPdStages;
-        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>(i / kPdStages) & 1u);
-        if (__syncthreads_or(!ok)) {
-            if (threadIdx.x == 0) report_error(kErrWaitTimeout);
-            break;
+        bool ok;
+        if (oneshot) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(i / kPdStages) & 1u));
+            if (!ok && lane == 0) report_error(kErrWaitTimeout);
+        } else {
+            ok = mbar_wait(&full[s], static_cast<uint32_t>(i / kPdStages) & 1u);
+            if (__syncthreads_or(!ok)) {
+                if (threadIdx.x == 0) report_error(kErrWaitTimeout);
+                break;
+            }
         }
         const uint8_t* sig = base + L.ring + s * 2u * half;
         const uint8_t* scl = sig + half;
         float acc = 0.0f;
-        for (int j4 = jlo; j4 < jlo + cnt; j4 += 4) {
+        for (int j4 = jlo; ok && j4 < jlo + cnt; j4 += 4) {
             // four blocks' words and scales: one 16-byte chunk of the lane's row in each (swizzled)
             const uint32_t off = static_cast<uint32_t>(j4 / kPdBoxWords) * 4096u + static_cast<uint32_t>(lane) * 128u +
                                  ((static_cast<uint32_t>((j4 % kPdBoxWords) >> 2) ^ static_cast<uint32_t>(lane & 7)) << 4);
@@ -451,28 +479,29 @@ lut4_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmS, const __g
                 acc = __fmaf_rn(sv[k4], S, acc);
             }
         }
+        if (oneshot) {
+            part[(s * kPdWarps + warp) * 32 + lane] = acc;
+            continue;
+        }
         part[warp * 32 + lane] = acc;
         __syncthreads();
-        if (warp == 0) {
-            float v[kPdWarps];
-#pragma unroll
-            for (int w2 = 0; w2 < kPdWarps; ++w2) v[w2] = part[w2 * 32 + lane];
-#pragma unroll
-            for (int h = kPdWarps / 2; h >= 1; h >>= 1)
-#pragma unroll
-                for (int w2 = 0; w2 < h; ++w2) v[w2] = __fadd_rn(v[w2], v[w2 + h]);
-            const int n = t * 32 + lane;
-            if (n < N) y[n] = v[0];
-        }
+        if (warp == 0) pd_reduce_store(part, t, lane, y, N);
         __syncthreads();                          // stage s and the partial sums are free
         if (threadIdx.x == 0 && t + kPdStages * static_cast<int>(gridDim.x) < tiles) {
             issue(t + kPdStages * gridDim.x, s);
             ++issued;
         }
     }
+    if (oneshot) {
+        __syncthreads();
+        if (warp < my_tiles)                      // warp w adds tile w's partial sums
+            pd_reduce_store(part + warp * kPdWarps * 32, static_cast<int>(blockIdx.x) + warp * static_cast<int>(gridDim.x),
+                            lane, y, N);
+    }
     if (threadIdx.x == 0) {
         // after an early exit, copies still in flight land before shared memory is released
-        for (int j = i; j < issued; ++j)
+        // (in the one-shot case every stage was used once, and a completed phase is seen at once)
+        for (int j = oneshot ? 0 : i; j < issued; ++j)
             if (!mbar_wait(&full[j % kPdStages], static_cast<uint32_t>(j / kPdStages) & 1u))
                 report_error(kErrDrainTimeout);
     }

@@ -276,6 +276,7 @@ def test_w1a32_exact_special_case(gq, path, M):
 @pytest.mark.parametrize("M,N,K", [(1, 1, 32), (1, 33, 96), (2, 130, 1024), (3, 300, 8224), (4, 64, 4096),
                                    (1, 200, 16384), (3, 129, 2560), (1, 14336, 4096), (1, 1000, 1152),
                                    (1, 33, 128), (1, 500, 5120), (1, 70, 5248),
+                                   (1, 20000, 1024),   # more than three 32-row tiles per block
                                    (5, 257, 160), (16, 513, 1056), (33, 300, 4128), (70, 1000, 512)])
 def test_w1a32_within_bound(gq, path, M, N, K):
     signs, ws, x = wl.prefill_inputs(wl.Rng(M + N + K), M, K, N)
