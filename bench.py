@@ -206,8 +206,9 @@ def run_probes(gq, torch, dev):
     del buf
     issue = {k: round(max(gq.probe_issue(k, 2000) for _ in range(2)), 3) for k in gq.PROBE_KINDS}
     mma = {}
-    for kind, name in ((gq.PROBE_MMA_F16, "f16_bf16"), (gq.PROBE_MMA_F8, "f8f6f4_e4m3")):
-        for n in (16, 64, 256):
+    for kind, name in ((gq.PROBE_MMA_F16, "f16_bf16"), (gq.PROBE_MMA_F8, "f8f6f4_e4m3"),
+                       (gq.PROBE_MMA_F16_TMEM_A, "f16_bf16_tmem_a")):
+        for n in (16, 64, 128, 256):
             fl, cpm = gq.probe_mma(kind, n, 2000)
             mma[f"{name}_n{n}"] = {"flop_per_sm_cycle": round(fl, 1), "cycles_per_mma": round(cpm, 1)}
     f_hz = 2070e6                                             # the SM clock the per-second figures assume

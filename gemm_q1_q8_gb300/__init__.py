@@ -480,7 +480,7 @@ PROBE_KINDS = {
     "imad": 9, "shfl": 10, "lds": 11, "dp4a+ffma2": 12, "lds+shfl": 13, "ffma+ffma2": 14, "lop3+dp4a": 15,
     "fadd+ffma2": 16, "lop3+ffma2": 17,
 }
-PROBE_MMA_F16, PROBE_MMA_F8 = 0, 1
+PROBE_MMA_F16, PROBE_MMA_F8, PROBE_MMA_F16_TMEM_A = 0, 1, 2
 
 
 def probe_fill(buf: torch.Tensor, seed: int = 1):
@@ -517,5 +517,5 @@ def probe_mma(kind: int, n: int, iters: int = 2000):
     cyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
     _check(L.gq_probe_mma(kind, n, iters, _ptr(cyc), _stream()), "gq_probe_mma")
     c = float(cyc.cpu().double().median())
-    k = 16 if kind == PROBE_MMA_F16 else 32
+    k = 32 if kind == PROBE_MMA_F8 else 16
     return 2.0 * 128 * n * k * iters / c, c / iters

@@ -203,7 +203,7 @@ cudaError_t launch_issue(int grid, int iters, unsigned long long* cycles, uint32
 // tcgen05 MMA rates
 // ------------------------------------------------------------------------------------------------
 constexpr int kMmaSmem = 160 * 1024;       // one block per SM (TMEM columns and a clean clock)
-constexpr int kMmaTmemCols = 256;
+constexpr int kMmaTmemCols = 512;          // the accumulator (N <= 256) and, for one kind, A
 
 struct MmaProbeBars {
     uint64_t done;
@@ -213,7 +213,14 @@ struct MmaProbeBars {
 template <int KIND>
 __device__ __forceinline__ void probe_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate) {
-    if (KIND == GQ_PROBE_MMA_F16) {
+    if (KIND == GQ_PROBE_MMA_F16_TMEM_A) {
+        // A from tensor memory: a_desc carries its TMEM address
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(static_cast<uint32_t>(a_desc)), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else if (KIND == GQ_PROBE_MMA_F16) {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
@@ -238,7 +245,7 @@ probe_mma_kernel(int n, int iters, unsigned long long* __restrict__ cycles) {
     MmaProbeBars* bars = reinterpret_cast<MmaProbeBars*>(sB + 256 * 128);
     const int warp = threadIdx.x >> 5;
     // small finite operands: 1/64 in both formats' encodings (bf16 0x3C80, e4m3 0x20)
-    const uint32_t fillw = (KIND == GQ_PROBE_MMA_F16) ? 0x3C803C80u : 0x20202020u;
+    const uint32_t fillw = (KIND == GQ_PROBE_MMA_F8) ? 0x20202020u : 0x3C803C80u;
     for (int i = threadIdx.x; i < (128 + 256) * 128 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(base)[i] = fillw;
     if (threadIdx.x == 0) {
         mbar_init(&bars->done, 1);
@@ -255,12 +262,26 @@ probe_mma_kernel(int n, int iters, unsigned long long* __restrict__ cycles) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    if (KIND == GQ_PROBE_MMA_F16_TMEM_A) {
+        // the A operand's 8 columns: bf16 1/64 in every lane (each warp its 32 lanes)
+        uint32_t v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = fillw;
+        tc_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 256u, v);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
     if (threadIdx.x == 0) {
         // D f32; A, B bf16 (kind::f16) or e4m3 (kind::f8f6f4, format code 0); both K-major; N, M = 128
-        const uint32_t fmt = (KIND == GQ_PROBE_MMA_F16) ? 1u : 0u;
+        const uint32_t fmt = (KIND == GQ_PROBE_MMA_F8) ? 0u : 1u;
         const uint32_t idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
                                (static_cast<uint32_t>(128 >> 4) << 24);
-        const uint64_t ad = smem_desc(sA), bd = smem_desc(sB);
+        // A from shared memory, or (the TMEM-operand kind) 8 columns of tensor memory after the
+        // 256-column accumulator
+        const uint64_t ad = (KIND == GQ_PROBE_MMA_F16_TMEM_A) ? static_cast<uint64_t>(tmem + 256u) : smem_desc(sA);
+        const uint64_t bd = smem_desc(sB);
         const unsigned long long t0 = clock64();
         for (int i = 0; i < iters; ++i) probe_mma_ss<KIND>(tmem, ad, bd, idesc, i > 0 ? 1u : 0u);
         tc_commit(&bars->done);
@@ -380,14 +401,15 @@ extern "C" int gq_probe_issue(int kind, int iters, unsigned long long* cycles_de
 }
 
 extern "C" int gq_probe_mma(int kind, int n, int iters, unsigned long long* cycles_device, gq_stream_t stream) {
-    if (kind != GQ_PROBE_MMA_F16 && kind != GQ_PROBE_MMA_F8) return GQ_EUNSUPPORTED;
+    if (kind != GQ_PROBE_MMA_F16 && kind != GQ_PROBE_MMA_F8 && kind != GQ_PROBE_MMA_F16_TMEM_A) return GQ_EUNSUPPORTED;
     if (n < 16 || n > 256 || n % 16 != 0 || iters < 1 || iters > 100000) return GQ_EINVAL_SHAPE;
     if (!cycles_device || (reinterpret_cast<uintptr_t>(cycles_device) & 7)) return GQ_EINVAL_PTR;
     int sms = 0;
     const int se = sm_count(&sms);
     if (se != 0) return fail(static_cast<cudaError_t>(se));
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = (kind == GQ_PROBE_MMA_F16) ? launch_mma_probe<GQ_PROBE_MMA_F16>(sms, n, iters, cycles_device, s)
-                                                     : launch_mma_probe<GQ_PROBE_MMA_F8>(sms, n, iters, cycles_device, s);
+    const cudaError_t e = (kind == GQ_PROBE_MMA_F16)   ? launch_mma_probe<GQ_PROBE_MMA_F16>(sms, n, iters, cycles_device, s)
+                          : (kind == GQ_PROBE_MMA_F8) ? launch_mma_probe<GQ_PROBE_MMA_F8>(sms, n, iters, cycles_device, s)
+                                                      : launch_mma_probe<GQ_PROBE_MMA_F16_TMEM_A>(sms, n, iters, cycles_device, s);
     return fail(e);
 }

@@ -442,12 +442,14 @@ double gq_probe_issue_insts(int kind, int iters);
  * kind::i8 for sm_103a. */
 enum gq_probe_mma_kind {
     GQ_PROBE_MMA_F16 = 0,       /* kind::f16, bf16 operands, f32 accumulator, K = 16 per MMA  */
-    GQ_PROBE_MMA_F8 = 1         /* kind::f8f6f4, e4m3 operands, f32 accumulator, K = 32       */
+    GQ_PROBE_MMA_F8 = 1,        /* kind::f8f6f4, e4m3 operands, f32 accumulator, K = 32       */
+    GQ_PROBE_MMA_F16_TMEM_A = 2 /* kind::f16 as kind 0, with the A operand in tensor memory   */
 };
 
 /* tcgen05 MMA rate: on every SM one thread issues `iters` MMAs of M = 128, N = n, with both
  * operands in shared memory, into one TMEM accumulator, then waits (bounded) for them to
  * complete; cycles_device[sm] receives the SM clock cycles from the first issue to completion.
+ * (Kind GQ_PROBE_MMA_F16_TMEM_A takes A from tensor memory, as the library's prefill does.)
  * Flops per MMA = 2 * 128 * n * K.  Errors: GQ_EUNSUPPORTED for another kind; GQ_EINVAL_SHAPE
  * unless n is a multiple of 16 in [16, 256] and 1 <= iters <= 100000; GQ_EINVAL_PTR; GQ_ECUDA. */
 int gq_probe_mma(int kind, int n, int iters, unsigned long long* cycles_device, gq_stream_t stream);

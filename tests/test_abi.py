@@ -118,7 +118,7 @@ X = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
     (lambda L: L.gq_probe_issue(99, 10, X, X, N), 1),
     (lambda L: L.gq_probe_issue(0, 0, X, X, N), 1),
     (lambda L: L.gq_probe_issue(0, 10, ctypes.c_void_p(0x1004), X, N), 2),
-    (lambda L: L.gq_probe_mma(2, 64, 10, X, N), 3),
+    (lambda L: L.gq_probe_mma(5, 64, 10, X, N), 3),
     (lambda L: L.gq_probe_mma(0, 24, 10, X, N), 1),
     (lambda L: L.gq_probe_mma(1, 64, 10, N, N), 2),
 ])
