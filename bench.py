@@ -100,7 +100,7 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- helpers
 # The sources the headline GEMV is built from: a recorded DRAM-traffic figure counts only while
 # their hash matches the one stored with it.
-GEMV_SOURCES = ("q1.cu", "gq_internal.cuh")
+GEMV_SOURCES = ("q1_gemv.cu", "q1_common.cuh", "gq_internal.cuh")
 
 
 def kernel_hash(*names):

@@ -54,7 +54,7 @@ int gq_last_cuda_error(void) { return t_last_cuda_error; }
 int gq_device_error(void) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_status(e) == GQ_OK ? 0 : -1;
-    const unsigned v = gq::error_read_clear_q1() | gq::error_read_clear_ternary() | gq::error_read_clear_prefill_mma() |
+    const unsigned v = gq::error_read_clear_q1() | gq::error_read_clear_q1_gemv() | gq::error_read_clear_ternary() | gq::error_read_clear_prefill_mma() |
                        gq::error_read_clear_wq_mma() | gq::error_read_clear_w1a32() | gq::error_read_clear_probes();
     return v == ~0u ? -1 : static_cast<int>(v);
 }

@@ -31,6 +31,7 @@ __device__ __forceinline__ void report_error(unsigned code) { atomicOr(&g_device
         return v;                                                                      \
     }
 unsigned error_read_clear_q1();
+unsigned error_read_clear_q1_gemv();
 unsigned error_read_clear_ternary();
 unsigned error_read_clear_prefill_mma();
 unsigned error_read_clear_w1a32();
@@ -175,6 +176,8 @@ cudaError_t launch_q1_pack(const void* raw, int rows, int n, void* packed, cudaS
 cudaError_t launch_q1_gemv(const void* packed, const void* act, float* y, int rows, int n, void* workspace,
                            int act_format, cudaStream_t s);   // act_format: GQ_ACT_Q8_0 or GQ_ACT_F32
 size_t gemv_workspace_bytes(int n);
+cudaError_t launch_q1_gemv_persistent(const void* packed, const void* act, float* y, int rows, int n, void* workspace,
+                                      int act_format, cudaStream_t s);   // q1_gemv.cu
 cudaError_t launch_q1s32_f32(const uint32_t* signs, const float* ws, const float* x, float* y, int M, int N, int K,
                              int path, cudaStream_t s);   // path: GQ_PATH_FMA or GQ_PATH_LUT4
 cudaError_t launch_q1_gemv_raw(const void* w, const void* act, float* y, int rows, int n, cudaStream_t s);
