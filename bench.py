@@ -233,6 +233,9 @@ def run_probes(gq, torch, dev):
         "tensor_bf16_flop_per_s": mma["f16_bf16_n256"]["flop_per_sm_cycle"] * sms * f_hz,
         "tensor_e4m3_flop_per_s": mma["f8f6f4_e4m3_n256"]["flop_per_sm_cycle"] * sms * f_hz,
         "tcgen05_kind_i8": "not available: ptxas rejects tcgen05.mma kind::i8 for sm_103a",
+        # warp-level mma.sync (A operand fed from the previous result, so conversions stay in the loop)
+        "mma_sync_flop_per_s": {k: issue[f"mma_sync_{k}"] * fl * sms * f_hz
+                                for k, fl in (("f16", 4096), ("bf16", 4096), ("e4m3", 8192), ("s8", 8192))},
         "sm_count": sms, "sm_clock_hz": f_hz,
     }
 

@@ -106,6 +106,33 @@ __device__ __forceinline__ void op_imad(uint32_t& a, uint32_t b, uint32_t c) {
 __device__ __forceinline__ void op_shfl(uint32_t& a) {
     asm volatile("shfl.sync.idx.b32 %0, %0, %0, 0x1f, 0xffffffff;" : "+r"(a));
 }
+// warp-level (legacy) tensor-core MMAs, accumulator in registers
+__device__ __forceinline__ void op_mma_f16(float4& d, uint32_t a, uint32_t b) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %4, %4, %4}, {%5, %5}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d.x), "+f"(d.y), "+f"(d.z), "+f"(d.w)
+                 : "r"(a), "r"(b));
+}
+__device__ __forceinline__ void op_mma_bf16(float4& d, uint32_t a, uint32_t b) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %4, %4, %4}, {%5, %5}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d.x), "+f"(d.y), "+f"(d.z), "+f"(d.w)
+                 : "r"(a), "r"(b));
+}
+__device__ __forceinline__ void op_mma_e4m3(float4& d, uint32_t a, uint32_t b) {
+    asm volatile("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %4, %4, %4}, {%5, %5}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d.x), "+f"(d.y), "+f"(d.z), "+f"(d.w)
+                 : "r"(a), "r"(b));
+}
+__device__ __forceinline__ void op_mma_s8(float4& d, uint32_t a, uint32_t b) {
+    int4 t = make_int4(__float_as_int(d.x), __float_as_int(d.y), __float_as_int(d.z), __float_as_int(d.w));
+    asm volatile("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %4, %4, %4}, {%5, %5}, "
+                 "{%0, %1, %2, %3};"
+                 : "+r"(t.x), "+r"(t.y), "+r"(t.z), "+r"(t.w)
+                 : "r"(a), "r"(b));
+    d = make_float4(__int_as_float(t.x), __int_as_float(t.y), __int_as_float(t.z), __int_as_float(t.w));
+}
 template <int OFF>
 __device__ __forceinline__ void op_lds(uint32_t& a, uint32_t saddr) {
     uint32_t v;
@@ -116,8 +143,10 @@ __device__ __forceinline__ void op_lds(uint32_t& a, uint32_t saddr) {
 // one round: eight ops (or four of each kind for a pair), chain j on accumulator j
 template <int KIND, int R>
 __device__ __forceinline__ void issue_round(uint32_t (&u)[kIssueChains], float (&f)[kIssueChains],
-                                            float2 (&g)[kIssueChains], uint32_t saddr) {
+                                            float2 (&g)[kIssueChains], float4 (&m)[kIssueChains], uint32_t saddr) {
     const float2 g1 = make_float2(0.999f, 1.001f), g2 = make_float2(1e-7f, -1e-7f);
+    // small operands: f16 2^-6 (0x2400), bf16 2^-6 (0x3C80), e4m3 2^-3 (0x20), s8 1
+    constexpr uint32_t kH = 0x24002400u, kBH = 0x3C803C80u, kE = 0x20202020u, kS = 0x01010101u;
 #pragma unroll
     for (int j = 0; j < kIssueChains; ++j) {
         constexpr int off = 128 * (R & 7);
@@ -152,6 +181,23 @@ __device__ __forceinline__ void issue_round(uint32_t (&u)[kIssueChains], float (
             case GQ_PROBE_LOP3_FFMA2:
                 if (j & 1) op_ffma2(g[j], g1, g2); else op_lop3(u[j], 0x5A5A5A5Au, 0x33333333u);
                 break;
+            // The A operand is the chain's previous result (bits masked to keep it small and finite),
+            // so no operand conversion can be hoisted out of the loop: e4m3 operands are converted in
+            // the issuing warp on this GPU, and that cost belongs to the rate.
+            case GQ_PROBE_HMMA_F16: op_mma_f16(m[j], (__float_as_uint(m[j].x) & 0x03FF03FFu) | kH, kH); break;
+            case GQ_PROBE_HMMA_BF16: op_mma_bf16(m[j], (__float_as_uint(m[j].x) & 0x007F007Fu) | kBH, kBH); break;
+            case GQ_PROBE_QMMA_E4M3: op_mma_e4m3(m[j], (__float_as_uint(m[j].x) & 0x07070707u) | kE, kE); break;
+            case GQ_PROBE_IMMA_S8: op_mma_s8(m[j], (__float_as_uint(m[j].x) & 0x03030303u) | kS, kS); break;
+            case GQ_PROBE_HMMA_MIX:     // mma : lop3 : lop3 : ffma
+                if ((j & 3) == 0) op_mma_f16(m[j], (__float_as_uint(m[j].x) & 0x03FF03FFu) | kH, kH);
+                else if ((j & 3) == 3) op_ffma(f[j], 0.999f, 1e-7f);
+                else op_lop3(u[j], 0x5A5A5A5Au, 0x33333333u);
+                break;
+            case GQ_PROBE_QMMA_MIX:
+                if ((j & 3) == 0) op_mma_e4m3(m[j], (__float_as_uint(m[j].x) & 0x07070707u) | kE, kE);
+                else if ((j & 3) == 3) op_ffma(f[j], 0.999f, 1e-7f);
+                else op_lop3(u[j], 0x5A5A5A5Au, 0x33333333u);
+                break;
             default: break;
         }
     }
@@ -166,27 +212,31 @@ probe_issue_kernel(int iters, unsigned long long* __restrict__ cycles, uint32_t*
     uint32_t u[kIssueChains];
     float f[kIssueChains];
     float2 g[kIssueChains];
+    float4 m[kIssueChains];
 #pragma unroll
     for (int j = 0; j < kIssueChains; ++j) {
         u[j] = threadIdx.x * 7u + j;
         f[j] = 1.0f + j;
         g[j] = make_float2(1.0f + j, 2.0f + j);
+        m[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
     __syncthreads();
     unsigned long long t0 = 0;
     if (threadIdx.x == 0) t0 = clock64();
 #pragma unroll 1
     for (int it = 0; it < iters; ++it) {
-        issue_round<KIND, 0>(u, f, g, saddr);
-        issue_round<KIND, 1>(u, f, g, saddr);
-        issue_round<KIND, 2>(u, f, g, saddr);
-        issue_round<KIND, 3>(u, f, g, saddr);
+        issue_round<KIND, 0>(u, f, g, m, saddr);
+        issue_round<KIND, 1>(u, f, g, m, saddr);
+        issue_round<KIND, 2>(u, f, g, m, saddr);
+        issue_round<KIND, 3>(u, f, g, m, saddr);
     }
     __syncthreads();
     if (threadIdx.x == 0) cycles[blockIdx.x] = clock64() - t0;
     uint32_t x = 0;
 #pragma unroll
-    for (int j = 0; j < kIssueChains; ++j) x ^= u[j] ^ __float_as_uint(f[j]) ^ __float_as_uint(g[j].x) ^ __float_as_uint(g[j].y);
+    for (int j = 0; j < kIssueChains; ++j)
+        x ^= u[j] ^ __float_as_uint(f[j]) ^ __float_as_uint(g[j].x) ^ __float_as_uint(g[j].y) ^
+             __float_as_uint(m[j].x) ^ __float_as_uint(m[j].y) ^ __float_as_uint(m[j].z) ^ __float_as_uint(m[j].w);
     if (x == 0x5EED5EEDu) sink[0] = x;    // keeps every chain live
 }
 
@@ -394,6 +444,12 @@ extern "C" int gq_probe_issue(int kind, int iters, unsigned long long* cycles_de
         GQ_PROBE_CASE(GQ_PROBE_LOP3_DP4A)
         GQ_PROBE_CASE(GQ_PROBE_FADD_FFMA2)
         GQ_PROBE_CASE(GQ_PROBE_LOP3_FFMA2)
+        GQ_PROBE_CASE(GQ_PROBE_HMMA_F16)
+        GQ_PROBE_CASE(GQ_PROBE_HMMA_BF16)
+        GQ_PROBE_CASE(GQ_PROBE_QMMA_E4M3)
+        GQ_PROBE_CASE(GQ_PROBE_IMMA_S8)
+        GQ_PROBE_CASE(GQ_PROBE_HMMA_MIX)
+        GQ_PROBE_CASE(GQ_PROBE_QMMA_MIX)
 #undef GQ_PROBE_CASE
         default: return GQ_EINVAL_SHAPE;
     }

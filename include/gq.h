@@ -424,7 +424,14 @@ enum gq_probe_kind {
     GQ_PROBE_LOP3_DP4A = 15,    /* lop3 and dp4a interleaved               */
     GQ_PROBE_FADD_FFMA2 = 16,   /* add.rn.f32 and fma.rn.f32x2 interleaved */
     GQ_PROBE_LOP3_FFMA2 = 17,   /* lop3 and fma.rn.f32x2 interleaved       */
-    GQ_PROBE_ISSUE_KINDS = 18
+    GQ_PROBE_HMMA_F16 = 18,     /* mma.sync m16n8k16 f16 x f16 + f32 (4096 flop each)  */
+    GQ_PROBE_HMMA_BF16 = 19,    /* mma.sync m16n8k16 bf16 x bf16 + f32 (4096 flop)     */
+    GQ_PROBE_QMMA_E4M3 = 20,    /* mma.sync m16n8k32 e4m3 x e4m3 + f32 (8192 flop),
+                                   operand conversion included                          */
+    GQ_PROBE_IMMA_S8 = 21,      /* mma.sync m16n8k32 s8 x s8 + s32 (8192 op)           */
+    GQ_PROBE_HMMA_MIX = 22,     /* f16 mma.sync : lop3 : lop3 : fma.rn.f32, 1:2:1      */
+    GQ_PROBE_QMMA_MIX = 23,     /* e4m3 mma.sync : lop3 : lop3 : fma.rn.f32, 1:2:1     */
+    GQ_PROBE_ISSUE_KINDS = 24
 };
 
 /* Instruction issue rate: one block of 32 warps per SM runs `iters` loop iterations of 32
