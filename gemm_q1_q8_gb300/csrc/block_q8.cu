@@ -383,6 +383,448 @@ block_q8_pair_kernel(const float* __restrict__ x, const uint32_t* __restrict__ q
     }
 }
 
+// Stages the tile's activations x[m0 .. m0 + MT)[0 .. k) into xs as [k][MT] (x[m0 + r][kk] at
+// kk*MT + r; rows past m as zeros): sixteen independent 16-byte loads per thread in flight when x
+// is 16-byte aligned (item i = 4 consecutive k of row i % MT), else single floats.
+template <int MT, int THREADS>
+__device__ __forceinline__ void stage_x(float* xs, const float* __restrict__ x, int m, int m0, int k) {
+    if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+        const int items = MT * k / 4;
+        for (int i0 = threadIdx.x; i0 < items; i0 += 16 * THREADS) {
+            float4 v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int i = i0 + u * THREADS;
+                const int r = i % MT, k4 = i / MT;
+                v[u] = (i < items && m0 + r < m)
+                           ? __ldg(reinterpret_cast<const float4*>(x + static_cast<size_t>(m0 + r) * k) + k4)
+                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int i = i0 + u * THREADS;
+                if (i < items) {
+                    const int r = i % MT, k4 = i / MT;
+                    float* d = xs + (4 * k4) * MT + r;
+                    d[0] = v[u].x;
+                    d[MT] = v[u].y;
+                    d[2 * MT] = v[u].z;
+                    d[3 * MT] = v[u].w;
+                }
+            }
+        }
+    } else {
+        const int total = MT * k;
+        for (int e0 = threadIdx.x; e0 < total; e0 += 8 * THREADS) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = e0 + u * THREADS;
+                const int kk = e / MT, r = e % MT;
+                v[u] = (e < total && m0 + r < m) ? __ldg(x + static_cast<size_t>(m0 + r) * k + kk) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = e0 + u * THREADS;
+                if (e < total) xs[e] = v[u];
+            }
+        }
+    }
+}
+
+// 3 to 16 activation rows (a tile of MT of them per grid row): a warp owns a strip of 32 weight
+// rows, one per lane, and runs every block of its row in order, so acc stays in a register and
+// needs no hand-over.  The thread block stages the tile's activations once, [k][MT], and every
+// read of them is a broadcast (all lanes at the same k).  Each lane streams its row's 32-byte
+// blocks with D blocks in flight.  Four warps per thread block: the grid (n / 128 blocks
+// per tile) is one wave with two or three thread blocks per SM.
+constexpr int kStWarps = 4;
+constexpr int kStDepth = 4;                    // blocks of codes in flight per lane (pairs)
+
+template <int MT>
+size_t st_smem(int k) { return static_cast<size_t>(k) * MT * 4; }
+constexpr size_t kStSmemMax = 200 * 1024;
+
+template <int MT, int W = kStWarps, int D = kStDepth>
+__global__ void __launch_bounds__(W * 32)
+block_q8_strip_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants,
+                      const float* __restrict__ scales, float* __restrict__ y, int m, int k, int n) {
+    extern __shared__ __align__(16) float smem_f[];          // [k][MT]: x[m0 + r][kk] at kk*MT + r
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbk = k / 32;
+    const int m0 = blockIdx.y * MT;
+    const int row = (blockIdx.x * W + warp) * 32 + lane;
+    const int rc = min(row, n - 1);                          // past-the-end rows: computed, not stored
+    const uint4* qp = reinterpret_cast<const uint4*>(quants) + static_cast<size_t>(rc) * (k / 16);
+    const float* sp = scales + static_cast<size_t>(rc) * nbk;
+
+    // the first blocks' codes are requested before the wait for the preceding grids (weights are
+    // not written by them); the activations are read after it
+    uint4 w0[D], w1[D];
+    float sc[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+        const int b = min(d, nbk - 1);
+        w0[d] = __ldg(qp + 2 * b);
+        w1[d] = __ldg(qp + 2 * b + 1);
+        sc[d] = __ldg(sp + b);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    stage_x<MT, W * 32>(smem_f, x, m, m0, k);
+    __syncthreads();
+    float acc[MT];
+#pragma unroll
+    for (int r = 0; r < MT; ++r) acc[r] = 0.0f;
+    static_assert(D % 2 == 0, "blocks are summed in pairs");
+    for (int b0 = 0; b0 < nbk; b0 += D) {
+#pragma unroll
+        for (int d = 0; d < D; d += 2) {             // slots d, d + 1 hold blocks b0 + d, b0 + d + 1
+            const int b = b0 + d;
+            if (b >= nbk) break;
+            const bool two = b + 1 < nbk;
+            uint32_t wq[2][8];
+            float s[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                wq[h][0] = w0[d + h].x ^ 0x80808080u; wq[h][1] = w0[d + h].y ^ 0x80808080u;
+                wq[h][2] = w0[d + h].z ^ 0x80808080u; wq[h][3] = w0[d + h].w ^ 0x80808080u;
+                wq[h][4] = w1[d + h].x ^ 0x80808080u; wq[h][5] = w1[d + h].y ^ 0x80808080u;
+                wq[h][6] = w1[d + h].z ^ 0x80808080u; wq[h][7] = w1[d + h].w ^ 0x80808080u;
+                s[h] = sc[d + h];
+                if (b + h + D < nbk) {                // refill the slot D blocks ahead
+                    w0[d + h] = __ldg(qp + 2 * (b + h + D));
+                    w1[d + h] = __ldg(qp + 2 * (b + h + D) + 1);
+                    sc[d + h] = __ldg(sp + b + h + D);
+                }
+            }
+            // the two blocks' sums are independent: their chains run side by side (a lone last
+            // block sums block 0's activations in its second half, unused)
+            const float* xb0 = smem_f + static_cast<size_t>(b) * 32 * MT;
+            const float* xb1 = two ? xb0 + 32 * MT : smem_f;
+            float bs0[MT], bs1[MT];
+#pragma unroll
+            for (int r = 0; r < MT; ++r) bs0[r] = bs1[r] = 0.0f;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                accumulate_rows<MT>(bs0, xb0 + t * MT, q_of(wq[0][t >> 2], t & 3));
+                accumulate_rows<MT>(bs1, xb1 + t * MT, q_of(wq[1][t >> 2], t & 3));
+            }
+#pragma unroll
+            for (int r = 0; r < MT; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s[0], bs0[r]));
+            if (two) {
+#pragma unroll
+                for (int r = 0; r < MT; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s[1], bs1[r]));
+            }
+        }
+    }
+    // the next launch may start now (its prologue overlaps these stores); released only here so
+    // that back-to-back launches do not pile up resident thread blocks that wait
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (row < n) {
+#pragma unroll
+        for (int r = 0; r < MT; ++r)
+            if (m0 + r < m) y[static_cast<size_t>(m0 + r) * n + row] = acc[r];
+    }
+}
+
+// Four activation rows per grid row (any m >= 3 as tiles of four), activations read straight from
+// global memory: a lane owns one weight row and runs its blocks in order (pairs of blocks summed
+// side by side), and at each step all lanes read the same four activations of a row, a broadcast
+// 16-byte load that stays in L1 (the tile's activations are k * 16 bytes); the codes stream past
+// L1 without allocating.  No shared memory and no staging before the first block.
+__device__ __forceinline__ uint4 ld_codes(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+template <int W, int D>
+__global__ void __launch_bounds__(W * 32)
+block_q8_regx_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants,
+                     const float* __restrict__ scales, float* __restrict__ y, int m, int k, int n) {
+    static_assert(D % 2 == 0, "blocks are summed in pairs");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbk = k / 32;
+    const int m0 = blockIdx.y * 4;
+    const int row = (blockIdx.x * W + warp) * 32 + lane;
+    const int rc = min(row, n - 1);                          // past-the-end rows: computed, not stored
+    const uint4* qp = reinterpret_cast<const uint4*>(quants) + static_cast<size_t>(rc) * (k / 16);
+    const float* sp = scales + static_cast<size_t>(rc) * nbk;
+    uint4 w0[D], w1[D];
+    float sc[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {                           // weights: before the wait
+        const int b = min(d, nbk - 1);
+        w0[d] = ld_codes(qp + 2 * b);
+        w1[d] = ld_codes(qp + 2 * b + 1);
+        sc[d] = __ldg(sp + b);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the tile's four activation rows (rows past m repeat row m - 1: computed, not stored)
+    const float4* xr[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) xr[r] = reinterpret_cast<const float4*>(x + static_cast<size_t>(min(m0 + r, m - 1)) * k);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int b0 = 0; b0 < nbk; b0 += D) {
+#pragma unroll
+        for (int d = 0; d < D; d += 2) {
+            const int b = b0 + d;
+            if (b >= nbk) break;
+            const bool two = b + 1 < nbk;
+            const int b1 = two ? b + 1 : b;                  // a lone last block sums itself twice, once unused
+            uint32_t wq[2][8];
+            float s[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                wq[h][0] = w0[d + h].x ^ 0x80808080u; wq[h][1] = w0[d + h].y ^ 0x80808080u;
+                wq[h][2] = w0[d + h].z ^ 0x80808080u; wq[h][3] = w0[d + h].w ^ 0x80808080u;
+                wq[h][4] = w1[d + h].x ^ 0x80808080u; wq[h][5] = w1[d + h].y ^ 0x80808080u;
+                wq[h][6] = w1[d + h].z ^ 0x80808080u; wq[h][7] = w1[d + h].w ^ 0x80808080u;
+                s[h] = sc[d + h];
+                if (b + h + D < nbk) {
+                    w0[d + h] = ld_codes(qp + 2 * (b + h + D));
+                    w1[d + h] = ld_codes(qp + 2 * (b + h + D) + 1);
+                    sc[d + h] = __ldg(sp + b + h + D);
+                }
+            }
+            float bs0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, bs1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int tq = 0; tq < 8; ++tq) {
+                float4 xa[4], xb[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    xa[r] = __ldg(xr[r] + b * 8 + tq);
+                    xb[r] = __ldg(xr[r] + b1 * 8 + tq);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float qa = q_of(wq[0][tq], i), qb = q_of(wq[1][tq], i);
+                    const float4 va = make_float4(i == 0 ? xa[0].x : i == 1 ? xa[0].y : i == 2 ? xa[0].z : xa[0].w,
+                                                  i == 0 ? xa[1].x : i == 1 ? xa[1].y : i == 2 ? xa[1].z : xa[1].w,
+                                                  i == 0 ? xa[2].x : i == 1 ? xa[2].y : i == 2 ? xa[2].z : xa[2].w,
+                                                  i == 0 ? xa[3].x : i == 1 ? xa[3].y : i == 2 ? xa[3].z : xa[3].w);
+                    const float4 vb = make_float4(i == 0 ? xb[0].x : i == 1 ? xb[0].y : i == 2 ? xb[0].z : xb[0].w,
+                                                  i == 0 ? xb[1].x : i == 1 ? xb[1].y : i == 2 ? xb[1].z : xb[1].w,
+                                                  i == 0 ? xb[2].x : i == 1 ? xb[2].y : i == 2 ? xb[2].z : xb[2].w,
+                                                  i == 0 ? xb[3].x : i == 1 ? xb[3].y : i == 2 ? xb[3].z : xb[3].w);
+                    float2 lo = fadd2(make_float2(bs0[0], bs0[1]), make_float2(__fmul_rn(va.x, qa), __fmul_rn(va.y, qa)));
+                    float2 hi = fadd2(make_float2(bs0[2], bs0[3]), make_float2(__fmul_rn(va.z, qa), __fmul_rn(va.w, qa)));
+                    bs0[0] = lo.x; bs0[1] = lo.y; bs0[2] = hi.x; bs0[3] = hi.y;
+                    lo = fadd2(make_float2(bs1[0], bs1[1]), make_float2(__fmul_rn(vb.x, qb), __fmul_rn(vb.y, qb)));
+                    hi = fadd2(make_float2(bs1[2], bs1[3]), make_float2(__fmul_rn(vb.z, qb), __fmul_rn(vb.w, qb)));
+                    bs1[0] = lo.x; bs1[1] = lo.y; bs1[2] = hi.x; bs1[3] = hi.y;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s[0], bs0[r]));
+            if (two) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s[1], bs1[r]));
+            }
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (row < n) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            if (m0 + r < m) y[static_cast<size_t>(m0 + r) * n + row] = acc[r];
+    }
+}
+
+// The strip kernel with the codes brought in by the tensor-memory accelerator: each warp keeps a
+// ring of S stages, one per block, each the 32 x 32-byte tile of its 32 weight rows (1 KB, one
+// tiled copy with the 32-byte swizzle, so each lane's two 16-byte reads of its row fall in distinct
+// bank groups).  Lane 0 refills a stage with the block S ahead as soon as the warp has read it, so
+// S blocks of codes are in flight per warp without holding them in registers; the scales (4 bytes
+// per row and block) are loaded by each lane S blocks ahead.  Every wait is bounded: a warp that
+// gives up reports it, lets its copies still in flight land, and stops.
+constexpr int kTmWarps = 4;
+
+template <int S, int W>
+__host__ __device__ constexpr size_t tm_ring_bytes() { return static_cast<size_t>(W) * S * 1024; }
+template <int S, int W>
+__host__ __device__ constexpr size_t tm_bar_bytes() { return (static_cast<size_t>(W) * S * 8 + 15) / 16 * 16; }
+template <int MT, int S, int W>
+size_t tm_smem(int k) { return 1024 + tm_ring_bytes<S, W>() + tm_bar_bytes<S, W>() + static_cast<size_t>(k) * MT * 4; }
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+template <int MT, int S, int W = kTmWarps>
+__global__ void __launch_bounds__(W * 32)
+block_q8_tma_kernel(const __grid_constant__ CUtensorMap tm, const float* __restrict__ x,
+                    const float* __restrict__ scales, float* __restrict__ y, int m, int k, int n) {
+    static_assert(S % 2 == 0, "blocks are summed in pairs");
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t* base = smem_align1024(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* ring = base + static_cast<size_t>(warp) * S * 1024;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + tm_ring_bytes<S, W>()) + warp * S;
+    float* xs = reinterpret_cast<float*>(base + tm_ring_bytes<S, W>() + tm_bar_bytes<S, W>());
+    const int nbk = k / 32;
+    const int m0 = blockIdx.y * MT;
+    const int row0 = (blockIdx.x * W + warp) * 32;
+    const int row = row0 + lane;
+    const float* sp = scales + static_cast<size_t>(min(row, n - 1)) * nbk;   // past-the-end rows: not stored
+    if (lane == 0) {
+        prefetch_tmap(&tm);
+#pragma unroll
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    // the first S blocks' codes and scales: before the wait for the preceding grids (weights)
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+            if (s < nbk) {
+                mbar_arrive_expect_tx(&bars[s], 1024);
+                tma_load_2d(ring + s * 1024, &tm, 32 * s, row0, &bars[s]);
+            }
+    }
+    float sc[S];
+#pragma unroll
+    for (int d = 0; d < S; ++d) sc[d] = __ldg(sp + min(d, nbk - 1));
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    stage_x<MT, W * 32>(xs, x, m, m0, k);
+    __syncthreads();
+
+    float acc[MT];
+#pragma unroll
+    for (int r = 0; r < MT; ++r) acc[r] = 0.0f;
+    for (int b0 = 0; b0 < nbk; b0 += S) {
+        const uint32_t par = static_cast<uint32_t>(b0 / S) & 1u;
+#pragma unroll
+        for (int d = 0; d < S; d += 2) {             // stages d, d + 1 hold blocks b0 + d, b0 + d + 1
+            const int b = b0 + d;
+            if (b >= nbk) break;
+            const bool two = b + 1 < nbk;
+            bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[d], par));
+            if (ok && two) ok = __all_sync(0xffffffffu, mbar_wait(&bars[d + 1], par));
+            if (!ok) {
+                if (lane == 0) {
+                    report_error(kErrWaitTimeout);
+                    for (int c = b; c < min(nbk, b + S); ++c)      // the copies still in flight
+                        if (!mbar_wait(&bars[c % S], static_cast<uint32_t>(c / S) & 1u)) report_error(kErrDrainTimeout);
+                }
+                return;
+            }
+            const uint4 a0 = lds128(ring + d * 1024 + swz32(lane, 0)), a1 = lds128(ring + d * 1024 + swz32(lane, 1));
+            uint4 c0 = a0, c1 = a1;
+            if (two) {
+                c0 = lds128(ring + (d + 1) * 1024 + swz32(lane, 0));
+                c1 = lds128(ring + (d + 1) * 1024 + swz32(lane, 1));
+            }
+            const float s0 = sc[d], s1 = sc[d + 1];
+            if (b + S < nbk) sc[d] = __ldg(sp + b + S);
+            if (b + 1 + S < nbk) sc[d + 1] = __ldg(sp + b + 1 + S);
+            __syncwarp();                            // every lane has read the two stages
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                if (b + S < nbk) {
+                    mbar_arrive_expect_tx(&bars[d], 1024);
+                    tma_load_2d(ring + d * 1024, &tm, 32 * (b + S), row0, &bars[d]);
+                }
+                if (b + 1 + S < nbk) {
+                    mbar_arrive_expect_tx(&bars[d + 1], 1024);
+                    tma_load_2d(ring + (d + 1) * 1024, &tm, 32 * (b + 1 + S), row0, &bars[d + 1]);
+                }
+            }
+            const uint32_t wq[2][8] = {{a0.x ^ 0x80808080u, a0.y ^ 0x80808080u, a0.z ^ 0x80808080u, a0.w ^ 0x80808080u,
+                                        a1.x ^ 0x80808080u, a1.y ^ 0x80808080u, a1.z ^ 0x80808080u, a1.w ^ 0x80808080u},
+                                       {c0.x ^ 0x80808080u, c0.y ^ 0x80808080u, c0.z ^ 0x80808080u, c0.w ^ 0x80808080u,
+                                        c1.x ^ 0x80808080u, c1.y ^ 0x80808080u, c1.z ^ 0x80808080u, c1.w ^ 0x80808080u}};
+            // the two blocks' sums are independent: their chains run side by side (a lone last
+            // block sums its own activations twice, the second copy unused)
+            const float* xb0 = xs + static_cast<size_t>(b) * 32 * MT;
+            const float* xb1 = two ? xb0 + 32 * MT : xb0;
+            float bs0[MT], bs1[MT];
+#pragma unroll
+            for (int r = 0; r < MT; ++r) bs0[r] = bs1[r] = 0.0f;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                accumulate_rows<MT>(bs0, xb0 + t * MT, q_of(wq[0][t >> 2], t & 3));
+                accumulate_rows<MT>(bs1, xb1 + t * MT, q_of(wq[1][t >> 2], t & 3));
+            }
+#pragma unroll
+            for (int r = 0; r < MT; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s0, bs0[r]));
+            if (two) {
+#pragma unroll
+                for (int r = 0; r < MT; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s1, bs1[r]));
+            }
+        }
+    }
+    // every copy issued has been waited for; the next launch may start its prologue
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (row < n) {
+#pragma unroll
+        for (int r = 0; r < MT; ++r)
+            if (m0 + r < m) y[static_cast<size_t>(m0 + r) * n + row] = acc[r];
+    }
+}
+
+// The tensor-memory-accelerator strip kernel when its shared memory fits and the driver encodes
+// the codes' tensor map ([n] rows of k bytes, 32 x 32-byte boxes, 32-byte swizzle); returns
+// cudaErrorNotSupported otherwise, so the caller can take the register-streaming kernel.
+template <int MT, int S, int W = kTmWarps>
+cudaError_t launch_tma(const float* x, const uint32_t* q, const float* s, float* y, int m, int k, int n,
+                       cudaStream_t st) {
+    const size_t smem = tm_smem<MT, S, W>(k);
+    if (smem > kStSmemMax) return cudaErrorNotSupported;
+    CUtensorMap tm;
+    if (!make_tmap_2d_swizzle(&tm, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(k), static_cast<uint64_t>(n),
+                              static_cast<uint64_t>(k), 32, 32, CU_TENSOR_MAP_SWIZZLE_32B))
+        return cudaErrorNotSupported;
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_dev != dev) {
+        e = cudaFuncSetAttribute(block_q8_tma_kernel<MT, S, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kStSmemMax));
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((n + W * 32 - 1) / (W * 32), (m + MT - 1) / MT);
+    cfg.blockDim = dim3(W * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, block_q8_tma_kernel<MT, S, W>, tm, x, s, y, m, k, n);
+}
+
+template <int MT>
+cudaError_t launch_strip(const float* x, const uint32_t* q, const float* s, float* y, int m, int k, int n,
+                         cudaStream_t st) {
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_dev != dev) {
+        e = cudaFuncSetAttribute(block_q8_strip_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kStSmemMax));
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    // a programmatic dependent of the previous launch on the stream (see the kernel)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((n + kStWarps * 32 - 1) / (kStWarps * 32), (m + MT - 1) / MT);
+    cfg.blockDim = dim3(kStWarps * 32);
+    cfg.dynamicSmemBytes = st_smem<MT>(k);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, block_q8_strip_kernel<MT>, x, q, s, y, m, k, n);
+}
+
 template <int MT>
 cudaError_t launch_mt(const float* x, const uint32_t* q, const float* s, float* y, int m, int k, int n,
                       cudaStream_t st) {
@@ -408,6 +850,8 @@ cudaError_t launch_mt(const float* x, const uint32_t* q, const float* s, float* 
 
 }  // namespace
 
+GQ_ERROR_ACCESSOR(block_q8)
+
 cudaError_t launch_block_q8(const float* x, const uint32_t* quants, const float* scales, float* y, int m, int k,
                             int n, cudaStream_t s) {
     if (m <= 2) {
@@ -432,9 +876,21 @@ cudaError_t launch_block_q8(const float* x, const uint32_t* quants, const float*
         }
         return m <= 1 ? launch_mt<1>(x, quants, scales, y, m, k, n, s) : launch_mt<2>(x, quants, scales, y, m, k, n, s);
     }
-    if (m <= 4) return launch_mt<4>(x, quants, scales, y, m, k, n, s);
-    if (m <= 8) return launch_mt<8>(x, quants, scales, y, m, k, n, s);
-    return launch_mt<16>(x, quants, scales, y, m, k, n, s);
+    // 3 or more rows: the strip kernels while the staged activations fit in shared memory (the
+    // TMA-fed one for tiles of 4 and 16 rows, where it measured faster; the register-streaming one
+    // for 8 and whenever the tensor map cannot be encoded), else the pass kernels.
+    if (m <= 4) {
+        const cudaError_t e = launch_tma<4, 4>(x, quants, scales, y, m, k, n, s);
+        if (e != cudaErrorNotSupported) return e;
+        return st_smem<4>(k) <= kStSmemMax ? launch_strip<4>(x, quants, scales, y, m, k, n, s)
+                                           : launch_mt<4>(x, quants, scales, y, m, k, n, s);
+    }
+    if (m <= 8) return st_smem<8>(k) <= kStSmemMax ? launch_strip<8>(x, quants, scales, y, m, k, n, s)
+                                                  : launch_mt<8>(x, quants, scales, y, m, k, n, s);
+    const cudaError_t e = launch_tma<16, 2>(x, quants, scales, y, m, k, n, s);
+    if (e != cudaErrorNotSupported) return e;
+    return st_smem<16>(k) <= kStSmemMax ? launch_strip<16>(x, quants, scales, y, m, k, n, s)
+                                        : launch_mt<16>(x, quants, scales, y, m, k, n, s);
 }
 
 }  // namespace gq

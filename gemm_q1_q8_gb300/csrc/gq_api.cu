@@ -55,7 +55,8 @@ int gq_device_error(void) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_status(e) == GQ_OK ? 0 : -1;
     const unsigned v = gq::error_read_clear_q1() | gq::error_read_clear_q1_gemv() | gq::error_read_clear_ternary() | gq::error_read_clear_prefill_mma() |
-                       gq::error_read_clear_wq_mma() | gq::error_read_clear_w1a32() | gq::error_read_clear_probes();
+                       gq::error_read_clear_wq_mma() | gq::error_read_clear_w1a32() | gq::error_read_clear_probes() |
+                       gq::error_read_clear_block_q8();
     return v == ~0u ? -1 : static_cast<int>(v);
 }
 

@@ -36,6 +36,7 @@ unsigned error_read_clear_ternary();
 unsigned error_read_clear_prefill_mma();
 unsigned error_read_clear_w1a32();
 unsigned error_read_clear_probes();
+unsigned error_read_clear_block_q8();
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
@@ -217,6 +218,11 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
                   uint64_t inner, uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner,
                   uint32_t box_rows, bool swizzle128);
 
+// The same with an explicit swizzle mode.
+bool make_tmap_2d_swizzle(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t inner,
+                          uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
+                          CUtensorMapSwizzle swizzle);
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -231,6 +237,11 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 // swizzle (rows of 128 bytes, tile base 1024-byte aligned).
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+// The same for the 32-byte swizzle (rows of 32 bytes, tile base 256-byte aligned): address bit 4
+// is XORed with bit 7, i.e. the chunk (0 or 1) with bit 2 of the row.
+__device__ __forceinline__ uint32_t swz32(int row, int chunk) {
+    return static_cast<uint32_t>(row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4));
 }
 
 }  // namespace gq
