@@ -632,14 +632,17 @@ block_q8_regx_kernel(const float* __restrict__ x, const uint32_t* __restrict__ q
     }
 }
 
-// The strip kernel with the codes brought in by the tensor-memory accelerator: each warp keeps a
-// ring of S stages, one per block, each the 32 x 32-byte tile of its 32 weight rows (1 KB, one
-// tiled copy with the 32-byte swizzle, so each lane's two 16-byte reads of its row fall in distinct
-// bank groups).  Lane 0 refills a stage with the block S ahead as soon as the warp has read it, so
-// S blocks of codes are in flight per warp without holding them in registers; the scales (4 bytes
-// per row and block) are loaded by each lane S blocks ahead.  Every wait is bounded: a warp that
-// gives up reports it, lets its copies still in flight land, and stops.
-constexpr int kTmWarps = 4;
+// The strip kernel with the codes brought in by the tensor-memory accelerator, persistent: one
+// thread block per SM stages the tile's activations once, and takes an even share of the 32-row
+// strips (ceil(n / 32) of them over the grid: every SM gets the same number to within one), its
+// warps taking the block's strips in turn.  Each warp keeps a ring of S stages, one per 32-byte
+// block, each the 32 x 32-byte tile of its strip's rows (1 KB, one tiled copy with the 32-byte
+// swizzle, so each lane's two 16-byte reads of its row fall in distinct bank groups).  Lane 0
+// refills a stage with the block S ahead as soon as the warp has read it, so S blocks of codes are
+// in flight per warp without holding them in registers; the scales (4 bytes per row and block)
+// are loaded by each lane S blocks ahead.  Every wait is bounded: a warp that gives up reports it,
+// lets its copies still in flight land, and stops.
+constexpr int kTmWarps = 11;                   // >= strips per SM for n up to 11 * 32 * SMs
 
 template <int S, int W>
 __host__ __device__ constexpr size_t tm_ring_bytes() { return static_cast<size_t>(W) * S * 1024; }
@@ -647,6 +650,7 @@ template <int S, int W>
 __host__ __device__ constexpr size_t tm_bar_bytes() { return (static_cast<size_t>(W) * S * 8 + 15) / 16 * 16; }
 template <int MT, int S, int W>
 size_t tm_smem(int k) { return 1024 + tm_ring_bytes<S, W>() + tm_bar_bytes<S, W>() + static_cast<size_t>(k) * MT * 4; }
+constexpr size_t kTmSmemOneBlock = 120 * 1024;   // requested at least: one thread block per SM
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
@@ -663,119 +667,139 @@ block_q8_tma_kernel(const __grid_constant__ CUtensorMap tm, const float* __restr
     float* xs = reinterpret_cast<float*>(base + tm_ring_bytes<S, W>() + tm_bar_bytes<S, W>());
     const int nbk = k / 32;
     const int m0 = blockIdx.y * MT;
-    const int row0 = (blockIdx.x * W + warp) * 32;
-    const int row = row0 + lane;
-    const float* sp = scales + static_cast<size_t>(min(row, n - 1)) * nbk;   // past-the-end rows: not stored
-    if (lane == 0) {
+    const int strips = (n + 31) / 32;
+    const int se = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * strips / gridDim.x);
+    const int sb = static_cast<int>(static_cast<long long>(blockIdx.x) * strips / gridDim.x);
+    const bool busy = sb + warp < se;
+    // ring of the warp's current strip: S blocks primed, phase counts per stage
+    uint32_t ph[S];
+#pragma unroll
+    for (int d = 0; d < S; ++d) ph[d] = 0;
+    auto prime = [&](int row0) {
+        if (lane == 0) {
+#pragma unroll
+            for (int d = 0; d < S; ++d)
+                if (d < nbk) {
+                    mbar_arrive_expect_tx(&bars[d], 1024);
+                    tma_load_2d(ring + d * 1024, &tm, 32 * d, row0, &bars[d]);
+                }
+        }
+    };
+    if (busy && lane == 0) {
         prefetch_tmap(&tm);
 #pragma unroll
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        for (int d = 0; d < S; ++d) mbar_init(&bars[d], 1);
         fence_barrier_init();
     }
     __syncwarp();
-    // the first S blocks' codes and scales: before the wait for the preceding grids (weights)
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < S; ++s)
-            if (s < nbk) {
-                mbar_arrive_expect_tx(&bars[s], 1024);
-                tma_load_2d(ring + s * 1024, &tm, 32 * s, row0, &bars[s]);
-            }
-    }
-    float sc[S];
-#pragma unroll
-    for (int d = 0; d < S; ++d) sc[d] = __ldg(sp + min(d, nbk - 1));
+    // the first strip's first S blocks: before the wait for the preceding grids (weights)
+    if (busy) prime((sb + warp) * 32);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     stage_x<MT, W * 32>(xs, x, m, m0, k);
     __syncthreads();
-
-    float acc[MT];
+    for (int strip = sb + warp; strip < se; strip += W) {
+        const int row0 = strip * 32;
+        const int row = row0 + lane;
+        const float* sp = scales + static_cast<size_t>(min(row, n - 1)) * nbk;   // past-the-end rows: not stored
+        if (strip != sb + warp) prime(row0);      // the ring is empty: every copy of the last strip was used
+        float sc[S];
 #pragma unroll
-    for (int r = 0; r < MT; ++r) acc[r] = 0.0f;
-    for (int b0 = 0; b0 < nbk; b0 += S) {
-        const uint32_t par = static_cast<uint32_t>(b0 / S) & 1u;
+        for (int d = 0; d < S; ++d) sc[d] = __ldg(sp + min(d, nbk - 1));
+        float acc[MT];
 #pragma unroll
-        for (int d = 0; d < S; d += 2) {             // stages d, d + 1 hold blocks b0 + d, b0 + d + 1
-            const int b = b0 + d;
-            if (b >= nbk) break;
-            const bool two = b + 1 < nbk;
-            bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[d], par));
-            if (ok && two) ok = __all_sync(0xffffffffu, mbar_wait(&bars[d + 1], par));
-            if (!ok) {
+        for (int r = 0; r < MT; ++r) acc[r] = 0.0f;
+        for (int b0 = 0; b0 < nbk; b0 += S) {
+#pragma unroll
+            for (int d = 0; d < S; d += 2) {         // stages d, d + 1 hold blocks b0 + d, b0 + d + 1
+                const int b = b0 + d;
+                if (b >= nbk) break;
+                const bool two = b + 1 < nbk;
+                bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[d], ph[d] & 1u));
+                if (ok && two) ok = __all_sync(0xffffffffu, mbar_wait(&bars[d + 1], ph[d + 1] & 1u));
+                if (!ok) {
+                    if (lane == 0) {
+                        report_error(kErrWaitTimeout);
+                        // the copies still in flight: blocks [b, b + S) that exist, block c in stage
+                        // c % S, each the next phase of its stage
+#pragma unroll
+                        for (int e = 0; e < S; ++e) {
+                            const int c = b + ((e - d) + S) % S;
+                            if (c < nbk && !mbar_wait(&bars[e], ph[e] & 1u)) report_error(kErrDrainTimeout);
+                        }
+                    }
+                    return;                          // no block-wide barrier follows
+                }
+                ++ph[d];
+                if (two) ++ph[d + 1];
+                const uint4 a0 = lds128(ring + d * 1024 + swz32(lane, 0)), a1 = lds128(ring + d * 1024 + swz32(lane, 1));
+                uint4 c0 = a0, c1 = a1;
+                if (two) {
+                    c0 = lds128(ring + (d + 1) * 1024 + swz32(lane, 0));
+                    c1 = lds128(ring + (d + 1) * 1024 + swz32(lane, 1));
+                }
+                const float s0 = sc[d], s1 = sc[d + 1];
+                if (b + S < nbk) sc[d] = __ldg(sp + b + S);
+                if (b + 1 + S < nbk) sc[d + 1] = __ldg(sp + b + 1 + S);
+                __syncwarp();                        // every lane has read the two stages
                 if (lane == 0) {
-                    report_error(kErrWaitTimeout);
-                    for (int c = b; c < min(nbk, b + S); ++c)      // the copies still in flight
-                        if (!mbar_wait(&bars[c % S], static_cast<uint32_t>(c / S) & 1u)) report_error(kErrDrainTimeout);
+                    fence_proxy_async_smem();
+                    if (b + S < nbk) {
+                        mbar_arrive_expect_tx(&bars[d], 1024);
+                        tma_load_2d(ring + d * 1024, &tm, 32 * (b + S), row0, &bars[d]);
+                    }
+                    if (b + 1 + S < nbk) {
+                        mbar_arrive_expect_tx(&bars[d + 1], 1024);
+                        tma_load_2d(ring + (d + 1) * 1024, &tm, 32 * (b + 1 + S), row0, &bars[d + 1]);
+                    }
                 }
-                return;
-            }
-            const uint4 a0 = lds128(ring + d * 1024 + swz32(lane, 0)), a1 = lds128(ring + d * 1024 + swz32(lane, 1));
-            uint4 c0 = a0, c1 = a1;
-            if (two) {
-                c0 = lds128(ring + (d + 1) * 1024 + swz32(lane, 0));
-                c1 = lds128(ring + (d + 1) * 1024 + swz32(lane, 1));
-            }
-            const float s0 = sc[d], s1 = sc[d + 1];
-            if (b + S < nbk) sc[d] = __ldg(sp + b + S);
-            if (b + 1 + S < nbk) sc[d + 1] = __ldg(sp + b + 1 + S);
-            __syncwarp();                            // every lane has read the two stages
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                if (b + S < nbk) {
-                    mbar_arrive_expect_tx(&bars[d], 1024);
-                    tma_load_2d(ring + d * 1024, &tm, 32 * (b + S), row0, &bars[d]);
+                const uint32_t wq[2][8] = {{a0.x ^ 0x80808080u, a0.y ^ 0x80808080u, a0.z ^ 0x80808080u, a0.w ^ 0x80808080u,
+                                            a1.x ^ 0x80808080u, a1.y ^ 0x80808080u, a1.z ^ 0x80808080u, a1.w ^ 0x80808080u},
+                                           {c0.x ^ 0x80808080u, c0.y ^ 0x80808080u, c0.z ^ 0x80808080u, c0.w ^ 0x80808080u,
+                                            c1.x ^ 0x80808080u, c1.y ^ 0x80808080u, c1.z ^ 0x80808080u, c1.w ^ 0x80808080u}};
+                // the two blocks' sums are independent: their chains run side by side (a lone last
+                // block sums its own activations twice, the second copy unused)
+                const float* xb0 = xs + static_cast<size_t>(b) * 32 * MT;
+                const float* xb1 = two ? xb0 + 32 * MT : xb0;
+                float bs0[MT], bs1[MT];
+#pragma unroll
+                for (int r = 0; r < MT; ++r) bs0[r] = bs1[r] = 0.0f;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    accumulate_rows<MT>(bs0, xb0 + t * MT, q_of(wq[0][t >> 2], t & 3));
+                    accumulate_rows<MT>(bs1, xb1 + t * MT, q_of(wq[1][t >> 2], t & 3));
                 }
-                if (b + 1 + S < nbk) {
-                    mbar_arrive_expect_tx(&bars[d + 1], 1024);
-                    tma_load_2d(ring + (d + 1) * 1024, &tm, 32 * (b + 1 + S), row0, &bars[d + 1]);
+#pragma unroll
+                for (int r = 0; r < MT; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s0, bs0[r]));
+                if (two) {
+#pragma unroll
+                    for (int r = 0; r < MT; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s1, bs1[r]));
                 }
-            }
-            const uint32_t wq[2][8] = {{a0.x ^ 0x80808080u, a0.y ^ 0x80808080u, a0.z ^ 0x80808080u, a0.w ^ 0x80808080u,
-                                        a1.x ^ 0x80808080u, a1.y ^ 0x80808080u, a1.z ^ 0x80808080u, a1.w ^ 0x80808080u},
-                                       {c0.x ^ 0x80808080u, c0.y ^ 0x80808080u, c0.z ^ 0x80808080u, c0.w ^ 0x80808080u,
-                                        c1.x ^ 0x80808080u, c1.y ^ 0x80808080u, c1.z ^ 0x80808080u, c1.w ^ 0x80808080u}};
-            // the two blocks' sums are independent: their chains run side by side (a lone last
-            // block sums its own activations twice, the second copy unused)
-            const float* xb0 = xs + static_cast<size_t>(b) * 32 * MT;
-            const float* xb1 = two ? xb0 + 32 * MT : xb0;
-            float bs0[MT], bs1[MT];
-#pragma unroll
-            for (int r = 0; r < MT; ++r) bs0[r] = bs1[r] = 0.0f;
-#pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                accumulate_rows<MT>(bs0, xb0 + t * MT, q_of(wq[0][t >> 2], t & 3));
-                accumulate_rows<MT>(bs1, xb1 + t * MT, q_of(wq[1][t >> 2], t & 3));
-            }
-#pragma unroll
-            for (int r = 0; r < MT; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s0, bs0[r]));
-            if (two) {
-#pragma unroll
-                for (int r = 0; r < MT; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s1, bs1[r]));
             }
         }
-    }
-    // every copy issued has been waited for; the next launch may start its prologue
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (row < n) {
+        if (strip + W >= se) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // last strip
+        if (row < n) {
 #pragma unroll
-        for (int r = 0; r < MT; ++r)
-            if (m0 + r < m) y[static_cast<size_t>(m0 + r) * n + row] = acc[r];
+            for (int r = 0; r < MT; ++r)
+                if (m0 + r < m) y[static_cast<size_t>(m0 + r) * n + row] = acc[r];
+        }
     }
 }
 
 // The tensor-memory-accelerator strip kernel when its shared memory fits and the driver encodes
 // the codes' tensor map ([n] rows of k bytes, 32 x 32-byte boxes, 32-byte swizzle); returns
-// cudaErrorNotSupported otherwise, so the caller can take the register-streaming kernel.
+// cudaErrorNotSupported otherwise, so the caller can take the register-streaming kernel.  One
+// thread block per SM and tile of MT activation rows.
 template <int MT, int S, int W = kTmWarps>
 cudaError_t launch_tma(const float* x, const uint32_t* q, const float* s, float* y, int m, int k, int n,
                        cudaStream_t st) {
-    const size_t smem = tm_smem<MT, S, W>(k);
-    if (smem > kStSmemMax) return cudaErrorNotSupported;
+    const size_t need = tm_smem<MT, S, W>(k);
+    if (need > kStSmemMax) return cudaErrorNotSupported;
+    const size_t smem = need < kTmSmemOneBlock ? kTmSmemOneBlock : need;
     CUtensorMap tm;
     if (!make_tmap_2d_swizzle(&tm, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(k), static_cast<uint64_t>(n),
                               static_cast<uint64_t>(k), 32, 32, CU_TENSOR_MAP_SWIZZLE_32B))
         return cudaErrorNotSupported;
-    static int configured_dev = -1;
+    static int configured_dev = -1, sms = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -783,10 +807,13 @@ cudaError_t launch_tma(const float* x, const uint32_t* q, const float* s, float*
         e = cudaFuncSetAttribute(block_q8_tma_kernel<MT, S, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kStSmemMax));
         if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
+    const int strips = (n + 31) / 32;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((n + W * 32 - 1) / (W * 32), (m + MT - 1) / MT);
+    cfg.gridDim = dim3(strips < sms ? strips : sms, (m + MT - 1) / MT);
     cfg.blockDim = dim3(W * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -854,6 +881,10 @@ GQ_ERROR_ACCESSOR(block_q8)
 
 cudaError_t launch_block_q8(const float* x, const uint32_t* quants, const float* scales, float* y, int m, int k,
                             int n, cudaStream_t s) {
+    if (m == 2) {
+        const cudaError_t e = launch_tma<2, 4>(x, quants, scales, y, m, k, n, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     if (m <= 2) {
         // x rows 16-byte aligned for the activations' vector loads (k % 32 == 0 and x 16-aligned)
         if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
