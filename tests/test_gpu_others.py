@@ -25,7 +25,7 @@ def gq():
 @pytest.mark.parametrize("m,k,n", [(1, 32, 1), (1, 960, 1001), (3, 96, 513), (4, 960, 257), (7, 64, 33),
                                    (16, 960, 300), (17, 320, 129), (40, 128, 64), (2, 2048, 700), (1, 2080, 100),
                                    (4, 32, 33), (1, 960, 20000), (5, 2080, 300), (16, 4096, 40), (4, 8192, 33),
-                                   (3, 32, 1), (12, 960, 2000)])
+                                   (3, 32, 1), (12, 960, 2000), (4, 64, 60000), (2, 32, 60001), (16, 96, 56000)])
 def test_block_q8_bit_exact(gq, m, k, n):
     rng = wl.Rng(m * 1000 + k + n)
     x, quants, scales = wl.block_q8_inputs(rng, m, k, n)
