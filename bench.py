@@ -558,7 +558,7 @@ def run_only(args):
 
 
 PROBES = ("lut4_decode", "lut4_prefill", "wq8_gemv", "wq4_gemv", "wq8_gemm", "wq4_gemm", "wq8_mma", "wq4_mma",
-          "bq8_m1", "bq8_m4", "q1_gemm512_lut4", "q1_gemm512_dp4a", "q1_gemv_2560x6912")
+          "bq8_m1", "bq8_m4", "bq8_m16", "q1_gemm512_lut4", "q1_gemm512_dp4a", "q1_gemv_2560x6912")
 
 
 def run_probe(name):
@@ -578,7 +578,7 @@ def run_probe(name):
         f = (lambda: gq.q1_q8_gemm(packed, act, rows, n, cols, path=path)) if cols > 1 else \
             (lambda: gq.q1_q8_gemv(packed, act, rows, n))
     elif name.startswith("bq8"):
-        m = int(name[-1])
+        m = int(name.split("_m")[-1])
         x, q, sc = wl.block_q8_inputs(wl.Rng(20), m, 960, 49152)
         x, q, sc = (torch.from_numpy(a).cuda() for a in (x, q.view(np.int32), sc))
         f = lambda: gq.block_q8_matmul_nt(x, q, sc)
