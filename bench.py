@@ -703,6 +703,16 @@ def run_ours(args, rank, world, dist):
     ts = time.perf_counter() - t0
     ts = max_over_ranks(ts, dist, dev)
     e2e_sync_value = whole_job_rate(world, wbytes, e2e_steps, ts)
+    # every request's outputs as read back must be the device-resident result for its activations
+    e2e_pipelined(2)
+    e2e_ok = True
+    for b in range(2):
+        act_bufs[b].copy_(act_pins[b])
+        groups[b]()
+        torch.cuda.synchronize()
+        e2e_ok &= bool(torch.equal(y_bufs[b].cpu().view(torch.int32), y_pins[b].view(torch.int32)))
+    if not e2e_ok:
+        raise SystemExit("bench: the end-to-end outputs differ from the device-resident results")
 
     khash = kernel_hash(*GEMV_SOURCES)
     probes = run_probes(gq, torch, dev) if (rank == 0 and not args.no_probes) else None
@@ -727,7 +737,8 @@ def run_ours(args, rank, world, dist):
                 "mode": "independent requests, two buffer sets; H2D and D2H on their own streams overlapping the "
                         "neighbouring steps' launches; every step's outputs read back to pinned host memory",
                 "sync": {"value": round(e2e_sync_value, 2), "unit": UNIT,
-                         "mode": "one request at a time: copy in, launch, copy out, host wait, per step"}},
+                         "mode": "one request at a time: copy in, launch, copy out, host wait, per step"},
+                "outputs_checked": "both requests' read-back outputs equal the device-resident results bit for bit"},
         "gpu_launches": 2 * args.steps,     # per step: the activation-constants kernel and the GEMV
         "clocks": clk,
     }
