@@ -527,111 +527,6 @@ block_q8_strip_kernel(const float* __restrict__ x, const uint32_t* __restrict__ 
     }
 }
 
-// Four activation rows per grid row (any m >= 3 as tiles of four), activations read straight from
-// global memory: a lane owns one weight row and runs its blocks in order (pairs of blocks summed
-// side by side), and at each step all lanes read the same four activations of a row, a broadcast
-// 16-byte load that stays in L1 (the tile's activations are k * 16 bytes); the codes stream past
-// L1 without allocating.  No shared memory and no staging before the first block.
-__device__ __forceinline__ uint4 ld_codes(const uint4* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-
-template <int W, int D>
-__global__ void __launch_bounds__(W * 32)
-block_q8_regx_kernel(const float* __restrict__ x, const uint32_t* __restrict__ quants,
-                     const float* __restrict__ scales, float* __restrict__ y, int m, int k, int n) {
-    static_assert(D % 2 == 0, "blocks are summed in pairs");
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nbk = k / 32;
-    const int m0 = blockIdx.y * 4;
-    const int row = (blockIdx.x * W + warp) * 32 + lane;
-    const int rc = min(row, n - 1);                          // past-the-end rows: computed, not stored
-    const uint4* qp = reinterpret_cast<const uint4*>(quants) + static_cast<size_t>(rc) * (k / 16);
-    const float* sp = scales + static_cast<size_t>(rc) * nbk;
-    uint4 w0[D], w1[D];
-    float sc[D];
-#pragma unroll
-    for (int d = 0; d < D; ++d) {                           // weights: before the wait
-        const int b = min(d, nbk - 1);
-        w0[d] = ld_codes(qp + 2 * b);
-        w1[d] = ld_codes(qp + 2 * b + 1);
-        sc[d] = __ldg(sp + b);
-    }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // the tile's four activation rows (rows past m repeat row m - 1: computed, not stored)
-    const float4* xr[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) xr[r] = reinterpret_cast<const float4*>(x + static_cast<size_t>(min(m0 + r, m - 1)) * k);
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int b0 = 0; b0 < nbk; b0 += D) {
-#pragma unroll
-        for (int d = 0; d < D; d += 2) {
-            const int b = b0 + d;
-            if (b >= nbk) break;
-            const bool two = b + 1 < nbk;
-            const int b1 = two ? b + 1 : b;                  // a lone last block sums itself twice, once unused
-            uint32_t wq[2][8];
-            float s[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                wq[h][0] = w0[d + h].x ^ 0x80808080u; wq[h][1] = w0[d + h].y ^ 0x80808080u;
-                wq[h][2] = w0[d + h].z ^ 0x80808080u; wq[h][3] = w0[d + h].w ^ 0x80808080u;
-                wq[h][4] = w1[d + h].x ^ 0x80808080u; wq[h][5] = w1[d + h].y ^ 0x80808080u;
-                wq[h][6] = w1[d + h].z ^ 0x80808080u; wq[h][7] = w1[d + h].w ^ 0x80808080u;
-                s[h] = sc[d + h];
-                if (b + h + D < nbk) {
-                    w0[d + h] = ld_codes(qp + 2 * (b + h + D));
-                    w1[d + h] = ld_codes(qp + 2 * (b + h + D) + 1);
-                    sc[d + h] = __ldg(sp + b + h + D);
-                }
-            }
-            float bs0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, bs1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int tq = 0; tq < 8; ++tq) {
-                float4 xa[4], xb[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    xa[r] = __ldg(xr[r] + b * 8 + tq);
-                    xb[r] = __ldg(xr[r] + b1 * 8 + tq);
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float qa = q_of(wq[0][tq], i), qb = q_of(wq[1][tq], i);
-                    const float4 va = make_float4(i == 0 ? xa[0].x : i == 1 ? xa[0].y : i == 2 ? xa[0].z : xa[0].w,
-                                                  i == 0 ? xa[1].x : i == 1 ? xa[1].y : i == 2 ? xa[1].z : xa[1].w,
-                                                  i == 0 ? xa[2].x : i == 1 ? xa[2].y : i == 2 ? xa[2].z : xa[2].w,
-                                                  i == 0 ? xa[3].x : i == 1 ? xa[3].y : i == 2 ? xa[3].z : xa[3].w);
-                    const float4 vb = make_float4(i == 0 ? xb[0].x : i == 1 ? xb[0].y : i == 2 ? xb[0].z : xb[0].w,
-                                                  i == 0 ? xb[1].x : i == 1 ? xb[1].y : i == 2 ? xb[1].z : xb[1].w,
-                                                  i == 0 ? xb[2].x : i == 1 ? xb[2].y : i == 2 ? xb[2].z : xb[2].w,
-                                                  i == 0 ? xb[3].x : i == 1 ? xb[3].y : i == 2 ? xb[3].z : xb[3].w);
-                    float2 lo = fadd2(make_float2(bs0[0], bs0[1]), make_float2(__fmul_rn(va.x, qa), __fmul_rn(va.y, qa)));
-                    float2 hi = fadd2(make_float2(bs0[2], bs0[3]), make_float2(__fmul_rn(va.z, qa), __fmul_rn(va.w, qa)));
-                    bs0[0] = lo.x; bs0[1] = lo.y; bs0[2] = hi.x; bs0[3] = hi.y;
-                    lo = fadd2(make_float2(bs1[0], bs1[1]), make_float2(__fmul_rn(vb.x, qb), __fmul_rn(vb.y, qb)));
-                    hi = fadd2(make_float2(bs1[2], bs1[3]), make_float2(__fmul_rn(vb.z, qb), __fmul_rn(vb.w, qb)));
-                    bs1[0] = lo.x; bs1[1] = lo.y; bs1[2] = hi.x; bs1[3] = hi.y;
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s[0], bs0[r]));
-            if (two) {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) acc[r] = __fadd_rn(acc[r], __fmul_rn(s[1], bs1[r]));
-            }
-        }
-    }
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (row < n) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-            if (m0 + r < m) y[static_cast<size_t>(m0 + r) * n + row] = acc[r];
-    }
-}
-
 // The strip kernel with the codes brought in by the tensor-memory accelerator, persistent: one
 // thread block per SM stages the tile's activations once, and takes an even share of the 32-row
 // strips (ceil(n / 32) of them over the grid: every SM gets the same number to within one), its
