@@ -14,7 +14,10 @@
 //  * warp l of the first eight runs acc[l] = fma(d0, ab[l], acc[l]) over the step's blocks in order;
 //  * at the end warp 0 adds each row's eight accumulators in the pages' order.
 // The table rows are 17 words apart, so the builders' stores and the 32 lanes' lookups (at most 16
-// distinct words of one table) are free of bank conflicts.
+// distinct words of one table) are free of bank conflicts.  The next step's weight and activation
+// words are loaded into registers while the current step is summed, so a step costs its work
+// rather than a round trip to memory; the kernel is launched as a programmatic dependent, its
+// first step's weights requested before the wait for the preceding grids.
 #include "gq_internal.cuh"
 
 namespace gq {
@@ -38,22 +41,54 @@ q1_gemv_raw_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ 
     const int row0 = blockIdx.x * kRawRows;
     const size_t row_halves = static_cast<size_t>(nb) * 9;          // 18 bytes per block
     float chain = 0.0f;                                             // warps 0..7: lane group `warp`
+    constexpr int kPer = kRawRows * kRawHalves / (kRawStep * 32);   // staged words per thread (9)
+    static_assert(kPer * kRawStep * 32 == kRawRows * kRawHalves, "whole words per thread");
+    const int k = lane >> 3, l = lane & 7;                          // a table builder's (sub-block, lane)
+
+    // the weight words of step b0 (thread t: items t, t + 256, ...) and the activation words of its
+    // table (warp j: block b0 + j)
+    uint16_t wn[kPer];
+    auto load_w = [&](int b0) {
+        const int nbs = min(kRawStep, nb - b0);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int u = threadIdx.x + i * kRawStep * 32;
+            const int r = u / kRawHalves, o = u % kRawHalves;
+            wn[i] = (row0 + r < rows && o < nbs * 9) ? w[static_cast<size_t>(row0 + r) * row_halves + b0 * 9 + o]
+                                                     : static_cast<uint16_t>(0);
+        }
+    };
+    uint16_t an[3];
+    auto load_a = [&](int b0) {
+        if (b0 + warp < nb) {
+            const uint16_t* blk = act + static_cast<size_t>(4 * (b0 + warp) + k) * 17;    // 34-byte Q8_0 block
+            an[0] = blk[0];
+            an[1] = blk[1 + 2 * l];
+            an[2] = blk[2 + 2 * l];
+        }
+    };
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    load_w(0);                                                      // weights: before the wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");              // the activations are ready
+    load_a(0);
 
     for (int b0 = 0; b0 < nb; b0 += kRawStep) {
         const int nbs = min(kRawStep, nb - b0);
-        // stage the step's raw weight bytes
-        for (int u = threadIdx.x; u < kRawRows * kRawHalves; u += blockDim.x) {
-            const int r = u / kRawHalves, o = u % kRawHalves;
-            uint16_t v = 0;
-            if (row0 + r < rows && o < nbs * 9) v = w[static_cast<size_t>(row0 + r) * row_halves + b0 * 9 + o];
-            s_w[r][o] = v;
+        // stage the step's raw weight words, then request the next step's
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int u = threadIdx.x + i * kRawStep * 32;
+            s_w[u / kRawHalves][u % kRawHalves] = wn[i];
+        }
+        const uint16_t a0 = an[0], a1 = an[1], a2 = an[2];
+        if (b0 + kRawStep < nb) {
+            load_w(b0 + kRawStep);
+            load_a(b0 + kRawStep);
         }
         // tables of block j = warp of the step
         if (warp < nbs) {
-            const int k = lane >> 3, l = lane & 7;
-            const uint16_t* blk = act + static_cast<size_t>(4 * (b0 + warp) + k) * 17;    // 34-byte Q8_0 block
-            const float d1 = f16_to_f32(blk[0]);
-            const uint32_t qw = static_cast<uint32_t>(blk[1 + 2 * l]) | (static_cast<uint32_t>(blk[2 + 2 * l]) << 16);
+            const float d1 = f16_to_f32(a0);
+            const uint32_t qw = static_cast<uint32_t>(a1) | (static_cast<uint32_t>(a2) << 16);
             int pos[4], neg[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -71,22 +106,22 @@ q1_gemv_raw_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ 
             }
         }
         __syncthreads();
-        // ab of block j = warp for the 32 rows
+        // ab of block j = warp for the 32 rows (the builders' k, l above name their own item)
         if (warp < nbs) {
             const uint16_t* wr = &s_w[lane][9 * warp];
             const float* tab = s_tab[warp];
             float ab[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t wk = static_cast<uint32_t>(wr[1 + 2 * k]) | (static_cast<uint32_t>(wr[2 + 2 * k]) << 16);
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t wk = static_cast<uint32_t>(wr[1 + 2 * kk]) | (static_cast<uint32_t>(wr[2 + 2 * kk]) << 16);
 #pragma unroll
-                for (int l = 0; l < 8; ++l) {
-                    const float p = tab[(8 * k + l) * kTabStride + ((wk >> (4 * l)) & 0xFu)];
-                    ab[l] = (k == 0) ? p : __fadd_rn(ab[l], p);
+                for (int ll = 0; ll < 8; ++ll) {
+                    const float p = tab[(8 * kk + ll) * kTabStride + ((wk >> (4 * ll)) & 0xFu)];
+                    ab[ll] = (kk == 0) ? p : __fadd_rn(ab[ll], p);
                 }
             }
 #pragma unroll
-            for (int l = 0; l < 8; ++l) s_ab[warp][l][lane] = ab[l];
+            for (int ll = 0; ll < 8; ++ll) s_ab[warp][ll][lane] = ab[ll];
             s_d0[warp][lane] = f16_to_f32(wr[0]);
         }
         __syncthreads();
@@ -123,9 +158,18 @@ __global__ void pack_q8_0_kernel(const uint16_t* __restrict__ raw, long long blo
 }  // namespace
 
 cudaError_t launch_q1_gemv_raw(const void* w, const void* act, float* y, int rows, int n, cudaStream_t s) {
-    q1_gemv_raw_kernel<<<(rows + kRawRows - 1) / kRawRows, kRawStep * 32, 0, s>>>(
-        static_cast<const uint16_t*>(w), static_cast<const uint16_t*>(act), y, rows, n / 128);
-    return cudaGetLastError();
+    // a programmatic dependent of the previous launch on the stream (see the kernel)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((rows + kRawRows - 1) / kRawRows);
+    cfg.blockDim = dim3(kRawStep * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, q1_gemv_raw_kernel, static_cast<const uint16_t*>(w),
+                              static_cast<const uint16_t*>(act), y, rows, n / 128);
 }
 
 cudaError_t launch_pack_q8_0(const void* raw, int cols, int n, float* d, uint32_t* q, cudaStream_t s) {
