@@ -77,7 +77,7 @@ def _oracle(bits, w, scale, x, T, N, K):
 @pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("T,N,K", [(1, 1, 32), (1, 77, 96), (1, 1000, 544), (2, 129, 4128), (3, 40, 1024),
                                    (4, 300, 2560), (5, 257, 160), (33, 130, 1056), (130, 300, 512),
-                                   (1, 3000, 16384)])
+                                   (1, 3000, 16384), (1, 97, 5152), (1, 50, 24608)])
 def test_within_bound(gq, bits, T, N, K):
     w, scale, x = wl.wq_inputs(wl.Rng(1000 * bits + T + N + K), T, K, N, bits, p_m8=0.02)
     _check(bits, _run(gq, bits, w, scale, x), _oracle(bits, w, scale, x, T, N, K), w, scale, x, T, N, K)
