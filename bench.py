@@ -240,6 +240,21 @@ def run_probes(gq, torch, dev):
     }
 
 
+def ternary_alu_seconds(b, probes, rows=14336, k=4096):
+    """Issue time of the ternary kernel's counting at batch b: per 32 words of a row, one LOP3 mask
+    per word and activation, 30 carry-save adders (two LOP3 each) and 6 POPC per activation and per
+    plane (P, N).  Whether LOP3 and POPC share a pipe is read off the interleaved probe: shared
+    pipes give 2 / (1/r_lop3 + 1/r_popc) warp instructions per SM-cycle, separate ones 2 min(r)."""
+    iss = probes["issue_warp_inst_per_sm_cycle"]
+    rl, rp, rm = iss["lop3"], iss["popc"], iss.get("lop3+popc")
+    units = rows * (k // 32) / 32.0                      # warp instructions per op per (row, word)
+    n_lop3 = units * (3.75 + 2.875 * b)
+    n_popc = units * (0.375 + 0.1875 * b)
+    shared = rm is None or abs(rm - 2.0 / (1.0 / rl + 1.0 / rp)) <= abs(rm - 2.0 * min(rl, rp))
+    cyc = (n_lop3 / rl + n_popc / rp) if shared else max(n_lop3 / rl, n_popc / rp)
+    return cyc / probes["sm_count"] / probes["sm_clock_hz"]
+
+
 def add_bounds(kernels, probes):
     """Each secondary measurement's fraction of its own bound, from the probes of this run."""
     rd = probes["hbm_read_GBps"]
@@ -256,9 +271,14 @@ def add_bounds(kernels, probes):
             m, n, k = 16, 49152, 960
             e["bound"] = "fp32_issue"
             e["frac_of_bound"] = round(2.0 * m * n * k / (e["us"] * 1e-6) / fp, 4)
-        if name == "ternary_b16":
-            e["bound"] = "popc_issue"
-            e["frac_of_bound"] = round(e["Gpopc_per_s"] * 1e9 / probes["popc_per_s"], 4)
+        if name.startswith("ternary_b"):
+            # the larger of the weight stream and the LOP3/POPC issue of the carry-save counting
+            t_alu = ternary_alu_seconds(int(name[len("ternary_b"):]), probes)
+            t_hbm = (2 * 14336 * 4096 // 8) / (rd * 1e9)
+            if t_alu > t_hbm:
+                e["bound"] = "alu_issue (lop3 + popc, carry-save counting)"
+                e["frac_of_bound"] = round(t_alu / (e["us"] * 1e-6), 4)
+            e["alu_bound_us"] = round(t_alu * 1e6, 2)
         if name.startswith("w1a32_decode"):
             e["bound"] = "hbm_read"
             e["lut4_frac_of_bound"] = round(e["lut4_weight_GBps"] / rd, 4)
@@ -332,41 +352,47 @@ def bench_block_q8(gq, torch, dev, hbm_peak, steps=40, warmup=5):
     return out
 
 
+def rotating_copies(torch, tensors, total_bytes=300_000_000):
+    """Enough distinct device copies of one weight set that a call never finds its weights in L2:
+    copy c holds the rows rotated by 131 c (same values and distribution, different bytes where
+    they sit), and all copies together hold at least `total_bytes`."""
+    per = sum(t.numel() * t.element_size() for t in tensors)
+    n = max(2, -(-total_bytes // per))
+    return [tuple(torch.roll(t, shifts=131 * c, dims=0).contiguous() for t in tensors) for c in range(n)]
+
+
 def bench_ternary(gq, torch, dev, hbm_peak, steps=80, warmup=8):
-    """Ternary 14336 x 4096 at batch 1, 4, 16; 8 rotating copies (8 x 14.7 MB > L2); device time
-    from CUDA-graph replay."""
+    """Ternary 14336 x 4096 at batch 1, 4, 16; rotating weight copies (>= 300 MB in all, more than
+    L2); device time from CUDA-graph replay."""
     out = {}
     rows, kk = 14336, 4096
-    planes = []
-    for c in range(8):
-        P, N, _ = wl.ternary_inputs(wl.Rng(40 + c), rows, kk, 1)
-        planes.append((torch.from_numpy(P.view(np.int32)).to(dev), torch.from_numpy(N.view(np.int32)).to(dev)))
+    P, N, _ = wl.ternary_inputs(wl.Rng(40), rows, kk, 1)
+    planes = rotating_copies(torch, (torch.from_numpy(P.view(np.int32)).to(dev),
+                                     torch.from_numpy(N.view(np.int32)).to(dev)))
     for b in (1, 4, 16):
         X = torch.from_numpy(wl.Rng(60 + b).u32(b * kk // 32).reshape(b, kk // 32).view(np.int32)).to(dev)
         y = torch.empty((b, rows), dtype=torch.int32, device=dev)
         it = [0]
 
         def f():
-            i = it[0] % 8
+            i = it[0] % len(planes)
             it[0] += 1
             gq.ternary_bitplane_gemv(planes[i][0], planes[i][1], X, out=y)
         t = time_graph(f, steps, warmup)
         wbytes = 2 * rows * kk // 8
         out[f"ternary_b{b}"] = {"us": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
                                 "hbm_frac": round(wbytes / t / 1e9 / hbm_peak, 4),
-                                "Gpopc_per_s": round(rows * (kk // 32) * (b + 2) / t / 1e9, 1)}
+                                "Gword_popcounts_per_s": round(rows * (kk // 32) * (b + 2) / t / 1e9, 1)}
     return out
 
 
 def bench_w1a32(gq, torch, dev, hbm_peak, steps=40, warmup=5):
-    """Bonsai 1-bit weights x f32 activations.  Decode: 14336 x 4096 at one token, 10 rotating
-    weight copies (10 x 14.7 MB > L2), both paths, device time from CUDA-graph replay.  Prefill:
-    512 tokens through the LUT4 path (and FMA for comparison)."""
+    """Bonsai 1-bit weights x f32 activations.  Decode: 14336 x 4096 at one token, rotating weight
+    copies (>= 300 MB in all, more than L2), both paths, device time from CUDA-graph replay.
+    Prefill: 512 tokens through the LUT4 path (and FMA for comparison)."""
     N, K = 14336, 4096
-    copies = []
-    for c in range(10):
-        signs, ws, _ = wl.prefill_inputs(wl.Rng(70 + c), 1, K, N)
-        copies.append((torch.from_numpy(signs.view(np.int32)).to(dev), torch.from_numpy(ws).to(dev)))
+    signs, ws, _ = wl.prefill_inputs(wl.Rng(70), 1, K, N)
+    copies = rotating_copies(torch, (torch.from_numpy(signs.view(np.int32)).to(dev), torch.from_numpy(ws).to(dev)))
     x = torch.from_numpy(wl.f32_normal(wl.Rng(80), K).reshape(1, K)).to(dev)
     y = torch.empty((1, N), dtype=torch.float32, device=dev)
     wbytes = N * (K // 32) * 8
@@ -465,19 +491,31 @@ def bench_prefill(gq, torch, dev, bf16_peak, steps=5, warmup=2, paths=("lut4", "
 
 def bench_q1_gemm(gq, torch, dev, hbm_peak, cols_list=(4, 64, 512)):
     """Token-tiled Q1_0 . Q8_0 GEMM (q1_q8_gemm) on a BitNet-2B FFN shape, 6912 x 2560 weights, for
-    `cols` activation vectors, DP4A and LUT4 paths: device time per call by CUDA-graph replay."""
+    `cols` activation vectors, DP4A and LUT4 paths: device time per call by CUDA-graph replay over
+    rotating weight copies (more bytes than L2)."""
     rows, n = 6912, 2560
     rng = wl.Rng(7)
     w = wl.q1_0_weights(rng, rows, n)
     packed = gq.q1_0_pack(torch.from_numpy(w).to(dev), rows, n)
+    # rotating copies, >= 300 MB in all, every one captured in the graph: the weights come from HBM
+    # as in a decode batch (each copy has the packed (tile, block) chunks of 2,304 bytes rotated,
+    # a valid packed matrix)
+    chunks = packed.view(-1, 2304)
+    copies = rotating_copies(torch, (chunks,))
+    copies = [c[0].view(-1) for c in copies]
     wbytes = rows * (n // 128) * 18
     res = {}
     for cols in cols_list:
         act = torch.from_numpy(wl.q8_0_acts(rng, cols, n)).to(dev)
         y = torch.empty((cols, rows), dtype=torch.float32, device=dev)
         for name, path in (("dp4a", gq.PATH_DP4A), ("lut4", gq.PATH_LUT4)):
-            calls = 20 if cols <= 64 else 3
-            t = time_graph(lambda: gq.q1_q8_gemm(packed, act, rows, n, cols, path=path, out=y), calls, 2, reps=3)
+            it = [0]
+
+            def f():
+                i = it[0] % len(copies)
+                it[0] += 1
+                gq.q1_q8_gemm(copies[i], act, rows, n, cols, path=path, out=y)
+            t = time_graph(f, len(copies), 2, reps=3 if cols <= 64 else 1)
             res[f"cols{cols}_{name}_us"] = round(t * 1e6, 2)
             res[f"cols{cols}_{name}_GOPs"] = round(2.0 * rows * n * cols / t / 1e9, 1)
         res[f"cols{cols}_weight_GBps_best"] = round(wbytes / (min(res[f"cols{cols}_dp4a_us"], res[f"cols{cols}_lut4_us"]) * 1e-6) / 1e9, 1)
@@ -558,12 +596,13 @@ def run_only(args):
 
 
 PROBES = ("lut4_decode", "lut4_prefill", "wq8_gemv", "wq4_gemv", "wq8_gemm", "wq4_gemm", "wq8_mma", "wq4_mma",
-          "bq8_m1", "bq8_m4", "bq8_m16", "q1_gemm512_lut4", "q1_gemm512_dp4a", "q1_gemv_2560x6912")
+          "bq8_m1", "bq8_m4", "bq8_m16", "q1_gemm512_lut4", "q1_gemm512_dp4a", "q1_gemv_2560x6912",
+          "tern_b1", "tern_b16")
 
 
 def run_probe(name):
-    """Three untimed calls of one kernel on its workload (14336 x 4096; one token or 512), for a
-    profiler to capture; prints a checksum."""
+    """Three untimed calls of one kernel on its workload (14336 x 4096; one token or 512, or the
+    ternary batch), for a profiler to capture; prints a checksum."""
     import torch
     import gemm_q1_q8_gb300 as gq
     N, K = 14336, 4096
@@ -577,6 +616,11 @@ def run_probe(name):
         path = gq.PATH_LUT4 if name.endswith("lut4") else gq.PATH_DP4A
         f = (lambda: gq.q1_q8_gemm(packed, act, rows, n, cols, path=path)) if cols > 1 else \
             (lambda: gq.q1_q8_gemv(packed, act, rows, n))
+    elif name.startswith("tern"):
+        b = int(name.split("_b")[-1])
+        P, Nn, X = wl.ternary_inputs(wl.Rng(40), 14336, 4096, b)
+        P, Nn, X = (torch.from_numpy(a.view(np.int32)).cuda() for a in (P, Nn, X))
+        f = lambda: gq.ternary_bitplane_gemv(P, Nn, X).float()
     elif name.startswith("bq8"):
         m = int(name.split("_m")[-1])
         x, q, sc = wl.block_q8_inputs(wl.Rng(20), m, 960, 49152)

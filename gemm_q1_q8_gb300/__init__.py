@@ -479,7 +479,7 @@ PROBE_KINDS = {
     "ffma": 0, "ffma2": 1, "fadd2": 2, "fadd": 3, "dp4a": 4, "lop3": 5, "popc": 6, "prmt": 7, "shf": 8,
     "imad": 9, "shfl": 10, "lds": 11, "dp4a+ffma2": 12, "lds+shfl": 13, "ffma+ffma2": 14, "lop3+dp4a": 15,
     "fadd+ffma2": 16, "lop3+ffma2": 17, "mma_sync_f16": 18, "mma_sync_bf16": 19, "mma_sync_e4m3": 20,
-    "mma_sync_s8": 21, "mma_sync_f16_mix": 22, "mma_sync_e4m3_mix": 23,
+    "mma_sync_s8": 21, "mma_sync_f16_mix": 22, "mma_sync_e4m3_mix": 23, "lop3+popc": 24,
 }
 PROBE_MMA_F16, PROBE_MMA_F8, PROBE_MMA_F16_TMEM_A = 0, 1, 2
 

@@ -181,6 +181,9 @@ __device__ __forceinline__ void issue_round(uint32_t (&u)[kIssueChains], float (
             case GQ_PROBE_LOP3_FFMA2:
                 if (j & 1) op_ffma2(g[j], g1, g2); else op_lop3(u[j], 0x5A5A5A5Au, 0x33333333u);
                 break;
+            case GQ_PROBE_LOP3_POPC:
+                if (j & 1) op_popc(u[j]); else op_lop3(u[j], 0x5A5A5A5Au, 0x33333333u);
+                break;
             // The A operand is the chain's previous result (bits masked to keep it small and finite),
             // so no operand conversion can be hoisted out of the loop: e4m3 operands are converted in
             // the issuing warp on this GPU, and that cost belongs to the rate.
@@ -450,6 +453,7 @@ extern "C" int gq_probe_issue(int kind, int iters, unsigned long long* cycles_de
         GQ_PROBE_CASE(GQ_PROBE_IMMA_S8)
         GQ_PROBE_CASE(GQ_PROBE_HMMA_MIX)
         GQ_PROBE_CASE(GQ_PROBE_QMMA_MIX)
+        GQ_PROBE_CASE(GQ_PROBE_LOP3_POPC)
 #undef GQ_PROBE_CASE
         default: return GQ_EINVAL_SHAPE;
     }

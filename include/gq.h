@@ -431,7 +431,8 @@ enum gq_probe_kind {
     GQ_PROBE_IMMA_S8 = 21,      /* mma.sync m16n8k32 s8 x s8 + s32 (8192 op)           */
     GQ_PROBE_HMMA_MIX = 22,     /* f16 mma.sync : lop3 : lop3 : fma.rn.f32, 1:2:1      */
     GQ_PROBE_QMMA_MIX = 23,     /* e4m3 mma.sync : lop3 : lop3 : fma.rn.f32, 1:2:1     */
-    GQ_PROBE_ISSUE_KINDS = 24
+    GQ_PROBE_LOP3_POPC = 24,    /* lop3 and popc interleaved               */
+    GQ_PROBE_ISSUE_KINDS = 25
 };
 
 /* Instruction issue rate: one block of 32 warps per SM runs `iters` loop iterations of 32
