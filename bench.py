@@ -241,15 +241,17 @@ def run_probes(gq, torch, dev):
 
 
 def ternary_alu_seconds(b, probes, rows=14336, k=4096):
-    """Issue time of the ternary kernel's counting at batch b: per 32 words of a row, one LOP3 mask
-    per word and activation, 30 carry-save adders (two LOP3 each) and 6 POPC per activation and per
-    plane (P, N).  Whether LOP3 and POPC share a pipe is read off the interleaved probe: shared
-    pipes give 2 / (1/r_lop3 + 1/r_popc) warp instructions per SM-cycle, separate ones 2 min(r)."""
+    """Issue time of the ternary kernel's counting at batch b.  Per activation and 32 words of a
+    row: 32 LOP3 masks, four 7-word adder groups (4 adders of two LOP3, 3 POPC each) and one triple
+    (one adder, 2 POPC) and a single word: 66 LOP3 and 15 POPC.  Per 64 words of P and N: nine
+    groups and a single word, 72 LOP3 and 28 POPC.  Whether LOP3 and POPC share a pipe is read off
+    the interleaved probe: shared pipes give 2 / (1/r_lop3 + 1/r_popc) warp instructions per
+    SM-cycle, separate ones 2 min(r)."""
     iss = probes["issue_warp_inst_per_sm_cycle"]
     rl, rp, rm = iss["lop3"], iss["popc"], iss.get("lop3+popc")
     units = rows * (k // 32) / 32.0                      # warp instructions per op per (row, word)
-    n_lop3 = units * (3.75 + 2.875 * b)
-    n_popc = units * (0.375 + 0.1875 * b)
+    n_lop3 = units * (66.0 * b + 72.0) / 32.0
+    n_popc = units * (15.0 * b + 28.0) / 32.0
     shared = rm is None or abs(rm - 2.0 / (1.0 / rl + 1.0 / rp)) <= abs(rm - 2.0 * min(rl, rp))
     cyc = (n_lop3 / rl + n_popc / rp) if shared else max(n_lop3 / rl, n_popc / rp)
     return cyc / probes["sm_count"] / probes["sm_clock_hz"]

@@ -5,9 +5,11 @@
 // Evaluated as dot = 2*popc((P & X) | (N & ~X)) - popc(P) - popc(N): the two masked sets are
 // disjoint when P & N = 0, and a position with both bits set contributes 2 - 2 = 0 either way,
 // so this is the same integer for every input -- one LOP3 per word and activation.  The popcounts
-// of a chunk row's 32 words are summed by a carry-save adder tree (Harley and Seal's method: full
-// adders on whole words keep bit-sliced counters of weight 1, 2, 4, 8 and 16), which needs 6
-// POPC and 60 LOP3 instead of 32 POPC; POPC issues at a quarter of LOP3's rate.
+// of a chunk row's 32 words are summed through carry-save adders (full adders on whole words, the
+// idea of Harley and Seal's popcount): each group of seven words goes through four adders into
+// counters of weight 1, 2 and 4, so 32 words take 34 LOP3 and 15 POPC instead of 32 POPC.  POPC
+// issues at a quarter of LOP3's rate on a pipe of its own; this split keeps both pipes about
+// equally busy (a full adder tree, 60 LOP3 and 6 POPC, left the POPC pipe idle and ran slower).
 //
 // The result is an integer sum, so K can be cut anywhere without changing it.  A thread block
 // covers `rt` rows (a multiple of 32, sized so that the row tiles fill the GPU once) and up to
@@ -60,33 +62,34 @@ __device__ __forceinline__ void csa(uint32_t& h, uint32_t& l, uint32_t a, uint32
     l = a ^ b ^ c;
 }
 
-// sum over j < 32 of popc(word(j)): two rounds of 16 words through the adder tree, the weight-16
-// carries counted per round and the lower counters at the end
-template <class F>
-__device__ __forceinline__ int popc32_csa(F word) {
-    uint32_t ones = 0, twos = 0, fours = 0, eights = 0;
-    int n16 = 0;
+// sum over j < NW of popc(word(j)): groups of seven words through four adders (7 -> counters of
+// weight 1, 2 and 4: three POPC), then a triple, then single words; about as much POPC issue as
+// LOP3 issue, which run on separate pipes
+template <int NW, class F>
+__device__ __forceinline__ int popc_sum(F word) {
+    int c1 = 0, c2 = 0, c4 = 0;
 #pragma unroll
-    for (int i = 0; i < 32; i += 16) {
-        uint32_t tA, tB, fA, fB, eA, eB, s16;
-        csa(tA, ones, ones, word(i), word(i + 1));
-        csa(tB, ones, ones, word(i + 2), word(i + 3));
-        csa(fA, twos, twos, tA, tB);
-        csa(tA, ones, ones, word(i + 4), word(i + 5));
-        csa(tB, ones, ones, word(i + 6), word(i + 7));
-        csa(fB, twos, twos, tA, tB);
-        csa(eA, fours, fours, fA, fB);
-        csa(tA, ones, ones, word(i + 8), word(i + 9));
-        csa(tB, ones, ones, word(i + 10), word(i + 11));
-        csa(fA, twos, twos, tA, tB);
-        csa(tA, ones, ones, word(i + 12), word(i + 13));
-        csa(tB, ones, ones, word(i + 14), word(i + 15));
-        csa(fB, twos, twos, tA, tB);
-        csa(eB, fours, fours, fA, fB);
-        csa(s16, eights, eights, eA, eB);
-        n16 += __popc(s16);
+    for (int i = 0; i + 7 <= NW; i += 7) {
+        uint32_t a1, s1, a2, s2, a3, s, f, t;
+        csa(a1, s1, word(i), word(i + 1), word(i + 2));
+        csa(a2, s2, word(i + 3), word(i + 4), word(i + 5));
+        csa(a3, s, s1, s2, word(i + 6));
+        csa(f, t, a1, a2, a3);
+        c1 += __popc(s);
+        c2 += __popc(t);
+        c4 += __popc(f);
     }
-    return 16 * n16 + 8 * __popc(eights) + 4 * __popc(fours) + 2 * __popc(twos) + __popc(ones);
+    constexpr int r0 = NW - NW % 7;
+#pragma unroll
+    for (int i = r0; i + 3 <= NW; i += 3) {
+        uint32_t h, l;
+        csa(h, l, word(i), word(i + 1), word(i + 2));
+        c1 += __popc(l);
+        c2 += __popc(h);
+    }
+#pragma unroll
+    for (int i = r0 + (NW - r0) / 3 * 3; i < NW; ++i) c1 += __popc(word(i));
+    return c1 + 2 * c2 + 4 * c4;
 }
 
 __global__ void __launch_bounds__(kMaxThreads)
@@ -148,14 +151,13 @@ ternary_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ 
                 p4[j] = *reinterpret_cast<const uint4*>(Pt + swz128(r, j));
                 n4[j] = *reinterpret_cast<const uint4*>(Nt + swz128(r, j));
             }
-            const int pn = popc32_csa([&](int j) { return u4w(p4[j >> 2], j & 3); }) +
-                           popc32_csa([&](int j) { return u4w(n4[j >> 2], j & 3); });
+            const int pn = popc_sum<64>([&](int j) { return j < 32 ? u4w(p4[j >> 2], j & 3) : u4w(n4[(j - 32) >> 2], j & 3); });
             atomicAdd(&pnr[r], pn);
             for (int b = 0; b < batch; ++b) {
                 uint4 x4[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) x4[j] = Xt[b * 8 + j];
-                const int cnt = popc32_csa([&](int j) {
+                const int cnt = popc_sum<32>([&](int j) {
                     const uint32_t x = u4w(x4[j >> 2], j & 3);
                     return (u4w(p4[j >> 2], j & 3) & x) | (u4w(n4[j >> 2], j & 3) & ~x);
                 });
