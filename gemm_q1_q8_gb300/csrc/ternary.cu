@@ -12,10 +12,10 @@
 // equally busy (a full adder tree, 60 LOP3 and 6 POPC, left the POPC pipe idle and ran slower).
 //
 // The result is an integer sum, so K can be cut anywhere without changing it.  A thread block
-// covers `rt` rows (a multiple of 32, sized so that the row tiles fill the GPU once) and up to
-// four 1024-bit K chunks: all of its P, N and X chunks are requested at once by TMA (128-byte
-// swizzle for P/N: conflict-free 16-byte reads per row), and four warp groups -- one per chunk,
-// one thread per row -- count their chunk and add into shared-memory totals.  K beyond four
+// covers `rt` rows (a multiple of 16 or 32, sized so that the row tiles fill the GPU once) and up
+// to four 1024-bit K chunks: all of its P, N and X chunks are requested at once by TMA (128-byte
+// swizzle for P/N: conflict-free 16-byte reads per row), and four groups of rt threads -- one per
+// chunk, one thread per row -- count their chunk and add into shared-memory totals.  K beyond four
 // chunks goes to more thread blocks of the same rows, which add their totals into y (zeroed on
 // the stream first); with K <= 4096 y is written once.
 //
@@ -132,8 +132,12 @@ ternary_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ 
     for (int i = threadIdx.x; i < rt; i += blockDim.x) pnr[i] = 0;
     __syncthreads();
 
+    // a warp may hold rows of two chunk groups (rt a multiple of 16): after the waits its threads
+    // count together
+    const bool landed = g < nch && mbar_wait(&bars[g], 0);
+    __syncwarp();
     if (g < nch) {
-        if (!mbar_wait(&bars[g], 0)) {
+        if (!landed) {
             // let the copy land (bounded) before the thread block can exit
             if (r == 0) {
                 report_error(kErrWaitTimeout);
@@ -205,13 +209,19 @@ cudaError_t launch_ternary(const uint32_t* P, const uint32_t* N, const uint32_t*
     // threads (four per row) and shared memory
     int max_rt = kMaxThreads / kChunksPerCta;
     while (max_rt > 32 && tern_layout(max_rt, batch).bytes + 1024 > 227u * 1024u) max_rt -= 32;
+    // rows per block in multiples of 32 (each chunk group whole warps), or of 16 at one activation:
+    // there the even split (48-row blocks, 96 rows on every SM for 14,336 rows, against 64-row
+    // blocks leaving 128 rows on some SMs) pays, 2.74 -> 2.65 us; with more activations a warp
+    // holding rows of two chunk groups waits for the later chunk before it counts (batch 4: 4.27
+    // against 3.58 us)
+    const int rq = batch == 1 ? 16 : 32;
     // thread blocks per SM: at a few activations the launch is a short fetch-bound wave, and two
     // smaller blocks per SM let one block's counting overlap the other's fetch (batch 1: 3.5 ->
     // 3.1 us; three per SM measured 3.8 us); at batch 16 the popcount work favours one larger block
     const int per_sm = batch <= 4 ? 2 : 1;
     const int want_tiles = per_sm * sms / slices > 0 ? per_sm * sms / slices : 1;
-    int rt = ((rows + want_tiles - 1) / want_tiles + 31) / 32 * 32;
-    if (rt < 32) rt = 32;
+    int rt = ((rows + want_tiles - 1) / want_tiles + rq - 1) / rq * rq;
+    if (rt < rq) rt = rq;
     if (rt > max_rt) rt = max_rt;
     const size_t smem = tern_layout(rt, batch).bytes + 1024;
 

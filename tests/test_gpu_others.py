@@ -65,7 +65,7 @@ def test_block_q8_full_size_sampled(gq, m):
 # ----------------------------------------------------------------------------- ternary
 
 @pytest.mark.parametrize("rows,k,batch,pz", [(1, 1024, 1, 0.4), (130, 2048, 3, 0.4), (300, 4096, 16, 0.0),
-                                             (129, 1024, 17, 1.0), (64, 8192, 64, 0.4)])
+                                             (129, 1024, 17, 1.0), (64, 8192, 64, 0.4), (1000, 4096, 1, 0.4)])
 def test_ternary_exact(gq, rows, k, batch, pz):
     P, N, X = wl.ternary_inputs(wl.Rng(rows + k + batch), rows, k, batch, p_zero=pz)
     y = gq.ternary_bitplane_gemv(to_dev(P), to_dev(N), to_dev(X)).cpu().numpy()
@@ -78,6 +78,26 @@ def test_ternary_overlapping_planes(gq):
     N = P | wl.Rng(5).u32(P.size).reshape(P.shape)
     y = gq.ternary_bitplane_gemv(to_dev(P), to_dev(N), to_dev(X)).cpu().numpy()
     assert np.array_equal(y, oracle.ternary_direct(P, N, X, rows, k, batch))
+
+
+@pytest.mark.parametrize("pattern", ["p_ones", "n_ones", "both_ones"])
+def test_ternary_saturated_words(gq, pattern):
+    """Planes of whole one-words: every word's popcount is 32 and every counter of the carry-save
+    grouping reaches its largest value.  K = 3072 leaves one of a block's four chunk groups idle.
+    Closed forms: P = 1s, N = 0 gives 2 popc(X) - k; N = 1s, P = 0 gives k - 2 popc(X); both set
+    gives 0."""
+    rows, k, batch = 100, 3072, 5
+    ones = np.full((rows, k // 32), 0xFFFFFFFF, np.uint32)
+    zeros = np.zeros_like(ones)
+    P, N = {"p_ones": (ones, zeros), "n_ones": (zeros, ones), "both_ones": (ones, ones)}[pattern]
+    kw = k // 32
+    X = np.stack([np.full(kw, 0xFFFFFFFF, np.uint32), np.zeros(kw, np.uint32), np.full(kw, 0xAAAAAAAA, np.uint32),
+                  np.full(kw, 0x55555555, np.uint32), wl.Rng(9).u32(kw)])
+    y = gq.ternary_bitplane_gemv(to_dev(P), to_dev(N), to_dev(X)).cpu().numpy()
+    assert np.array_equal(y, oracle.ternary_direct(P, N, X, rows, k, batch))
+    px = np.array([sum(bin(int(v)).count("1") for v in X[b]) for b in range(batch)], np.int64)
+    closed = {"p_ones": 2 * px - k, "n_ones": k - 2 * px, "both_ones": 0 * px}[pattern]
+    assert np.array_equal(y, np.repeat(closed[:, None], rows, axis=1).astype(np.int32))
 
 
 @pytest.mark.parametrize("batch", [1, 4, 16])
