@@ -98,6 +98,10 @@ __device__ __forceinline__ TileInfo tile_info(const gq_gemv_desc& single, const 
 
 __global__ void __launch_bounds__(256)
 act_prep_kernel(gq_gemv_desc single, const gq_gemv_desc* __restrict__ descs, int count, int* counter) {
+    // launched as a programmatic dependent of the work before it on the stream (often the previous
+    // GEMV, which still uses the workspace and the counter): everything is read and written after
+    // this wait, and only the launch and the thread blocks' start overlap that work's end
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // the GEMV grid may launch now; its griddepcontrol.wait still waits for this grid's writes
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const gq_gemv_desc d = (count == 0) ? single : descs[blockIdx.y];
@@ -196,6 +200,9 @@ q1_gemv_kernel(GemvArgs a) {
     // launched as a programmatic dependent of act_prep_kernel: its constants and the zeroed unit
     // counter are visible after this wait (a no-op when launched the ordinary way)
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the next call's constants launch may start; it waits for this whole grid before it reads or
+    // writes anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!active) return;
     int next_unit = 0;
     if (lane == 0) {
@@ -336,6 +343,21 @@ static cudaError_t gemv_grid(int total_tiles, int* grid, int* active_warps) {
     return cudaSuccess;
 }
 
+// act_prep_kernel as a programmatic dependent of the work before it on `s` (see the kernel).
+static cudaError_t launch_act_prep(int count, cudaStream_t s, const gq_gemv_desc& single,
+                                   const gq_gemv_desc* descs, int* counter) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(8, count > 0 ? count : 1);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, act_prep_kernel, single, descs, count, counter);
+}
+
 // The GEMV grid as a programmatic dependent launch of the act_prep_kernel just queued on `s`: its
 // thread blocks start (shared memory set-up, descriptor cache) while act_prep_kernel still runs.
 static cudaError_t launch_gemv_dependent(int grid, cudaStream_t s, const GemvArgs& args) {
@@ -363,8 +385,7 @@ cudaError_t launch_q1_gemv_persistent(const void* packed, const void* act, float
     if (e != cudaSuccess) return e;
     int* counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + gemv_workspace_bytes(n) - 16);
     gq_gemv_desc d{packed, act, y, workspace, rows, n, 0, act_format};
-    act_prep_kernel<<<dim3(8, 1), 256, 0, s>>>(d, nullptr, 0, counter);
-    e = cudaGetLastError();
+    e = launch_act_prep(0, s, d, nullptr, counter);
     if (e != cudaSuccess) return e;
     return launch_gemv_dependent(grid, s, GemvArgs{d, nullptr, 0, tiles, active, counter});
 }
@@ -375,8 +396,7 @@ cudaError_t launch_q1_gemv_grouped(const gq_gemv_desc* descs, int count, int tot
     cudaError_t e = gemv_grid(total_tiles, &grid, &active);
     if (e != cudaSuccess) return e;
     gq_gemv_desc none{nullptr, nullptr, nullptr, nullptr, 0, 128, 0, 0};
-    act_prep_kernel<<<dim3(8, count), 256, 0, s>>>(none, descs, count, counter);
-    e = cudaGetLastError();
+    e = launch_act_prep(count, s, none, descs, counter);
     if (e != cudaSuccess) return e;
     return launch_gemv_dependent(grid, s, GemvArgs{none, descs, count, total_tiles, active, counter});
 }
