@@ -30,7 +30,7 @@ namespace gq {
 namespace {
 
 constexpr int kWords = 32;                 // words per chunk row (1024 bits, 128 bytes)
-constexpr int kChunksPerCta = 4;           // K chunks per thread block, one warp group each
+constexpr int kChunksPerCta = 4;           // K chunks per thread block, one group of rt threads each
 constexpr int kChunkRowBytes = kWords * 4;
 
 struct TernLayout {
