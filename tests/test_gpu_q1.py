@@ -149,6 +149,38 @@ def test_grouped_equals_single_small(gq):
     assert gq.device_error() == 0
 
 
+def test_grouped_more_tiles_than_warps(gq):
+    """More 128-row tiles than the persistent grid has warps, so every warp takes several units
+    through the hand-out counter: every row of every matrix (ragged last tiles, several n, Q8_0
+    and f32 activations) equals the oracle bit for bit, and a second call over the same outputs
+    (counter and constants rebuilt) gives the same bits."""
+    import torch
+    sms = gq.lib().gq_probe_sm_count()
+    rng = wl.Rng(777)
+    shapes = [(20_001, 640), (100_005, 384), (40_077, 256), (120_033, 256), (30_001, 128), (70_003, 128)]
+    assert sum((r + 127) // 128 for r, _ in shapes) > 16 * sms     # more tiles than warps
+    items, want = [], []
+    for i, (rows, n) in enumerate(shapes):
+        w = wl.q1_0_weights(rng, rows, n, scales="page")
+        packed = gq.q1_0_pack(to_dev(w), rows, n)
+        y = torch.empty(rows, dtype=torch.float32, device="cuda")
+        if i == 4:
+            x = _act_f32(rng, n, "normal")
+            items.append((packed, to_dev(x), y, rows, n))
+            want.append(oracle.q1_q8_gemv(w, _q8_0_blocks(x, n), rows, n))
+        else:
+            a = wl.q8_0_acts(rng, 1, n, quants="page")
+            items.append((packed, to_dev(a), y, rows, n))
+            want.append(oracle.q1_q8_gemv(w, a, rows, n))
+    g = gq.GroupedGemv(items)
+    for call in range(2):
+        g()
+        torch.cuda.synchronize()
+        for (_, _, y, rows, n), wv in zip(items, want):
+            assert_same_bits(y.cpu().numpy(), wv, f"many tiles {rows}x{n}, call {call}")
+    assert gq.device_error() == 0
+
+
 def test_bitnet_sweep_full_size_sampled(gq):
     """The BitNet-2B decode sweep (30 layers x 7 matrices, 334.5 MB of Q1_0 weights) in one grouped
     launch, as the benchmark times it: every matrix's output equals its single-matrix GEMV bit for
