@@ -65,7 +65,8 @@ def test_block_q8_full_size_sampled(gq, m):
 # ----------------------------------------------------------------------------- ternary
 
 @pytest.mark.parametrize("rows,k,batch,pz", [(1, 1024, 1, 0.4), (130, 2048, 3, 0.4), (300, 4096, 16, 0.0),
-                                             (129, 1024, 17, 1.0), (64, 8192, 64, 0.4), (1000, 4096, 1, 0.4)])
+                                             (129, 1024, 17, 1.0), (64, 8192, 64, 0.4), (1000, 4096, 1, 0.4),
+                                             (300, 5120, 1, 0.4)])
 def test_ternary_exact(gq, rows, k, batch, pz):
     P, N, X = wl.ternary_inputs(wl.Rng(rows + k + batch), rows, k, batch, p_zero=pz)
     y = gq.ternary_bitplane_gemv(to_dev(P), to_dev(N), to_dev(X)).cpu().numpy()
